@@ -1,0 +1,401 @@
+"""Pins of the CPU oracle against things other than itself: hand-derived closed forms,
+invariants the mathematics fixes, library routines, brute force on tiny inputs, and the
+values the pages print (tests/golden/page_values.json).
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped term, a wrong sign
+or index, a transposed operand, a swapped axis) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as WL
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_values.json")))
+
+
+# ----------------------------------------------------------------------------
+# QK-Norm
+# ----------------------------------------------------------------------------
+def test_rmsnorm_hand_example():
+    # x = [3, 4]: mean square 12.5, so y = x / sqrt(12.5) * w (eps = 0).
+    y = O.rms_norm(np.array([3.0, 4.0]), np.array([2.0, 0.5]), 0.0)
+    np.testing.assert_allclose(y, [1.6970562748477140, 0.5656854249492380], rtol=1e-15)
+
+
+def test_rmsnorm_eps_inside_sqrt():
+    # x = [1, 1], eps = 1: 1 / sqrt(1 + 1) = 0.7071...
+    y = O.rms_norm(np.array([1.0, 1.0]), np.ones(2), 1.0)
+    np.testing.assert_allclose(y, [0.7071067811865476] * 2, rtol=1e-15)
+    # all-zero row stays finite and zero
+    assert np.all(O.rms_norm(np.zeros(8), np.ones(8), 1e-6) == 0.0)
+
+
+def test_rmsnorm_unit_rms_closed_form():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((5, 3, 128)) * 7.0
+    eps = 1e-6
+    y = O.rms_norm(x, np.ones(128), eps)
+    ms = np.mean(x * x, axis=-1)
+    rms_y = np.sqrt(np.mean(y * y, axis=-1))
+    np.testing.assert_allclose(rms_y, np.sqrt(ms / (ms + eps)), rtol=1e-14)
+
+
+def test_rmsnorm_scale_invariance():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((4, 128))
+    w = 1 + 0.1 * rng.standard_normal(128)
+    np.testing.assert_allclose(O.rms_norm(37.0 * x, w, 0.0), O.rms_norm(x, w, 0.0), rtol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# RoPE
+# ----------------------------------------------------------------------------
+ROPE1D = O.Rope("1d", base=100.0)
+
+
+def test_rope_hand_examples_1d():
+    # D = 4, base 100: inv = [1, 100^(-2/4)] = [1, 0.1].
+    x = np.eye(4)[:, None, :]                      # 4 "tokens" = unit vectors e0..e3
+    pos = np.array([[1], [2], [1], [2]])
+    y = O.rope_apply(x, pos, ROPE1D)[:, 0, :]
+    # e0 at pos 1: pair (0, 2), angle 1 -> y0 = cos 1, y2 = sin 1
+    np.testing.assert_allclose(y[0], [0.5403023058681398, 0, 0.8414709848078965, 0], atol=1e-16)
+    # e1 at pos 2: pair (1, 3), angle 0.2 -> y1 = cos .2, y3 = sin .2
+    np.testing.assert_allclose(y[1], [0, 0.9800665778412416, 0, 0.19866933079506122], atol=1e-16)
+    # e2 at pos 1 (second half of pair 0): y0 = -sin 1, y2 = cos 1
+    np.testing.assert_allclose(y[2], [-0.8414709848078965, 0, 0.5403023058681398, 0], atol=1e-16)
+    # e3 at pos 2: y1 = -sin .2, y3 = cos .2
+    np.testing.assert_allclose(y[3], [0, -0.19866933079506122, 0, 0.9800665778412416], atol=1e-16)
+
+
+def test_rope_position_zero_is_identity():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 2, 128))
+    for rope, n_axes in ((O.Rope("1d", 1e6), 1), (O.Rope("sections", 1.11588e7, (16,) * 4), 4),
+                         (O.Rope("2d", 1e6), 2)):
+        np.testing.assert_array_equal(O.rope_apply(x, np.zeros((3, n_axes), int), rope), x)
+
+
+def test_rope_preserves_pair_norms():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((7, 3, 128))
+    pos = rng.integers(0, 40000, size=(7, 1))
+    y = O.rope_apply(x, pos, O.Rope("1d", 1e6))
+    n_in = x[..., :64] ** 2 + x[..., 64:] ** 2
+    n_out = y[..., :64] ** 2 + y[..., 64:] ** 2
+    np.testing.assert_allclose(n_out, n_in, rtol=1e-13)
+
+
+def test_rope_relative_position_property():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((1, 1, 128))
+    k = rng.standard_normal((1, 1, 128))
+    rope = O.Rope("1d", 1e6)
+    dots = []
+    for p in (0, 5, 333, 4096):
+        qr = O.rope_apply(q, [[p + 17]], rope)
+        kr = O.rope_apply(k, [[p]], rope)
+        dots.append(float(np.sum(qr * kr)))
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-11)
+
+
+def test_xdrope_sections_pick_axes():
+    # D = 8, four sections of one frequency each, base 16: inv = 16^(-j/4) = 1, 1/2, 1/4, 1/8.
+    # Positions (1, 2, 4, 8) on the four axes give angle 1 for every pair.
+    rope = O.Rope("sections", base=16.0, sections=(1, 1, 1, 1))
+    x = np.zeros((1, 1, 8)); x[..., :4] = 1.0
+    y = O.rope_apply(x, [[1, 2, 4, 8]], rope)[0, 0]
+    np.testing.assert_allclose(y[:4], [math.cos(1.0)] * 4, rtol=1e-15)
+    np.testing.assert_allclose(y[4:], [math.sin(1.0)] * 4, rtol=1e-15)
+
+
+def test_xdrope_equal_axes_is_1d():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((6, 2, 128))
+    p = rng.integers(0, 600, size=(6, 1))
+    a = O.rope_apply(x, np.repeat(p, 4, axis=1), O.Rope("sections", 1.11588e7, (16,) * 4))
+    b = O.rope_apply(x, p, O.Rope("1d", 1.11588e7))
+    np.testing.assert_allclose(a, b, rtol=0, atol=0)
+
+
+def test_rope_2d_hand_example_and_axes():
+    # D = 8 -> halves of 4, base 1e6: inv (width 4) = [1, 1e-3].
+    rope = O.Rope("2d", 1e6)
+    x = np.zeros((1, 1, 8)); x[0, 0, 4] = 1.0      # first element of the column half
+    y = O.rope_apply(x, [[5, 1]], rope)[0, 0]       # row 5, col 1
+    np.testing.assert_allclose(y, [0, 0, 0, 0, math.cos(1.0), 0, math.sin(1.0), 0], atol=1e-16)
+    x = np.zeros((1, 1, 8)); x[0, 0, 1] = 1.0      # second frequency of the row half
+    y = O.rope_apply(x, [[5, 1]], rope)[0, 0]
+    np.testing.assert_allclose(y, [0, math.cos(5e-3), 0, math.sin(5e-3), 0, 0, 0, 0], atol=1e-16)
+
+
+def test_rope_2d_equal_axes_is_per_half_1d():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((5, 3, 72))
+    p = rng.integers(0, 92, size=(5, 1))
+    a = O.rope_apply(x, np.repeat(p, 2, axis=1), O.Rope("2d", 1e6))
+    one = O.Rope("1d", 1e6)
+    b = np.concatenate([O.rope_apply(x[..., :36], p, one), O.rope_apply(x[..., 36:], p, one)], -1)
+    np.testing.assert_allclose(a, b, rtol=0, atol=0)
+
+
+def test_norm_rope_order():
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((4, 2, 128))
+    pos = rng.integers(0, 1000, size=(4, 1))
+    rope = O.Rope("1d", 1e6)
+    ones = np.ones(128)
+    a = O.qk_transform(x, pos, ones, 1e-6, rope, norm_after_rope=False)
+    b = O.qk_transform(x, pos, ones, 1e-6, rope, norm_after_rope=True)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)   # RoPE keeps the RMS
+    w = 1 + 0.1 * rng.standard_normal(128)
+    a = O.qk_transform(x, pos, w, 1e-6, rope, norm_after_rope=False)
+    b = O.qk_transform(x, pos, w, 1e-6, rope, norm_after_rope=True)
+    assert np.max(np.abs(a - b)) > 1e-3                          # the flag matters
+
+
+# ----------------------------------------------------------------------------
+# bf16 storage
+# ----------------------------------------------------------------------------
+def test_bf16_round_ties_to_even():
+    u = 2.0 ** -8
+    vals = [1 + u, 1 + 3 * u, -(1 + u), 1 + 0.9 * u, 1 + 1.1 * u, 0.0, 2.0 ** -20 * (1 + u)]
+    expect = [1.0, 1 + 4 * u, -1.0, 1.0, 1 + 2 * u, 0.0, 2.0 ** -20]
+    np.testing.assert_array_equal(O.bf16_round(vals), expect)
+
+
+def test_bf16_round_matches_library_on_fp32_inputs():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
+    # add exact ties: low 16 bits 0x8000
+    bits = x.view(np.uint32).copy()
+    bits[::7] = (bits[::7] & 0xFFFF0000) | 0x8000
+    x = bits.view(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.bf16_round(x.astype(np.float64)), ref)
+
+
+# ----------------------------------------------------------------------------
+# Attention
+# ----------------------------------------------------------------------------
+def test_attention_two_key_closed_form():
+    # D = 2, scale 1/sqrt(2).  q = [sqrt(2) ln 3, 0], k0 = 0, k1 = e0  ->  logits 0, ln 3
+    # -> p = [1/4, 3/4] -> o = v0/4 + 3 v1/4 = [0.25, 1.5].
+    q = np.array([[[math.sqrt(2) * math.log(3.0), 0.0]]])
+    K = np.array([[[0.0, 0.0], [1.0, 0.0]]])
+    V = np.array([[[1.0, 0.0], [0.0, 2.0]]])
+    o = O.attend(q, K, V, np.array([[True, True]]))
+    np.testing.assert_allclose(o[0, 0], [0.25, 1.5], rtol=1e-15)
+
+
+def test_attention_large_logits_stable():
+    # logits 1000 and 1000 + ln 3 must not overflow: same p = [1/4, 3/4].
+    q = np.array([[[1000.0, math.log(3.0)]]])
+    K = np.array([[[1.0, 0.0], [1.0, 1.0]]])
+    V = np.array([[[1.0, 0.0], [0.0, 2.0]]])
+    o = O.attend(q, K, V, np.array([[True, True]]), scale=1.0)
+    np.testing.assert_allclose(o[0, 0], [0.25, 1.5], rtol=1e-12)
+
+
+def _rand_case(seed, S=9, Hq=4, Hkv=2, D=8, W=12):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((S, Hq, D)), rng.standard_normal((Hkv, W, D)),
+            rng.standard_normal((Hkv, W, D)))
+
+
+def test_attention_brute_force_tiny():
+    # Independent formulation: direct ratio sum_j e^{s_j} v_j / sum_j e^{s_j}, scalar loops,
+    # no max subtraction, math.fsum.
+    q, K, V = _rand_case(12)
+    S, Hq, D = q.shape
+    allowed = O.prefill_mask(S, "causal")
+    allowed = np.concatenate([allowed, np.zeros((S, K.shape[1] - S), bool)], axis=1)
+    o = O.attend(q, K, V, allowed)
+    for i in range(S):
+        for h in range(Hq):
+            g = h // 2
+            w = []
+            for j in range(i + 1):
+                s = math.fsum(q[i, h, d] * K[g, j, d] for d in range(D)) / math.sqrt(D)
+                w.append(math.exp(s))
+            den = math.fsum(w)
+            for d in range(D):
+                num = math.fsum(w[j] * V[g, j, d] for j in range(i + 1))
+                assert abs(o[i, h, d] - num / den) <= 1e-13 * (1 + abs(num / den))
+
+
+def test_softmax_rows_sum_to_one_and_mask_is_honoured():
+    # V = identity rows: o[i] equals the probability row itself.
+    rng = np.random.default_rng(13)
+    S, D = 10, 10
+    q = rng.standard_normal((S, 1, D)) * 3
+    K = rng.standard_normal((1, S, D))
+    V = np.eye(S)[None]
+    for kind, seg in (("causal", None), ("full", None), ("segment", [0, 0, 0, 1, 1, 2, 2, 2, 2, 3])):
+        p = O.prefill(q, K, V, S, kind, seg)[:, 0, :]
+        np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-14)
+        assert np.all(p >= 0)
+        assert np.all(p[~O.prefill_mask(S, kind, seg)] == 0.0)
+
+
+def test_logit_shift_invariance():
+    rng = np.random.default_rng(14)
+    q = rng.standard_normal((3, 1, 6))
+    K = rng.standard_normal((1, 5, 6))
+    V = rng.standard_normal((1, 5, 4))
+    # append a constant feature: every logit of a row shifts by the same c
+    q2 = np.concatenate([q, np.full((3, 1, 1), 2.5)], axis=-1)
+    K2 = np.concatenate([K, np.ones((1, 5, 1))], axis=-1)
+    allowed = np.ones((3, 5), bool)
+    np.testing.assert_allclose(O.attend(q2, K2, V, allowed, scale=1.0),
+                               O.attend(q, K, V, allowed, scale=1.0), rtol=1e-13)
+
+
+def test_causal_row0_and_uniform_v():
+    q, K, V = _rand_case(15)
+    o = O.prefill(q, K, V, q.shape[0], "causal")
+    for h in range(q.shape[1]):
+        np.testing.assert_array_equal(o[0, h], V[h // 2, 0])        # only key 0 visible
+    Vc = np.full_like(V, -1.25)
+    np.testing.assert_allclose(O.prefill(q, K, Vc, q.shape[0], "causal"), -1.25, rtol=1e-15)
+
+
+def test_equal_keys_give_mean_of_values():
+    rng = np.random.default_rng(16)
+    K = np.repeat(rng.standard_normal((1, 1, 8)), 6, axis=1)
+    V = rng.standard_normal((1, 6, 8))
+    q = rng.standard_normal((1, 1, 8))
+    o = O.attend(q, K, V, np.ones((1, 6), bool))
+    np.testing.assert_allclose(o[0, 0], V[0].mean(axis=0), rtol=1e-14)
+
+
+def test_gqa_equals_mha_on_repeated_kv():
+    q, K, V = _rand_case(17, Hq=8, Hkv=2)
+    S = q.shape[0]
+    Krep, Vrep = np.repeat(K, 4, axis=0), np.repeat(V, 4, axis=0)   # repeat_interleave
+    np.testing.assert_allclose(O.prefill(q, K, V, S, "causal"), O.prefill(q, Krep, Vrep, S, "causal"),
+                               rtol=1e-15)
+
+
+def test_decode_equals_prefill_row():
+    q, K, V = _rand_case(18)
+    S = q.shape[0]
+    pre = O.prefill(q, K, V, S, "causal")
+    bound = GOLDEN["decode_vs_prefill_rel_err"]["value"]
+    for t in range(S):
+        dec = O.decode(q[t], K, V, t + 1)
+        rel = np.linalg.norm(dec - pre[t]) / np.linalg.norm(pre[t])
+        assert rel <= bound * 1e-6                                   # far inside the page's 3.0e-7
+
+
+def test_segment_mask_equals_separate_windows_and_is_permutation_invariant():
+    rng = np.random.default_rng(19)
+    seg = np.array([0, 0, 0, 1, 1, 1, 1, 2, 2])
+    S = seg.size
+    q = rng.standard_normal((S, 2, 8)); K = rng.standard_normal((2, S, 8)); V = rng.standard_normal((2, S, 8))
+    o = O.prefill(q, K, V, S, "segment", seg)
+    for w in range(3):
+        idx = np.nonzero(seg == w)[0]
+        ow = O.prefill(q[idx], K[:, idx], V[:, idx], idx.size, "full")
+        np.testing.assert_allclose(o[idx], ow, rtol=1e-13, atol=1e-15)
+    perm = np.array([2, 0, 1, 5, 3, 6, 4, 8, 7])                     # permute inside windows
+    op = O.prefill(q[perm], K[:, perm], V[:, perm], S, "segment", seg[perm])
+    np.testing.assert_allclose(op, o[perm], rtol=1e-13, atol=1e-15)
+    # a single segment is full attention
+    np.testing.assert_allclose(O.prefill(q, K, V, S, "segment", np.zeros(S, int)),
+                               O.prefill(q, K, V, S, "full"), rtol=0, atol=0)
+
+
+def test_cache_append_slots_and_storage():
+    rng = np.random.default_rng(20)
+    T, Hq, Hkv, D, W = 3, 4, 2, 8, 6
+    q = rng.standard_normal((T, Hq, D)); k = rng.standard_normal((T, Hkv, D)); v = rng.standard_normal((T, Hkv, D))
+    ck = np.full((Hkv, W, D), 7.0); cv = np.full((Hkv, W, D), 7.0)
+    slot = np.array([4, 0, 2])
+    rope = O.Rope("1d", 1e6)
+    qr = O.cache_append(q, k, v, [[3], [4], [5]], slot, None, None, 1e-6, rope, False, ck, cv, "bf16")
+    np.testing.assert_allclose(qr, O.rope_apply(q, [[3], [4], [5]], rope))
+    for t in range(T):
+        np.testing.assert_array_equal(cv[:, slot[t]], O.bf16_round(v[t]))
+        np.testing.assert_array_equal(ck[:, slot[t]], O.bf16_round(O.rope_apply(k, [[3], [4], [5]], rope)[t]))
+    assert np.all(ck[:, [1, 3, 5]] == 7.0) and np.all(cv[:, [1, 3, 5]] == 7.0)   # other slots untouched
+    with pytest.raises(IndexError):
+        O.cache_append(q[:1], k[:1], v[:1], [[0]], [W], None, None, 1e-6, rope, False, ck, cv, "f32")
+
+
+# ----------------------------------------------------------------------------
+# lm_head + argmax
+# ----------------------------------------------------------------------------
+def test_lm_logits_against_exact_sums_and_bf16_widening():
+    rng = np.random.default_rng(21)
+    W = WL.f32_to_bf16_bits(rng.standard_normal((50, 16)).astype(np.float32) * 0.02)
+    h = rng.standard_normal(16)
+    z = O.lm_logits(h, W, 50)
+    Wf = WL.bf16_bits_to_f32(W).astype(np.float64)
+    for v in range(50):
+        assert abs(z[v] - math.fsum(Wf[v, i] * h[i] for i in range(16))) <= 1e-15
+    one = np.array([[0x3F80, 0xC000]], dtype=np.uint16)              # 1.0, -2.0
+    np.testing.assert_array_equal(O.lm_logits(np.array([3.0, 0.5]), one, 1), [2.0])
+
+
+def test_argmax_ties_lowest_id_vocab_clamp_and_last_row():
+    H = 8
+    W = np.zeros((20, H), dtype=np.float32)
+    h = np.ones(H)
+    W[7] = 1.0; W[3] = 1.0                                             # tie: 3 and 7
+    ids, mx, mg = O.lmhead_argmax(h, W, 20)
+    assert ids[0] == 3 and mx[0] == 8.0 and mg[0] == 0.0
+    W[19] = 2.0                                                        # last row wins...
+    assert O.lmhead_argmax(h, W, 20)[0][0] == 19
+    assert O.lmhead_argmax(h, W, 19)[0][0] == 3                        # ...unless clamped away
+
+
+# ----------------------------------------------------------------------------
+# Page-printed values: workload layouts
+# ----------------------------------------------------------------------------
+def test_image_span_layout_matches_pages():
+    g = GOLDEN["image_span"]["value"]
+    pos = WL.image_span_positions(0, g["grid_rows"], g["grid_cols"], 0)
+    assert pos.shape[0] == g["rows"] == 1 + 16 * 17 + 1
+    vt = GOLDEN["visual_token_count"]["value"]
+    gh, gw = vt["patch_grid"]; m = vt["merge_size"]
+    assert (gh // m) * (gw // m + 1) + 2 == vt["tokens"] == pos.shape[0]
+    full = WL.image_span_positions(20, 16, 16, 218)
+    assert full.shape == (512, 4)
+    assert np.array_equal(full[:20], np.repeat(np.arange(20)[:, None], 4, 1))
+    assert np.all(full[:, 0] == np.arange(512))                      # axis 0 is the sequence position
+    assert tuple(full[21]) == (21, 0, 0, 0) and tuple(full[21 + 16]) == (37, 0, 16, 0)
+    assert tuple(full[292]) == (292, 15, 16, 0)
+
+
+def test_vision_layout_matches_pages():
+    g = GOLDEN["vision_grid"]["value"]
+    lay = WL.vision_window_layout()
+    assert lay.pos_rc.shape[0] == g["patches"] == g["patch_rows"] * g["patch_cols"]
+    assert g["merged_tokens"] == g["patches"] // 4
+    assert sum(lay.window_sizes) == g["patches"]
+    assert lay.window_sizes == [224] * 5 + [168]
+    assert np.array_equal(np.sort(lay.slot), np.arange(1288))
+    assert np.array_equal(lay.row_of_slot[lay.slot], np.arange(1288))
+    assert np.all(np.diff(lay.segment) >= 0)
+    # every window spans 16 patch columns (8 merged) except the ragged last one
+    for w in range(6):
+        toks = lay.row_of_slot[lay.segment == w]
+        cols = lay.pos_rc[toks, 1]
+        assert cols.min() == 16 * w and cols.max() == min(16 * w + 15, 91)
+
+
+def test_qwen3_constants_match_pages():
+    g = GOLDEN["qwen3_geometry"]["value"]
+    assert (WL.QWEN3_N_Q_HEADS, WL.QWEN3_N_KV_HEADS, WL.QWEN3_HEAD_DIM, WL.QWEN3_HIDDEN,
+            WL.QWEN3_LAYERS, WL.QWEN3_VOCAB) == (g["n_q_heads"], g["n_kv_heads"], g["head_dim"],
+                                                g["hidden"], g["layers"], g["vocab"])
+    assert WL.QWEN3_ROPE_THETA == g["rope_theta"] and WL.QWEN3_RMS_EPS == g["rms_eps"]
+    assert GOLDEN["xdrope"]["value"]["effective_base"] == WL.XDROPE_BASE
+    assert tuple(GOLDEN["xdrope"]["value"]["sections"]) == WL.XDROPE_SECTIONS
