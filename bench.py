@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the KV-cache GQA attention step on the Qwen3-0.6B-shaped workload.
+
+One benchmark step = one whole generation job through the C ABI:
+  * prefill: fused QK-Norm+RoPE+cache append of 512 tokens into 28 layer caches, then causal
+    flash prefill attention of all 28 layers, then the lm_head argmax;
+  * 256 decode steps, each: append of the new token into the 28 caches, split-KV decode
+    attention of the 28 layers over the 1024-slot window, lm_head argmax (151936 x 1024 bf16).
+Inputs are synthetic (seeded), resident in HBM; the job is captured once as a CUDA graph.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead (the only
+reference implementation for this path) on a bounded sample of the same job.
+"""
+import os
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")     # the CPU oracle baseline runs single-threaded
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV GB/s + tokens/s; prefill-attn TFLOPS; % of GB300 roofline"
+UNIT = "tokens/s"
+LAYERS, PROMPT, STEPS, WINDOW = 28, 512, 256, 1024
+HQ, HKV, D, HIDDEN, VOCAB = 16, 8, 128, 1024, 151936
+TOKENS_PER_JOB = STEPS + 1          # one greedy token after prefill + one per decode step
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work of one job
+# ----------------------------------------------------------------------------
+def append_bytes(tokens):
+    # fp32 q, k, v in; bf16 q_out, k, v out
+    return tokens * ((HQ + 2 * HKV) * D * 4 + (HQ + 2 * HKV) * D * 2)
+
+
+def prefill_flops():
+    return LAYERS * HQ * 4 * D * (PROMPT * (PROMPT + 1) // 2)
+
+
+def decode_bytes(L):
+    kv = LAYERS * HKV * L * D * 2 * 2
+    return kv + LAYERS * HQ * D * (2 + 4)          # + bf16 q in, fp32 out
+
+
+def lmhead_bytes(B=1):
+    return VOCAB * HIDDEN * 2 + B * (HIDDEN * 4 + 4)
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (one process per GPU, independent replicas: weak scaling)
+# ----------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max(value, world, device=None):
+    """Max of a float over ranks (identity when world == 1)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank, world, max_seconds):
+    """Whole-job throughput: units processed by all ranks / the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def gpu_smi_id(local_rank):
+    """nvidia-smi identifier of CUDA device `local_rank` (its UUID: device indices differ from
+    nvidia-smi's when CUDA_VISIBLE_DEVICES remaps them)."""
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x for x in vis.split(",") if x.strip()]
+        return ids[local_rank] if local_rank < len(ids) else str(local_rank)
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu, self.proc, self.file = gpu_index, None, None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush(); self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.count(",") >= 7]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0])); mx.append(float(r[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[4:8]):
+                if val.strip() == "Active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# the GPU job
+# ----------------------------------------------------------------------------
+class Qwen3Job:
+    """Resident inputs, caches and workspaces of one generation job; `record(stream)` enqueues
+    the job's 771 kernel launches (optionally bracketing each with timing events)."""
+
+    def __init__(self, seed=0):
+        import torch
+        import kv_cache_gqa_gb300 as K
+        self.K, self.torch = K, torch
+        dev = "cuda"
+        g = torch.Generator(device=dev); g.manual_seed(seed)
+        rn = lambda *s: torch.randn(s, device=dev, generator=g)
+        self.q, self.k, self.v = rn(LAYERS, PROMPT, HQ, D), rn(LAYERS, PROMPT, HKV, D), rn(LAYERS, PROMPT, HKV, D)
+        self.dq, self.dk, self.dv = rn(STEPS, LAYERS, 1, HQ, D), rn(STEPS, LAYERS, 1, HKV, D), rn(STEPS, LAYERS, 1, HKV, D)
+        self.qw = 1 + 0.1 * rn(LAYERS, D)
+        self.kw = 1 + 0.1 * rn(LAYERS, D)
+        self.h = rn(TOKENS_PER_JOB, 1, HIDDEN)
+        self.W = (0.02 * rn(VOCAB, HIDDEN)).to(torch.bfloat16)
+        self.kc = torch.zeros((LAYERS, HKV, WINDOW, D), device=dev, dtype=torch.bfloat16)
+        self.vc = torch.zeros_like(self.kc)
+        self.cache = K.KVCache(self.kc, self.vc)
+        self.rope = K.Rope("1d", 1e6)
+        self.q_pre = torch.empty((LAYERS, PROMPT, HQ, D), device=dev, dtype=torch.bfloat16)
+        self.out_pre = torch.empty((LAYERS, PROMPT, HQ, D), device=dev)
+        self.q_dec = torch.empty((STEPS, LAYERS, 1, HQ, D), device=dev, dtype=torch.bfloat16)
+        self.out_dec = torch.empty((STEPS, LAYERS, HQ, D), device=dev)
+        self.pre_slot = np.arange(PROMPT, dtype=np.int32)[None]
+        self.pre_slot_d = torch.from_numpy(self.pre_slot).to(dev)
+        self.pre_pos_d = torch.arange(PROMPT, dtype=torch.int32, device=dev)[None, :, None].contiguous()
+        self.step_slot = [np.array([[PROMPT + s]], np.int32) for s in range(STEPS)]
+        self.step_slot_d = torch.arange(PROMPT, PROMPT + STEPS, dtype=torch.int32, device=dev).view(STEPS, 1, 1)
+        self.len_host = [np.full(LAYERS, PROMPT + s + 1, np.int32) for s in range(STEPS)]
+        self.len_d = torch.from_numpy(np.stack(self.len_host)).to(dev)
+        self.ids = torch.empty((TOKENS_PER_JOB,), dtype=torch.int32, device=dev)
+        self.dec_ws = torch.zeros(K.decode_workspace_bytes(LAYERS, HKV, HQ, WINDOW, D), dtype=torch.uint8, device=dev)
+        self.lm_ws = torch.zeros(K.lmhead_workspace_bytes(1), dtype=torch.uint8, device=dev)
+        self.events = None
+
+    def _ev(self, key):
+        if self.events is not None:
+            e = self.torch.cuda.Event(enable_timing=True)
+            e.record()
+            self.events.setdefault(key, []).append(e)
+
+    def record(self, with_events=False):
+        K = self.K
+        self.events = {} if with_events else None
+        c = self.cache
+        self._ev("t0")
+        K.kv_cache_append_rope_qknorm(self.q, self.k, self.v, self.pre_pos_d, self.pre_slot_d, self.pre_slot, c,
+                                      self.q_pre, self.rope, q_norm_w=self.qw, k_norm_w=self.kw, eps=1e-6,
+                                      norm_inst_stride=D)
+        self._ev("append_pre")
+        K.kv_attn_prefill(self.q_pre, c, self.out_pre, mask="causal")
+        self._ev("prefill")
+        K.lmhead_argmax(self.h[0], self.W, self.ids[0:1], self.lm_ws)
+        self._ev("lm_head")
+        for s in range(STEPS):
+            K.kv_cache_append_rope_qknorm(self.dq[s], self.dk[s], self.dv[s], self.step_slot_d[s:s + 1],
+                                          self.step_slot_d[s], self.step_slot[s], c, self.q_dec[s], self.rope,
+                                          q_norm_w=self.qw, k_norm_w=self.kw, eps=1e-6, norm_inst_stride=D)
+            self._ev("append_dec")
+            K.kv_attn_decode(self.q_dec[s, :, 0], c, self.len_d[s], self.len_host[s], self.out_dec[s], self.dec_ws)
+            self._ev("decode")
+            K.lmhead_argmax(self.h[s + 1], self.W, self.ids[s + 1:s + 2], self.lm_ws)
+            self._ev("lm_head")
+
+    def kernel_times_ms(self):
+        """Per-kind launch durations (ms) of the last replay, from consecutive events."""
+        order = ["t0", "append_pre", "prefill", "lm_head"] + ["append_dec", "decode", "lm_head"] * STEPS
+        seq, idx = [], {}
+        for key in order:
+            i = idx.get(key, 0); idx[key] = i + 1
+            seq.append((key, self.events[key][i]))
+        out = {}
+        for (k0, e0), (k1, e1) in zip(seq[:-1], seq[1:]):
+            out.setdefault(k1, []).append(e0.elapsed_time(e1))
+        return out
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import kv_cache_gqa_gb300 as K
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    job = Qwen3Job(seed=rank)
+    stream = torch.cuda.Stream()
+    # eager warm-up (also initialises every kernel's attributes before capture)
+    with torch.cuda.stream(stream):
+        job.record()
+    torch.cuda.synchronize()
+    n0 = K.launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        job.record(with_events=True)
+    launches_per_job = K.launch_count() - n0
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(gpu_smi_id(local_rank))
+    clocks.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    max_ms = reduce_max(ms, world, device=torch.device("cuda", local_rank))
+    value = aggregate_throughput(TOKENS_PER_JOB * args.steps, world, max_ms / 1e3)
+    kt = job.kernel_times_ms()
+
+    # ---- end to end: inputs from pinned host memory, ids back to the host, every step ----
+    host_in = {n: getattr(job, n).cpu().pin_memory() for n in ("q", "k", "v", "dq", "dk", "dv", "h")}
+    ids_host = torch.empty_like(job.ids, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = ids_host.numel() * ids_host.element_size()
+
+    def e2e_step():
+        for n, t in host_in.items():
+            getattr(job, n).copy_(t, non_blocking=True)
+        graph.replay()
+        ids_host.copy_(job.ids, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world, device=torch.device("cuda", local_rank))
+    e2e_value = aggregate_throughput(TOKENS_PER_JOB * args.steps, world, e2e_ms / 1e3)
+
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        dec_ms = kt["decode"]
+        dec_bytes = [decode_bytes(PROMPT + s + 1) for s in range(STEPS)]
+        dec_gbs = sum(dec_bytes) / (sum(dec_ms) / 1e3) / 1e9
+        lm_ms = statistics.mean(kt["lm_head"])
+        lm_gbs = lmhead_bytes() / (lm_ms / 1e3) / 1e9
+        pre_ms = kt["prefill"][0]
+        pre_tf = prefill_flops() / (pre_ms / 1e3) / 1e12
+        app_ms = kt["append_pre"][0]
+        app_gbs = append_bytes(LAYERS * PROMPT) / (app_ms / 1e3) / 1e9
+        totals = {k: sum(v) for k, v in kt.items()}
+        dominant = max(totals, key=totals.get)
+        roof = {"kernel": "lmhead_argmax", "bound": "hbm", "achieved": round(lm_gbs, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(lm_gbs / hbm, 4), "traffic": lm_traffic(),
+                "algorithmic_bytes_per_launch": lmhead_bytes(), "avg_launch_us": round(lm_ms * 1e3, 2),
+                "peak_source": f"{peak_src} hbm_gbs"}
+        if dominant == "decode":
+            roof.update({"kernel": "kv_attn_decode", "achieved": round(dec_gbs, 1), "frac": round(dec_gbs / hbm, 4),
+                         "traffic": None, "algorithmic_bytes_per_launch": int(np.mean(dec_bytes)),
+                         "avg_launch_us": round(statistics.mean(dec_ms) * 1e3, 2)})
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "Qwen3-0.6B-shaped attention step: 28 layers x (512-token causal prefill + "
+                                   "256 decode steps), 1024-slot bf16 window, tied lm_head 151936x1024 bf16 argmax",
+                       "layers": LAYERS, "prompt": PROMPT, "decode_steps": STEPS, "window": WINDOW,
+                       "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "vocab": VOCAB, "batch": 1,
+                       "step": "one whole job (prefill + 256 decode steps) as one CUDA graph replay",
+                       "l2": "inputs larger than L2: the 311 MB lm_head table streams through the 129 MB L2 "
+                             "between decode steps"},
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": int(launches_per_job * args.steps),
+            "roofline": roof,
+            "kernels": {
+                "decode_attn": {"GB/s": round(dec_gbs, 1), "frac_hbm": round(dec_gbs / hbm, 4),
+                                "avg_launch_us": round(statistics.mean(dec_ms) * 1e3, 2)},
+                "prefill_attn": {"TFLOP/s": round(pre_tf, 2), "frac_bf16": round(pre_tf / bf16, 4),
+                                 "launch_us": round(pre_ms * 1e3, 1), "flops": prefill_flops()},
+                "append_prefill": {"GB/s": round(app_gbs, 1), "frac_hbm": round(app_gbs / hbm, 4),
+                                   "launch_us": round(app_ms * 1e3, 1)},
+                "append_decode": {"avg_launch_us": round(statistics.mean(kt["append_dec"]) * 1e3, 2)},
+                "lm_head": {"GB/s": round(lm_gbs, 1), "frac_hbm": round(lm_gbs / hbm, 4),
+                            "avg_launch_us": round(lm_ms * 1e3, 2)},
+                "time_share": {k: round(v / sum(totals.values()), 4) for k, v in totals.items()},
+                "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": peak_src},
+            },
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(target_s=args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def lm_traffic():
+    """DRAM bytes per lm_head launch from the committed ncu summary, if it was taken on the
+    current kernel source (else null)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)["lmhead_argmax"]
+        src = open(os.path.join(ROOT, "kv_cache_gqa_gb300", "csrc", "lmhead.cu"), "rb").read()
+        if d.get("source_sha256") == hashlib.sha256(src).hexdigest():
+            return d["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the job
+# ----------------------------------------------------------------------------
+def oracle_sample_times(rows_pf=32, dec_layers=1, lm_rows=8192, seed=0):
+    """Time the oracle on one sample of each part of the job; return seconds per part and the
+    factor that scales each part to the whole job."""
+    import oracle as O
+    import workloads as WL
+    rng = np.random.default_rng(seed)
+    rope = O.Rope("1d", 1e6)
+    qw = 1 + 0.1 * rng.standard_normal(D); kw = 1 + 0.1 * rng.standard_normal(D)
+    q = rng.standard_normal((PROMPT, HQ, D)).astype(np.float32)
+    k = rng.standard_normal((PROMPT, HKV, D)).astype(np.float32)
+    v = rng.standard_normal((PROMPT, HKV, D)).astype(np.float32)
+    t = {}
+    ck = np.zeros((HKV, WINDOW, D)); cv = np.zeros((HKV, WINDOW, D))
+    t0 = time.perf_counter()
+    qr = O.cache_append(q, k, v, np.arange(PROMPT)[:, None], np.arange(PROMPT), qw, kw, 1e-6, rope, False, ck, cv, "bf16")
+    t["append_pre"] = time.perf_counter() - t0
+    rows = np.linspace(0, PROMPT - 1, rows_pf).astype(int)
+    allowed = np.zeros((rows.size, WINDOW), bool)
+    for i, r in enumerate(rows):
+        allowed[i, :r + 1] = True
+    t0 = time.perf_counter()
+    O.attend(qr[rows], ck, cv, allowed)
+    t["prefill"] = time.perf_counter() - t0
+    dq = rng.standard_normal((1, HQ, D)); dk = rng.standard_normal((1, HKV, D)); dv = rng.standard_normal((1, HKV, D))
+    t0 = time.perf_counter()
+    for _ in range(dec_layers):
+        qd = O.cache_append(dq, dk, dv, [[PROMPT + 128]], [PROMPT + 128], qw, kw, 1e-6, rope, False, ck, cv, "bf16")
+        O.decode(qd[0], ck, cv, PROMPT + 129)
+    t["decode_step"] = time.perf_counter() - t0
+    W = WL.f32_to_bf16_bits((0.02 * rng.standard_normal((lm_rows, HIDDEN))).astype(np.float32))
+    h = rng.standard_normal(HIDDEN)
+    t0 = time.perf_counter()
+    O.lmhead_argmax(h, W, lm_rows)
+    t["lm_head"] = time.perf_counter() - t0
+    scale = {"append_pre": LAYERS, "prefill": LAYERS * PROMPT / rows_pf,
+             "decode_step": STEPS * LAYERS / dec_layers, "lm_head": TOKENS_PER_JOB * VOCAB / lm_rows}
+    job_s = sum(t[p] * scale[p] for p in t)
+    sample = (f"per sample: 1 layer's 512-token append, {rows_pf} of 512 causal prefill rows x 16 heads, "
+              f"{dec_layers} layer decode step (append + attention at L=641), lm_head over {lm_rows} of "
+              f"{VOCAB} vocab rows; each part scaled to the full job (28 layers, 256 steps, 257 lm_head calls)")
+    return job_s, sample
+
+
+def cpu_baseline(target_s=12.0):
+    """Oracle (single thread, float64) on repeated bounded samples for ~target_s seconds."""
+    t_start = time.perf_counter()
+    jobs, sample = [], ""
+    while not jobs or time.perf_counter() - t_start < target_s:
+        js, sample = oracle_sample_times(seed=len(jobs))
+        jobs.append(js)
+    job_s = statistics.median(jobs)
+    return {"value": round(TOKENS_PER_JOB / job_s, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(jobs)} samples; {sample}", "job_seconds_extrapolated": round(job_s, 2),
+            "cpu_seconds": round(time.perf_counter() - t_start, 1)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        js, sample = oracle_sample_times(rows_pf=8, dec_layers=1, lm_rows=2048, seed=i)
+        if i >= args.warmup:
+            per_step.append(js)
+    job_s = statistics.median(per_step)
+    value = TOKENS_PER_JOB / job_s
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(job_s * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "Qwen3-0.6B-shaped attention step: 28 layers x (512-token causal prefill + "
+                                   "256 decode steps), 1024-slot bf16 window, tied lm_head 151936x1024 bf16 argmax"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kv_attn", choices=["kv_attn", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    from kv_cache_gqa_gb300 import build
+    build.build_library(verbose=False)
+    run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

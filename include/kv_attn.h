@@ -1,0 +1,223 @@
+/*
+ * kv_attn.h — C ABI of the GB300 KV-cache GQA attention step.
+ *
+ * Four compute entry points, one per step of the decoder's attention hot path:
+ *   kv_cache_append_rope_qknorm  QK-Norm + RoPE fused into the K/V cache write
+ *   kv_attn_prefill              parallel prefill attention over the cache
+ *   kv_attn_decode               single-token split-KV decode attention
+ *   lmhead_argmax                tied lm_head GEMV + greedy argmax
+ *
+ * Conventions shared by every call
+ *  - Ownership: every buffer belongs to the caller.  The library never allocates or
+ *    frees memory; pointers are borrowed for the duration of the stream work the call
+ *    enqueues (inputs are referenced, not copied: HunyuanOCR v1.0 ncnn port, section
+ *    five item 10).  Device pointers must stay valid until that work completes.
+ *  - Streams: every call is asynchronous on the caller's stream `stream` (a
+ *    cudaStream_t; NULL = legacy default stream).
+ *  - Errors: arguments are validated on the host before anything is launched; a
+ *    call that returns a status other than KVA_OK has enqueued nothing, so the cache
+ *    keeps its committed contents (the cache is only replaced after success:
+ *    HunyuanOCR v1.5 ncnn port, section 3.7).  Context overflow is rejected, never
+ *    wrapped (Youtu-VL-4B ncnn port, known limitations: sequences beyond the window
+ *    are refused).  Kernels also guard every index they write, so a host mirror that
+ *    disagrees with its device copy can drop a write but never corrupt memory.
+ *  - Layouts are row-major with the last dimension contiguous.  D = head_dim.
+ *    Token-major activations: q [.., T, Hq, D], k/v [.., T, Hkv, D], as a projection
+ *    emits them.  Cache instance: K [Hkv, capacity, D], V [Hkv, capacity, D]
+ *    (fixed-window cache of static shape: Youtu-VL-4B ncnn port, step 7).
+ *  - GQA: query head h reads KV head h / (Hq / Hkv) (repeat-interleave grouping:
+ *    Penguin-VL ncnn port, section 3 item 2).
+ *  - Alignment: every device pointer must be 16-byte aligned, and D must be a
+ *    multiple of 8 (vectorised 16-byte accesses); violations return KVA_EALIGN.
+ */
+#ifndef KV_ATTN_H_
+#define KV_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kva_stream; /* identical to cudaStream_t */
+
+typedef enum {
+  KVA_OK = 0,
+  KVA_EINVAL = 1,       /* bad shape, null pointer, unknown enum */
+  KVA_ECAPACITY = 2,    /* slot or length beyond the cache window */
+  KVA_EUNSUPPORTED = 3, /* valid request this build does not implement */
+  KVA_ECUDA = 4,        /* a CUDA launch or driver call failed */
+  KVA_EALIGN = 5,       /* pointer or stride not 16-byte aligned, D % 8 != 0 */
+  KVA_EWORKSPACE = 6    /* workspace missing or smaller than required */
+} kva_status;
+
+typedef enum { KVA_F32 = 0, KVA_BF16 = 1 } kva_dtype;
+
+typedef enum {
+  KVA_MASK_CAUSAL = 0,  /* key slot j visible to query slot i iff j <= i */
+  KVA_MASK_FULL = 1,    /* all S keys visible (bidirectional vision layers) */
+  KVA_MASK_SEGMENT = 2  /* block diagonal: j visible iff segment[j] == segment[i] */
+} kva_mask;
+
+typedef enum {
+  KVA_ROPE_NONE = 0,
+  KVA_ROPE_1D = 1,       /* rotate-half over D, every frequency uses position axis 0 */
+  KVA_ROPE_SECTIONS = 2, /* xdRoPE: frequency j uses the axis whose section holds j */
+  KVA_ROPE_2D = 3        /* two halves of D/2, each rotate-half; half b uses axis b */
+} kva_rope_kind;
+
+/* One cache: N instances (layers and/or sequences) of K and V, each
+ * [n_kv_heads, capacity, head_dim] of `dtype`, instance i starting at
+ * k + i * inst_stride elements (same for v).  inst_stride >= n_kv_heads*capacity*head_dim. */
+typedef struct {
+  void* k;
+  void* v;
+  kva_dtype dtype;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t capacity;
+  int64_t inst_stride;
+} kva_cache;
+
+/* Rotary embedding (rotate-half pairs (j, j + W/2) inside each rotated block of width W):
+ *   angle_j = pos[axis(j)] * base^(-2j/W),  y_j = x_j cos - x_{j+W/2} sin,
+ *   y_{j+W/2} = x_{j+W/2} cos + x_j sin.
+ *  1D (theta 1e6: Penguin-VL ncnn port, section 2.1), xdRoPE sections [16,16,16,16]
+ *  with effective base 1.11588e7 (HunyuanOCR v1.0 ncnn port, section five items 1, 3),
+ *  2D vision halves (Penguin-VL ncnn port, section 2.3).
+ *  n_axes: position ids per token (1 for 1D, number of sections, 2 for 2D). */
+typedef struct {
+  kva_rope_kind kind;
+  int32_t n_axes;
+  int32_t sections[4];
+  double base;
+} kva_rope;
+
+/* Per-head RMSNorm y = x / sqrt(mean(x^2) + eps) * w with w [D] float32 on the device
+ * (Penguin-VL ncnn port, sections 2.1, 4.2).  q_w == NULL and k_w == NULL: no norm.
+ * inst_stride: floats between the weights of consecutive instances (0 = shared).
+ * after_rope: 0 = norm then RoPE (Qwen3); 1 = RoPE then norm, the cache holding the
+ * normalised K (HunyuanOCR v1.0 ncnn port, section five item 2). */
+typedef struct {
+  const float* q_w;
+  const float* k_w;
+  int64_t inst_stride;
+  float eps;
+  int32_t after_rope;
+} kva_qknorm;
+
+/* ---------------------------------------------------------------------------------
+ * kv_cache_append_rope_qknorm
+ *   For each instance n < N and token t < T:
+ *     q_out[n,t,h,:] = f_q(q[n,t,h,:])                      h < Hq
+ *     K_n[g, slot[n,t], :] = store(f_k(k[n,t,g,:]))          g < Hkv
+ *     V_n[g, slot[n,t], :] = store(v[n,t,g,:])
+ *   f = QK-Norm and RoPE in the order `norm.after_rope` gives; store rounds to the cache
+ *   dtype (bf16: round to nearest even).  The runtime writes the new token's k/v into its
+ *   cache slot between the qkv and the attention step (Youtu-VL-4B ncnn port, step 6).
+ *  q       [N,T,Hq,D] of in_dtype (device);  k, v [N,T,Hkv,D] of in_dtype (device)
+ *  pos     [.., T, rope.n_axes] int32 (device); instance n reads pos + n*pos_inst_stride
+ *  slot    [.., T] int32 destination slot (device); instance n reads slot + n*slot_inst_stride
+ *  slot_host  host mirror of the slot values actually read (same strides), used to reject
+ *          slots outside [0, capacity) with KVA_ECAPACITY before launching
+ *  q_out   [N,T,Hq,D] of q_out_dtype (device), token order
+ *  Errors: KVA_EINVAL (N,T < 0, Hq % Hkv, sections not summing to D/2, D/2 odd for 2D),
+ *          KVA_ECAPACITY, KVA_EALIGN, KVA_EUNSUPPORTED (D > 256), KVA_ECUDA.
+ *  N == 0 or T == 0 is a no-op returning KVA_OK. */
+kva_status kv_cache_append_rope_qknorm(
+    const void* q, const void* k, const void* v, kva_dtype in_dtype,
+    int32_t N, int32_t T, int32_t n_q_heads,
+    const int32_t* pos, int64_t pos_inst_stride,
+    const int32_t* slot, int64_t slot_inst_stride, const int32_t* slot_host,
+    kva_qknorm norm, kva_rope rope,
+    void* q_out, kva_dtype q_out_dtype,
+    kva_cache cache, kva_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * kv_attn_prefill
+ *   Parallel prefill over cache slots 0..S-1 of each instance (Youtu-VL-4B ncnn port,
+ *   step 7; the fused flash-style form of MNN llm_demo walkthrough, section 5.1):
+ *     o_i = softmax_j( q_i . K[g, j] * scale, j visible to i ) . V[g, j]
+ *   softmax taken as max -> subtract -> exp -> sum -> divide (Youtu-VL-4B ncnn port,
+ *   implementation difficulty 3), accumulated in fp32.
+ *  q       [N,S,Hq,D] of q_dtype (device), token order.  The query of cache slot i is
+ *          q row r(i) = row_of_slot[i] (or i when row_of_slot == NULL), and its output
+ *          goes to out row r(i): this undoes a window permutation (the vision tower's
+ *          window_index grouping: Youtu-VL-4B ncnn port, step 3).
+ *  segment [S] int32 (device), non-decreasing window id per slot, for KVA_MASK_SEGMENT
+ *          (else NULL); segment_host: its host mirror (validated: non-decreasing).
+ *  scale   softmax scale; <= 0 selects 1/sqrt(D).
+ *  out     [N,S,Hq,D] float32 (device).
+ *  Errors: KVA_EINVAL, KVA_ECAPACITY (S > capacity), KVA_EALIGN, KVA_EUNSUPPORTED
+ *          (D > 256), KVA_ECUDA.  q_dtype must equal cache.dtype. */
+kva_status kv_attn_prefill(
+    const void* q, kva_dtype q_dtype, kva_cache cache,
+    int32_t N, int32_t S, int32_t n_q_heads, kva_mask mask,
+    const int32_t* segment, const int32_t* segment_host,
+    const int32_t* row_of_slot,
+    float scale, float* out, kva_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * kv_attn_decode
+ *   One query token per instance b against its first L_b cache slots (the new token's
+ *   slot included): o = softmax(q K[:L]^T * scale) V[:L] (Youtu-VL-4B ncnn port,
+ *   step 8; dattn consumes the whole cache window plus the mask).  Split-KV: the
+ *   L_b keys are cut into chunks processed by separate CTAs whose partial
+ *   (max, sum, acc) triples are merged by the last CTA of each (b, kv head).
+ *  q          [B,Hq,D] of q_dtype (device)
+ *  lengths    [B] int32 valid slots per instance (device); lengths_host: host mirror,
+ *             required (validation 1 <= L_b <= capacity, and chunk planning)
+ *  out        [B,Hq,D] float32 (device)
+ *  workspace  device scratch of at least kva_decode_workspace_size(...) bytes whose
+ *             first kva_decode_workspace_zero_bytes(B, Hkv) bytes are zero before the first
+ *             call; every call leaves them zero again.  Calls sharing one workspace must
+ *             not overlap on the GPU.
+ *  Errors: KVA_EINVAL, KVA_ECAPACITY, KVA_EALIGN, KVA_EWORKSPACE,
+ *          KVA_EUNSUPPORTED (D != 128), KVA_ECUDA.  B == 0 is a no-op. */
+kva_status kv_attn_decode(
+    const void* q, kva_dtype q_dtype, kva_cache cache,
+    const int32_t* lengths, const int32_t* lengths_host, int32_t B, int32_t n_q_heads,
+    float scale, float* out, void* workspace, size_t workspace_bytes, kva_stream stream);
+
+size_t kva_decode_workspace_size(int32_t B, int32_t n_kv_heads, int32_t n_q_heads,
+                                 int32_t max_len, int32_t head_dim);
+size_t kva_decode_workspace_zero_bytes(int32_t B, int32_t n_kv_heads);
+
+/* ---------------------------------------------------------------------------------
+ * lmhead_argmax
+ *   Greedy tied lm_head: z[b, v] = sum_k W[v, k] h[b, k] for v < V, ids[b] = argmax_v z[b, v]
+ *   (Youtu-VL-4B ncnn port, step 6: final-norm hidden dotted with every vocab row,
+ *   argmax only; HunyuanOCR v1.5 ncnn port, section 3.4: one [vocab, hidden] copy).
+ *   Ties go to the lowest id.  Only rows v < V are candidates; V > V_rows is rejected
+ *   (the vocab is clamped to the logits length: Penguin-VL ncnn port, section 4.1).
+ *   Logits accumulate in float32.  NaN inputs are outside the contract.
+ *  h          [B,H] float32 (device);  W [V_rows, H] of w_dtype (device)
+ *  out_ids    [B] int32 (device);  out_max [B] float32 max logit (device, nullable)
+ *  logits     [B,V] float32 (device, nullable): every logit, for inspection
+ *  workspace  device scratch of at least kva_lmhead_workspace_size(B) bytes, zero before the
+ *             first call; every call leaves it zero.  Calls sharing one workspace must not
+ *             overlap on the GPU.
+ *  Errors: KVA_EINVAL, KVA_EALIGN (H % 8), KVA_EWORKSPACE, KVA_ECUDA.  B == 0 is a no-op. */
+kva_status lmhead_argmax(
+    const float* h, const void* W, kva_dtype w_dtype,
+    int32_t B, int32_t H, int32_t V, int32_t V_rows,
+    int32_t* out_ids, float* out_max, float* logits,
+    void* workspace, size_t workspace_bytes, kva_stream stream);
+
+size_t kva_lmhead_workspace_size(int32_t B);
+
+/* ---------------------------------------------------------------------------------
+ * Introspection */
+const char* kva_strerror(kva_status s);
+/* Message describing the last non-OK status returned on the calling host thread. */
+const char* kva_last_error(void);
+/* Number of kernels this library has launched in this process (all threads). */
+uint64_t kva_launch_count(void);
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int32_t kva_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KV_ATTN_H_ */

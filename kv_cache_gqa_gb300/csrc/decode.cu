@@ -1,0 +1,344 @@
+// Kernel (c): split-KV single-token decode attention over the fixed-window cache.
+//
+// Work unit = (chunk c, KV head g, instance b).  A CTA streams its chunk of the K and V
+// rows of head g through a 3-stage shared-memory ring filled by 1-D bulk async copies
+// (one elected thread issues them; completion is an mbarrier transaction count), and
+// serves all G = Hq/Hkv query heads of the group from each staged tile, so each cache
+// byte is read from HBM once per step.  Scores stay in fp32 (log2 domain) with an
+// online softmax across stages; the partial (max, sum, acc) of every chunk goes to the
+// workspace and the last CTA to finish a (b, g) merges them - no CTA ever waits on
+// another.
+//
+// Method: one query against the valid prefix of the cache window (Youtu-VL-4B ncnn port,
+// step 8: each new token attends to the whole cache behind the mask), GQA by
+// repeat-interleave grouping (Penguin-VL ncnn port, section 3), softmax as
+// max/subtract/exp/sum/divide (Youtu-VL-4B ncnn port, implementation difficulty 3),
+// bf16 cache with fp32 accumulation (HunyuanOCR v1.5 ncnn port, section 3.7).
+#include <cfloat>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace kva {
+
+namespace {
+
+constexpr int D = DECODE_HEAD_DIM;
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
+constexpr int NSTAGE = 3;
+
+template <typename CacheT> struct DecodeTile;
+template <> struct DecodeTile<bf16_t> { static constexpr int KT = DECODE_SUBTILE_BF16; };
+template <> struct DecodeTile<float> { static constexpr int KT = DECODE_SUBTILE_F32; };
+
+__device__ __forceinline__ float load_q(const void* q, kva_dtype dt, int64_t i) {
+  if (dt == KVA_BF16)
+    return __uint_as_float(((uint32_t) reinterpret_cast<const uint16_t*>(q)[i]) << 16);
+  return reinterpret_cast<const float*>(q)[i];
+}
+
+// Convert one 16-byte chunk of cache row elements to floats.
+template <typename CacheT, int N> __device__ __forceinline__ void chunk_to_f32(uint4 w, float (&x)[N]);
+template <> __device__ __forceinline__ void chunk_to_f32<bf16_t, 8>(uint4 w, float (&x)[8]) {
+  x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+  x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+}
+template <> __device__ __forceinline__ void chunk_to_f32<float, 4>(uint4 w, float (&x)[4]) {
+  x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+  x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+}
+
+template <typename CacheT, int G>
+__global__ void __launch_bounds__(THREADS, 2)
+decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
+  constexpr int ES = ElemSize<CacheT>::value;
+  constexpr int KT = DecodeTile<CacheT>::KT;   // keys per stage
+  constexpr int ROWB = D * ES;                 // bytes per cache row
+  constexpr int TILEB = KT * ROWB;             // bytes per K (or V) stage
+  constexpr int CH = 16 / ES;                  // elements per 16-byte chunk
+  constexpr int NCH = 16 / CH;                 // chunks per lane in the QK phase (16 dims)
+  constexpr int KPW = KT / WARPS;              // keys per warp per stage
+  constexpr int QK_PASSES = KPW / 4;           // 4 keys per warp pass (8 lanes per key)
+  constexpr int SPL = KT / 32;                 // scores per lane in the softmax phase
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* sK = smem;
+  unsigned char* sV = smem + NSTAGE * TILEB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * NSTAGE * TILEB);  // [NSTAGE]
+  float* sS = reinterpret_cast<float*>(full + NSTAGE);               // [G][KT]
+  float* sP = sS + G * KT;                                           // [KT][G]
+  float* sAlpha = sP + KT * G;                                       // [G]
+  float* sML = sAlpha + G;                                           // [G][2]
+  __shared__ int s_flag;
+
+  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = a.lengths[b];
+  const int n_chunks = (L + a.chunk - 1) / a.chunk;
+  if (c >= n_chunks) return;
+  const int k0 = c * a.chunk;
+  const int k1 = min(L, k0 + a.chunk);
+  const int n_sub = (k1 - k0 + KT - 1) / KT;
+
+  const unsigned char* Kg = reinterpret_cast<const unsigned char*>(a.kc) +
+      ((int64_t)b * a.inst_stride + (int64_t)g * a.capacity * D) * ES;
+  const unsigned char* Vg = reinterpret_cast<const unsigned char*>(a.vc) +
+      ((int64_t)b * a.inst_stride + (int64_t)g * a.capacity * D) * ES;
+
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+    s_flag = 0;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE && s < n_sub; ++s) {
+      const int ks = k0 + s * KT;
+      const uint32_t bytes = (uint32_t)(min(KT, k1 - ks) * ROWB);
+      mbar_arrive_expect_tx(&full[s], 2 * bytes);
+      bulk_g2s(sK + s * TILEB, Kg + (int64_t)ks * ROWB, bytes, &full[s]);
+      bulk_g2s(sV + s * TILEB, Vg + (int64_t)ks * ROWB, bytes, &full[s]);
+    }
+  }
+
+  // Query registers for the QK phase: lane owns 16 dims, NCH chunks of CH elements at
+  // element offsets CH*(lane&7) + 8*CH*i.  Pre-scaled so dots are log2-domain logits.
+  const int l8 = lane & 7;
+  float qv[G][16];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    const int64_t qbase = ((int64_t)b * a.Hq + g * G + hh) * D;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i)
+#pragma unroll
+      for (int e = 0; e < CH; ++e)
+        qv[hh][i * CH + e] = load_q(a.q, q_dtype, qbase + CH * l8 + 8 * CH * i + e) * a.scale_log2;
+  }
+
+  float acc[G][4];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[hh][e] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;   // meaningful in warp hh < G only
+  bool timed_out = false;
+
+  for (int it = 0; it < n_sub; ++it) {
+    const int stage = it % NSTAGE;
+    const uint32_t parity = (uint32_t)((it / NSTAGE) & 1);
+    if (!mbar_wait_bounded(&full[stage], parity)) s_flag = 1;
+    __syncthreads();
+    if (s_flag) { timed_out = true; break; }
+    const int nk = min(KT, k1 - (k0 + it * KT));
+    const unsigned char* tK = sK + stage * TILEB;
+    const unsigned char* tV = sV + stage * TILEB;
+
+    // ---- S = q K^T (8 lanes per key, 4 keys per warp pass) ----
+#pragma unroll
+    for (int pass = 0; pass < QK_PASSES; ++pass) {
+      const int j = warp * KPW + pass * 4 + (lane >> 3);
+      float part[G];
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) part[hh] = 0.f;
+      if (j < nk) {
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          const uint4 w = *reinterpret_cast<const uint4*>(tK + j * ROWB + 16 * l8 + 128 * i);
+          float x[CH];
+          chunk_to_f32<CacheT, CH>(w, x);
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+            for (int e = 0; e < CH; ++e) part[hh] = fmaf(qv[hh][i * CH + e], x[e], part[hh]);
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        float v = part[hh];
+        v += __shfl_xor_sync(FULL_MASK, v, 1);
+        v += __shfl_xor_sync(FULL_MASK, v, 2);
+        v += __shfl_xor_sync(FULL_MASK, v, 4);
+        if (l8 == 0) sS[hh * KT + j] = (j < nk) ? v : -INFINITY;
+      }
+    }
+    __syncthreads();
+
+    // ---- online softmax statistics: warp hh owns query head hh ----
+    if (warp < G) {
+      float s[SPL];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) { s[i] = sS[warp * KT + lane + 32 * i]; mx = fmaxf(mx, s[i]); }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, o));
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = exp2f(m_run - m_new);   // 0 on the first stage (m_run = -inf)
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) {
+        const float p = exp2f(s[i] - m_new);      // 0 for masked keys
+        sP[(lane + 32 * i) * G + warp] = p;
+        sum += p;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL_MASK, sum, o);
+      l_run = l_run * alpha + sum;
+      m_run = m_new;
+      if (lane == 0) sAlpha[warp] = alpha;
+    }
+    __syncthreads();
+
+    // ---- acc = acc * alpha + P V (lane owns 4 dims; warp owns KPW keys) ----
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      const float al = sAlpha[hh];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[hh][e] *= al;
+    }
+    const int jend = min(nk, (warp + 1) * KPW);
+    for (int j = warp * KPW; j < jend; ++j) {
+      float x[4];
+      if constexpr (ES == 2) {
+        const uint2 w = *reinterpret_cast<const uint2*>(tV + j * ROWB + 8 * lane);
+        x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+      } else {
+        const float4 w = *reinterpret_cast<const float4*>(tV + j * ROWB + 16 * lane);
+        x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+      }
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float p = sP[j * G + hh];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[hh][e] = fmaf(p, x[e], acc[hh][e]);
+      }
+    }
+    __syncthreads();   // stage consumed by every warp
+
+    if (tid == 0 && it + NSTAGE < n_sub) {
+      const int ks = k0 + (it + NSTAGE) * KT;
+      const uint32_t bytes = (uint32_t)(min(KT, k1 - ks) * ROWB);
+      mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+      bulk_g2s(sK + stage * TILEB, Kg + (int64_t)ks * ROWB, bytes, &full[stage]);
+      bulk_g2s(sV + stage * TILEB, Vg + (int64_t)ks * ROWB, bytes, &full[stage]);
+    }
+  }
+
+  // ---- reduce the warps' partial accumulators (stage buffers are free now) ----
+  if (warp < G && lane == 0) {
+    sML[2 * warp] = timed_out ? NAN : m_run;
+    sML[2 * warp + 1] = timed_out ? NAN : l_run;
+  }
+  float* red = reinterpret_cast<float*>(smem);   // [WARPS][G][D]
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) red[(warp * G + hh) * D + 4 * lane + e] = acc[hh][e];
+  __syncthreads();
+
+  // Each (head hh, dim d) of the group is owned by one thread per iteration.
+  if (n_chunks == 1) {
+    for (int idx = tid; idx < G * D; idx += THREADS) {
+      const int hh = idx / D, d = idx % D;
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < WARPS; ++w) tot += red[(w * G + hh) * D + d];
+      a.out[((int64_t)b * a.Hq + g * G + hh) * D + d] = tot / sML[2 * hh + 1];
+    }
+    return;
+  }
+
+  for (int idx = tid; idx < G * D; idx += THREADS) {
+    const int hh = idx / D, d = idx % D;
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) tot += red[(w * G + hh) * D + d];
+    const int64_t pidx = ((int64_t)b * a.Hq + g * G + hh) * a.max_chunks + c;
+    a.part_acc[pidx * D + d] = tot;
+    if (d == 0) { a.part_ml[2 * pidx] = sML[2 * hh]; a.part_ml[2 * pidx + 1] = sML[2 * hh + 1]; }
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (tid == 0) {
+    const unsigned ticket = atomicAdd(&a.counters[b * a.Hkv + g], 1u);
+    s_last = (ticket == (unsigned)(n_chunks - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- last CTA of (b, g): merge the chunk partials ----
+  for (int idx = tid; idx < G * D; idx += THREADS) {
+    const int hh = idx / D, d = idx % D;
+    const int64_t p0 = ((int64_t)b * a.Hq + g * G + hh) * a.max_chunks;
+    float M = -INFINITY;
+    for (int cc = 0; cc < n_chunks; ++cc) M = fmaxf(M, __ldcg(&a.part_ml[2 * (p0 + cc)]));
+    float num = 0.f, den = 0.f;
+    for (int cc = 0; cc < n_chunks; ++cc) {
+      const float w = exp2f(__ldcg(&a.part_ml[2 * (p0 + cc)]) - M);
+      num = fmaf(w, __ldcg(&a.part_acc[(p0 + cc) * D + d]), num);
+      den = fmaf(w, __ldcg(&a.part_ml[2 * (p0 + cc) + 1]), den);
+    }
+    a.out[((int64_t)b * a.Hq + g * G + hh) * D + d] = num / den;
+  }
+  if (tid == 0) a.counters[b * a.Hkv + g] = 0u;   // ready for the next call
+}
+
+template <typename CacheT, int G>
+size_t decode_smem_bytes() {
+  constexpr int ES = ElemSize<CacheT>::value;
+  constexpr int KT = DecodeTile<CacheT>::KT;
+  return (size_t)2 * NSTAGE * KT * D * ES + sizeof(uint64_t) * NSTAGE +
+         sizeof(float) * (2 * G * KT + 3 * G) + 16;
+}
+
+template <typename CacheT, int G>
+cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
+  const size_t smem = decode_smem_bytes<CacheT, G>();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<CacheT, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(a.max_chunks, a.Hkv, a.B);
+  decode_kernel<CacheT, G><<<grid, THREADS, smem, s>>>(a, q_dtype);
+  return cudaGetLastError();
+}
+
+template <typename CacheT>
+cudaError_t launch_t(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_g<CacheT, 1>(a, q_dtype, s);
+    case 2: return launch_g<CacheT, 2>(a, q_dtype, s);
+    case 4: return launch_g<CacheT, 4>(a, q_dtype, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int decode_subtile(kva_dtype cache_dtype) {
+  return cache_dtype == KVA_BF16 ? DECODE_SUBTILE_BF16 : DECODE_SUBTILE_F32;
+}
+
+int decode_num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, kva_dtype q_dtype, kva_dtype cache_dtype,
+                          cudaStream_t s) {
+  if (cache_dtype == KVA_BF16) return launch_t<bf16_t>(a, q_dtype, s);
+  return launch_t<float>(a, q_dtype, s);
+}
+
+}  // namespace kva

@@ -1,0 +1,348 @@
+// Host side of the C ABI declared in include/kv_attn.h: argument validation, launch
+// planning and dispatch to the kernels.  Nothing here allocates device memory.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "kv_attn.h"
+#include "launch.h"
+
+namespace kva {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int lmhead_max_hidden();
+bool prefill_simt_supports_head_dim(int D);
+cudaError_t launch_prefill_simt(const PrefillArgs& a, kva_dtype dt, cudaStream_t s);
+bool prefill_tc_supports(int D, kva_dtype dt);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+kva_status fail(kva_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+kva_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return KVA_OK;
+  return fail(KVA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int elem_size(kva_dtype d) { return d == KVA_BF16 ? 2 : 4; }
+bool valid_dtype(kva_dtype d) { return d == KVA_F32 || d == KVA_BF16; }
+
+kva_status check_cache(const kva_cache& c, int n_instances) {
+  if (!valid_dtype(c.dtype)) return fail(KVA_EINVAL, "cache dtype %d unknown", (int)c.dtype);
+  if (!c.k || !c.v) return fail(KVA_EINVAL, "cache k/v pointer is NULL");
+  if (c.n_kv_heads <= 0 || c.head_dim <= 0 || c.capacity <= 0)
+    return fail(KVA_EINVAL, "cache shape must be positive (Hkv=%d D=%d capacity=%d)",
+                c.n_kv_heads, c.head_dim, c.capacity);
+  const int64_t inst = (int64_t)c.n_kv_heads * c.capacity * c.head_dim;
+  if (n_instances > 1 && c.inst_stride < inst)
+    return fail(KVA_EINVAL, "cache inst_stride %lld < Hkv*capacity*D = %lld",
+                (long long)c.inst_stride, (long long)inst);
+  if (c.head_dim % 8 != 0) return fail(KVA_EALIGN, "head_dim %d is not a multiple of 8", c.head_dim);
+  if (!aligned16(c.k) || !aligned16(c.v)) return fail(KVA_EALIGN, "cache k/v not 16-byte aligned");
+  if ((c.inst_stride * elem_size(c.dtype)) % 16 != 0)
+    return fail(KVA_EALIGN, "cache inst_stride is not a multiple of 16 bytes");
+  return KVA_OK;
+}
+
+kva_status build_rope(const kva_rope& r, int D, RopeTable* t) {
+  std::memset(t, 0, sizeof(*t));
+  t->kind = (int)r.kind;
+  t->n_axes = r.n_axes;
+  if (r.kind == KVA_ROPE_NONE) return KVA_OK;
+  if (!(r.base > 0.0) || !std::isfinite(r.base)) return fail(KVA_EINVAL, "rope base must be > 0");
+  if (D / 2 > MAX_ROPE_FREQ) return fail(KVA_EUNSUPPORTED, "head_dim %d too large for RoPE", D);
+  switch (r.kind) {
+    case KVA_ROPE_1D:
+      if (r.n_axes < 1) return fail(KVA_EINVAL, "1D RoPE needs n_axes >= 1");
+      for (int j = 0; j < D / 2; ++j) { t->inv[j] = std::pow(r.base, -2.0 * j / D); t->axis[j] = 0; }
+      return KVA_OK;
+    case KVA_ROPE_SECTIONS: {
+      if (r.n_axes < 1 || r.n_axes > 4) return fail(KVA_EINVAL, "section RoPE needs 1..4 axes");
+      int j = 0;
+      for (int ax = 0; ax < r.n_axes; ++ax) {
+        if (r.sections[ax] < 0) return fail(KVA_EINVAL, "negative RoPE section");
+        for (int u = 0; u < r.sections[ax]; ++u, ++j) {
+          if (j >= D / 2) return fail(KVA_EINVAL, "RoPE sections exceed D/2 = %d", D / 2);
+          t->inv[j] = std::pow(r.base, -2.0 * j / D);
+          t->axis[j] = (unsigned char)ax;
+        }
+      }
+      if (j != D / 2) return fail(KVA_EINVAL, "RoPE sections sum to %d, expected D/2 = %d", j, D / 2);
+      return KVA_OK;
+    }
+    case KVA_ROPE_2D: {
+      if (r.n_axes != 2) return fail(KVA_EINVAL, "2D RoPE needs n_axes == 2");
+      if (D % 4 != 0) return fail(KVA_EINVAL, "2D RoPE needs head_dim %% 4 == 0");
+      const int Q = D / 4;
+      for (int b = 0; b < 2; ++b)
+        for (int j = 0; j < Q; ++j) {
+          t->inv[b * Q + j] = std::pow(r.base, -2.0 * j / (D / 2));
+          t->axis[b * Q + j] = (unsigned char)b;
+        }
+      return KVA_OK;
+    }
+    default:
+      return fail(KVA_EINVAL, "rope kind %d unknown", (int)r.kind);
+  }
+}
+
+constexpr int DECODE_MAX_CHUNKS = 64;
+constexpr int DECODE_CHUNK_ALIGN = 64;
+constexpr int DECODE_MAX_CHUNK_TARGET = 4096;
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+size_t decode_zero_bytes(int B, int Hkv) { return round_up(sizeof(unsigned) * (size_t)B * Hkv, 256); }
+
+size_t decode_ws_bytes(int B, int Hkv, int Hq, int max_chunks, int D) {
+  return decode_zero_bytes(B, Hkv) + round_up(sizeof(float) * (size_t)B * Hq * max_chunks * 2, 256) +
+         sizeof(float) * (size_t)B * Hq * max_chunks * D;
+}
+
+int decode_max_chunks_bound(int max_len) {
+  return std::max(1, std::min(DECODE_MAX_CHUNKS, (max_len + DECODE_CHUNK_ALIGN - 1) / DECODE_CHUNK_ALIGN));
+}
+
+// Split-KV plan: enough (chunk, head, instance) units for ~4 CTAs per SM, chunks a multiple
+// of 64 keys, at most DECODE_MAX_CHUNKS chunks per instance.
+int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len) {
+  long long total = 0;
+  for (int b = 0; b < B; ++b) total += lengths[b];
+  const long long units_per_head = std::max(1LL, (long long)4 * decode_num_sms() / Hkv);
+  long long chunk = (total + units_per_head - 1) / units_per_head;
+  chunk = std::min<long long>(chunk, DECODE_MAX_CHUNK_TARGET);
+  const long long floor_chunk = (max_len + DECODE_MAX_CHUNKS - 1) / DECODE_MAX_CHUNKS;
+  chunk = std::max<long long>(chunk, floor_chunk);
+  chunk = std::max<long long>(DECODE_CHUNK_ALIGN, round_up((size_t)chunk, DECODE_CHUNK_ALIGN));
+  return (int)chunk;
+}
+
+}  // namespace
+}  // namespace kva
+
+using namespace kva;
+
+extern "C" {
+
+const char* kva_strerror(kva_status s) {
+  switch (s) {
+    case KVA_OK: return "ok";
+    case KVA_EINVAL: return "invalid argument";
+    case KVA_ECAPACITY: return "slot or length beyond the cache capacity";
+    case KVA_EUNSUPPORTED: return "unsupported configuration";
+    case KVA_ECUDA: return "CUDA error";
+    case KVA_EALIGN: return "misaligned pointer, stride or head_dim";
+    case KVA_EWORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+const char* kva_last_error(void) { return g_msg; }
+uint64_t kva_launch_count(void) { return g_launches.load(); }
+int32_t kva_version(void) { return 100; }
+
+size_t kva_decode_workspace_size(int32_t B, int32_t n_kv_heads, int32_t n_q_heads, int32_t max_len,
+                                 int32_t head_dim) {
+  if (B <= 0 || n_kv_heads <= 0 || n_q_heads <= 0 || max_len <= 0 || head_dim <= 0) return 0;
+  return decode_ws_bytes(B, n_kv_heads, n_q_heads, decode_max_chunks_bound(max_len), head_dim);
+}
+
+size_t kva_decode_workspace_zero_bytes(int32_t B, int32_t n_kv_heads) {
+  if (B <= 0 || n_kv_heads <= 0) return 0;
+  return decode_zero_bytes(B, n_kv_heads);
+}
+
+size_t kva_lmhead_workspace_size(int32_t B) { return lmhead_workspace_bytes(B); }
+
+kva_status kv_cache_append_rope_qknorm(
+    const void* q, const void* k, const void* v, kva_dtype in_dtype,
+    int32_t N, int32_t T, int32_t n_q_heads,
+    const int32_t* pos, int64_t pos_inst_stride,
+    const int32_t* slot, int64_t slot_inst_stride, const int32_t* slot_host,
+    kva_qknorm norm, kva_rope rope,
+    void* q_out, kva_dtype q_out_dtype,
+    kva_cache cache, kva_stream stream) {
+  if (N < 0 || T < 0) return fail(KVA_EINVAL, "N=%d T=%d must be >= 0", N, T);
+  if (N == 0 || T == 0) return KVA_OK;
+  if (!valid_dtype(in_dtype) || !valid_dtype(q_out_dtype)) return fail(KVA_EINVAL, "unknown dtype");
+  kva_status st = check_cache(cache, N);
+  if (st != KVA_OK) return st;
+  const int D = cache.head_dim, Hkv = cache.n_kv_heads;
+  if (n_q_heads <= 0 || n_q_heads % Hkv != 0)
+    return fail(KVA_EINVAL, "n_q_heads %d must be a positive multiple of n_kv_heads %d", n_q_heads, Hkv);
+  if (!q || !k || !v || !q_out || !slot || !slot_host) return fail(KVA_EINVAL, "NULL q/k/v/q_out/slot");
+  if (rope.kind != KVA_ROPE_NONE && !pos) return fail(KVA_EINVAL, "RoPE needs positions");
+  if (pos_inst_stride < 0 || slot_inst_stride < 0) return fail(KVA_EINVAL, "negative instance stride");
+  if ((norm.q_w == nullptr) != (norm.k_w == nullptr))
+    return fail(KVA_EINVAL, "q and k norm weights must both be given or both be NULL");
+  if (norm.q_w && (!(norm.eps >= 0.f) || norm.inst_stride < 0))
+    return fail(KVA_EINVAL, "QK-Norm eps must be >= 0 and inst_stride >= 0");
+  if (!append_supports_head_dim(D)) return fail(KVA_EUNSUPPORTED, "append: head_dim %d not built", D);
+  if (N > 65535) return fail(KVA_EUNSUPPORTED, "append: N=%d > 65535", N);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out))
+    return fail(KVA_EALIGN, "q/k/v/q_out must be 16-byte aligned");
+  if (norm.q_w && (!aligned16(norm.q_w) || !aligned16(norm.k_w) || (norm.inst_stride * 4) % 16 != 0))
+    return fail(KVA_EALIGN, "norm weights must be 16-byte aligned with a 16-byte instance stride");
+
+  AppendArgs a{};
+  st = build_rope(rope, D, &a.rope);
+  if (st != KVA_OK) return st;
+  for (int n = 0; n < N; ++n)
+    for (int t = 0; t < T; ++t) {
+      const int32_t s = slot_host[(int64_t)n * slot_inst_stride + t];
+      if (s < 0 || s >= cache.capacity)
+        return fail(KVA_ECAPACITY, "slot %d of instance %d token %d outside [0, %d)", s, n, t,
+                    cache.capacity);
+    }
+  a.q = q; a.k = k; a.v = v; a.q_out = q_out; a.kc = cache.k; a.vc = cache.v;
+  a.pos = pos; a.pos_stride = pos_inst_stride; a.slot = slot; a.slot_stride = slot_inst_stride;
+  a.q_w = norm.q_w; a.k_w = norm.k_w; a.w_stride = norm.inst_stride; a.eps = norm.eps;
+  a.after_rope = norm.after_rope ? 1 : 0;
+  a.N = N; a.T = T; a.Hq = n_q_heads; a.Hkv = Hkv; a.D = D; a.capacity = cache.capacity;
+  a.inst_stride = cache.inst_stride;
+  cudaError_t e = launch_append(a, in_dtype, q_out_dtype, cache.dtype, (cudaStream_t)stream);
+  if (e == cudaSuccess) count_launches(1);
+  return cuda_status(e, "append launch");
+}
+
+kva_status kv_attn_prefill(
+    const void* q, kva_dtype q_dtype, kva_cache cache,
+    int32_t N, int32_t S, int32_t n_q_heads, kva_mask mask,
+    const int32_t* segment, const int32_t* segment_host,
+    const int32_t* row_of_slot,
+    float scale, float* out, kva_stream stream) {
+  if (N < 0 || S < 0) return fail(KVA_EINVAL, "N=%d S=%d must be >= 0", N, S);
+  if (N == 0 || S == 0) return KVA_OK;
+  kva_status st = check_cache(cache, N);
+  if (st != KVA_OK) return st;
+  if (q_dtype != cache.dtype) return fail(KVA_EINVAL, "prefill: q dtype must equal the cache dtype");
+  const int D = cache.head_dim, Hkv = cache.n_kv_heads;
+  if (n_q_heads <= 0 || n_q_heads % Hkv != 0)
+    return fail(KVA_EINVAL, "n_q_heads %d must be a positive multiple of n_kv_heads %d", n_q_heads, Hkv);
+  if (!q || !out) return fail(KVA_EINVAL, "NULL q/out");
+  if (S > cache.capacity) return fail(KVA_ECAPACITY, "prefill S=%d > capacity %d", S, cache.capacity);
+  if (mask != KVA_MASK_CAUSAL && mask != KVA_MASK_FULL && mask != KVA_MASK_SEGMENT)
+    return fail(KVA_EINVAL, "mask %d unknown", (int)mask);
+  if (mask == KVA_MASK_SEGMENT) {
+    if (!segment || !segment_host) return fail(KVA_EINVAL, "segment mask needs segment ids");
+    for (int i = 1; i < S; ++i)
+      if (segment_host[i] < segment_host[i - 1])
+        return fail(KVA_EINVAL, "segment ids must be non-decreasing (slot %d)", i);
+  }
+  if (!aligned16(q) || !aligned16(out)) return fail(KVA_EALIGN, "q/out must be 16-byte aligned");
+  if (N > 65535 || n_q_heads > 65535) return fail(KVA_EUNSUPPORTED, "prefill: N or Hq > 65535");
+  PrefillArgs a{};
+  a.q = q; a.kc = cache.k; a.vc = cache.v;
+  a.segment = mask == KVA_MASK_SEGMENT ? segment : nullptr;
+  a.row_of_slot = row_of_slot; a.out = out;
+  a.N = N; a.S = S; a.Hq = n_q_heads; a.Hkv = Hkv; a.D = D; a.capacity = cache.capacity;
+  a.mask = (int)mask; a.inst_stride = cache.inst_stride;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+  a.scale_log2 = sc * 1.4426950408889634f;
+  cudaError_t e;
+  if (prefill_tc_supports(D, cache.dtype)) {
+    e = launch_prefill_tc(a, (cudaStream_t)stream);
+  } else if (prefill_simt_supports_head_dim(D)) {
+    e = launch_prefill_simt(a, cache.dtype, (cudaStream_t)stream);
+  } else {
+    return fail(KVA_EUNSUPPORTED, "prefill: head_dim %d not built", D);
+  }
+  if (e == cudaSuccess) count_launches(1);
+  return cuda_status(e, "prefill launch");
+}
+
+kva_status kv_attn_decode(
+    const void* q, kva_dtype q_dtype, kva_cache cache,
+    const int32_t* lengths, const int32_t* lengths_host, int32_t B, int32_t n_q_heads,
+    float scale, float* out, void* workspace, size_t workspace_bytes, kva_stream stream) {
+  if (B < 0) return fail(KVA_EINVAL, "B=%d must be >= 0", B);
+  if (B == 0) return KVA_OK;
+  if (!valid_dtype(q_dtype)) return fail(KVA_EINVAL, "unknown q dtype");
+  kva_status st = check_cache(cache, B);
+  if (st != KVA_OK) return st;
+  const int D = cache.head_dim, Hkv = cache.n_kv_heads;
+  if (n_q_heads <= 0 || n_q_heads % Hkv != 0)
+    return fail(KVA_EINVAL, "n_q_heads %d must be a positive multiple of n_kv_heads %d", n_q_heads, Hkv);
+  if (D != DECODE_HEAD_DIM) return fail(KVA_EUNSUPPORTED, "decode: head_dim %d (built: 128)", D);
+  const int G = n_q_heads / Hkv;
+  if (G != 1 && G != 2 && G != 4) return fail(KVA_EUNSUPPORTED, "decode: group size %d", G);
+  if (!q || !out || !lengths || !lengths_host) return fail(KVA_EINVAL, "NULL q/out/lengths");
+  if (!workspace) return fail(KVA_EWORKSPACE, "decode: workspace is NULL");
+  if (!aligned16(workspace)) return fail(KVA_EALIGN, "workspace must be 16-byte aligned");
+  if (B > 65535 || Hkv > 65535) return fail(KVA_EUNSUPPORTED, "decode: B or Hkv > 65535");
+  int max_len = 0;
+  for (int b = 0; b < B; ++b) {
+    const int L = lengths_host[b];
+    if (L < 1 || L > cache.capacity)
+      return fail(KVA_ECAPACITY, "length %d of instance %d outside [1, %d]", L, b, cache.capacity);
+    max_len = std::max(max_len, L);
+  }
+  const int chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len);
+  const int max_chunks = (max_len + chunk - 1) / chunk;
+  const size_t need = decode_ws_bytes(B, Hkv, n_q_heads, max_chunks, D);
+  if (workspace_bytes < need)
+    return fail(KVA_EWORKSPACE, "decode workspace %zu bytes < %zu needed", workspace_bytes, need);
+
+  DecodeArgs a{};
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.counters = reinterpret_cast<unsigned*>(ws);
+  a.part_ml = reinterpret_cast<float*>(ws + decode_zero_bytes(B, Hkv));
+  a.part_acc = reinterpret_cast<float*>(ws + decode_zero_bytes(B, Hkv) +
+                                        round_up(sizeof(float) * (size_t)B * n_q_heads * max_chunks * 2, 256));
+  a.q = q; a.kc = cache.k; a.vc = cache.v; a.lengths = lengths; a.out = out;
+  a.B = B; a.Hq = n_q_heads; a.Hkv = Hkv; a.capacity = cache.capacity;
+  a.chunk = chunk; a.max_chunks = max_chunks; a.inst_stride = cache.inst_stride;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+  a.scale_log2 = sc * 1.4426950408889634f;
+  cudaError_t e = launch_decode(a, q_dtype, cache.dtype, (cudaStream_t)stream);
+  if (e == cudaSuccess) count_launches(1);
+  return cuda_status(e, "decode launch");
+}
+
+kva_status lmhead_argmax(
+    const float* h, const void* W, kva_dtype w_dtype,
+    int32_t B, int32_t H, int32_t V, int32_t V_rows,
+    int32_t* out_ids, float* out_max, float* logits,
+    void* workspace, size_t workspace_bytes, kva_stream stream) {
+  if (B < 0) return fail(KVA_EINVAL, "B=%d must be >= 0", B);
+  if (B == 0) return KVA_OK;
+  if (!valid_dtype(w_dtype)) return fail(KVA_EINVAL, "unknown weight dtype");
+  if (H <= 0 || V <= 0 || V_rows <= 0) return fail(KVA_EINVAL, "H, V, V_rows must be positive");
+  if (V > V_rows) return fail(KVA_EINVAL, "vocab V=%d exceeds the table's %d rows", V, V_rows);
+  if (H % 8 != 0) return fail(KVA_EALIGN, "hidden %d is not a multiple of 8", H);
+  if (H > lmhead_max_hidden()) return fail(KVA_EUNSUPPORTED, "hidden %d > %d", H, lmhead_max_hidden());
+  if (!h || !W || !out_ids) return fail(KVA_EINVAL, "NULL h/W/out_ids");
+  if (!aligned16(h) || !aligned16(W)) return fail(KVA_EALIGN, "h and W must be 16-byte aligned");
+  if (!workspace) return fail(KVA_EWORKSPACE, "lm_head: workspace is NULL");
+  if (!aligned16(workspace)) return fail(KVA_EALIGN, "workspace must be 16-byte aligned");
+  if (workspace_bytes < lmhead_workspace_bytes(B))
+    return fail(KVA_EWORKSPACE, "lm_head workspace %zu bytes < %zu needed", workspace_bytes,
+                lmhead_workspace_bytes(B));
+  if (B > 65535 * 8) return fail(KVA_EUNSUPPORTED, "lm_head: batch too large");
+  LmheadArgs a{};
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.counter = reinterpret_cast<unsigned*>(ws);
+  a.best = reinterpret_cast<unsigned long long*>(ws + 256);
+  a.h = h; a.W = W; a.out_ids = out_ids; a.out_max = out_max; a.logits = logits;
+  a.B = B; a.H = H; a.V = V;
+  cudaError_t e = launch_lmhead(a, w_dtype, (cudaStream_t)stream);
+  if (e == cudaSuccess) count_launches(1);
+  return cuda_status(e, "lm_head launch");
+}
+
+}  // extern "C"

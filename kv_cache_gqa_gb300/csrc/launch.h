@@ -1,0 +1,103 @@
+// Internal interface between the host entry points (kv_attn_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kv_attn.h"
+
+namespace kva {
+
+constexpr int MAX_ROPE_FREQ = 128;  // D/2 for D <= 256
+
+// Rotary table description: angle slot j (0 <= j < D/2) uses position axis axis[j] and
+// inverse frequency inv[j] (float64, computed on the host).
+struct RopeTable {
+  int kind;
+  int n_axes;
+  double inv[MAX_ROPE_FREQ];
+  unsigned char axis[MAX_ROPE_FREQ];
+};
+
+struct AppendArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* q_out;
+  void* kc;
+  void* vc;
+  const int32_t* pos;
+  int64_t pos_stride;
+  const int32_t* slot;
+  int64_t slot_stride;
+  const float* q_w;
+  const float* k_w;
+  int64_t w_stride;
+  float eps;
+  int after_rope;
+  int N, T, Hq, Hkv, D, capacity;
+  int64_t inst_stride;
+  RopeTable rope;
+};
+
+bool append_supports_head_dim(int D);
+cudaError_t launch_append(const AppendArgs& a, kva_dtype in_dtype, kva_dtype q_out_dtype,
+                          kva_dtype cache_dtype, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------
+struct DecodeArgs {
+  const void* q;          // [B, Hq, D]
+  const void* kc;
+  const void* vc;
+  const int32_t* lengths; // [B]
+  float* out;             // [B, Hq, D]
+  unsigned int* counters; // [B * Hkv] zero on entry, zero on exit
+  float* part_acc;        // [B, Hq, max_chunks, D]
+  float* part_ml;         // [B, Hq, max_chunks, 2]
+  int B, Hq, Hkv, capacity, chunk, max_chunks;
+  int64_t inst_stride;
+  float scale_log2;       // softmax scale * log2(e)
+};
+
+constexpr int DECODE_HEAD_DIM = 128;
+// Chunk granularity: keys per pipeline stage.
+constexpr int DECODE_SUBTILE_BF16 = 64;
+constexpr int DECODE_SUBTILE_F32 = 32;
+int decode_subtile(kva_dtype cache_dtype);
+int decode_num_sms();
+cudaError_t launch_decode(const DecodeArgs& a, kva_dtype q_dtype, kva_dtype cache_dtype,
+                          cudaStream_t s);
+
+// ---------------------------------------------------------------------------------
+struct LmheadArgs {
+  const float* h;            // [B, H]
+  const void* W;             // [V_rows, H]
+  int32_t* out_ids;          // [B]
+  float* out_max;            // [B] or null
+  float* logits;             // [B, V] or null
+  unsigned long long* best;  // [B] zero on entry, zero on exit
+  unsigned int* counter;     // [1] zero on entry, zero on exit
+  int B, H, V;
+};
+size_t lmhead_workspace_bytes(int B);
+cudaError_t launch_lmhead(const LmheadArgs& a, kva_dtype w_dtype, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------
+struct PrefillArgs {
+  const void* q;              // [N, S, Hq, D]
+  const void* kc;
+  const void* vc;
+  const int32_t* segment;     // [S] or null
+  const int32_t* row_of_slot; // [S] or null
+  float* out;                 // [N, S, Hq, D]
+  int N, S, Hq, Hkv, D, capacity, mask;
+  int64_t inst_stride;
+  float scale_log2;
+};
+int lmhead_max_hidden();
+cudaError_t launch_prefill(const PrefillArgs& a, kva_dtype dtype, cudaStream_t s);
+
+// Launch bookkeeping (kernel launches issued by this library).
+void count_launches(unsigned n);
+
+}  // namespace kva

@@ -1,0 +1,239 @@
+"""Thin ctypes binding of the C ABI in include/kv_attn.h.
+
+Argument marshalling only: every step of the attention path runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (PyTorch supplies device memory and streams);
+their data pointers, sizes and the current CUDA stream go straight to the C entry points
+of the same names.  There is no fallback: if libkv_attn.so is missing or a call fails, a
+KvaError is raised.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import dataclasses
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkv_attn.so")
+
+# enums (include/kv_attn.h)
+KVA_OK, KVA_EINVAL, KVA_ECAPACITY, KVA_EUNSUPPORTED, KVA_ECUDA, KVA_EALIGN, KVA_EWORKSPACE = range(7)
+KVA_F32, KVA_BF16 = 0, 1
+MASKS = {"causal": 0, "full": 1, "segment": 2}
+ROPE_KINDS = {"none": 0, "1d": 1, "sections": 2, "2d": 3}
+
+
+class KvaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"[{status}] {msg}")
+        self.status = status
+
+
+class _Cache(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("dtype", C.c_int),
+                ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("capacity", C.c_int32),
+                ("inst_stride", C.c_int64)]
+
+
+class _Rope(C.Structure):
+    _fields_ = [("kind", C.c_int), ("n_axes", C.c_int32), ("sections", C.c_int32 * 4),
+                ("base", C.c_double)]
+
+
+class _Norm(C.Structure):
+    _fields_ = [("q_w", C.c_void_p), ("k_w", C.c_void_p), ("inst_stride", C.c_int64),
+                ("eps", C.c_float), ("after_rope", C.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load libkv_attn.so (built by kv_cache_gqa_gb300/build.py); raises if it is absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise KvaError(KVA_EUNSUPPORTED, f"{_LIB_PATH} is missing: run kv_cache_gqa_gb300/build.py "
+                           "(there is no CPU fallback)")
+        L = C.CDLL(_LIB_PATH)
+        vp, i32, i64, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
+        L.kv_cache_append_rope_qknorm.argtypes = [vp, vp, vp, C.c_int, i32, i32, i32, vp, i64, vp, i64,
+                                                  vp, _Norm, _Rope, vp, C.c_int, _Cache, vp]
+        L.kv_attn_prefill.argtypes = [vp, C.c_int, _Cache, i32, i32, i32, C.c_int, vp, vp, vp,
+                                      C.c_float, vp, vp]
+        L.kv_attn_decode.argtypes = [vp, C.c_int, _Cache, vp, vp, i32, i32, C.c_float, vp, vp, sz, vp]
+        L.lmhead_argmax.argtypes = [vp, vp, C.c_int, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.kva_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.kva_decode_workspace_size.restype = sz
+        L.kva_decode_workspace_zero_bytes.argtypes = [i32, i32]
+        L.kva_decode_workspace_zero_bytes.restype = sz
+        L.kva_lmhead_workspace_size.argtypes = [i32]
+        L.kva_lmhead_workspace_size.restype = sz
+        L.kva_strerror.argtypes = [C.c_int]
+        L.kva_strerror.restype = C.c_char_p
+        L.kva_last_error.restype = C.c_char_p
+        L.kva_launch_count.restype = C.c_uint64
+        L.kva_version.restype = C.c_int32
+        for f in ("kv_cache_append_rope_qknorm", "kv_attn_prefill", "kv_attn_decode", "lmhead_argmax"):
+            getattr(L, f).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != KVA_OK:
+        raise KvaError(status, lib().kva_last_error().decode())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return KVA_F32
+    if t.dtype == torch.bfloat16:
+        return KVA_BF16
+    raise KvaError(KVA_EINVAL, f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    if not t.is_cuda:
+        raise KvaError(KVA_EINVAL, "expected a CUDA tensor")
+    return t.data_ptr()
+
+
+def _host_i32(a) -> np.ndarray:
+    """Host mirror (int32, C-contiguous) of an index array given as numpy or a CPU tensor."""
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+@dataclasses.dataclass
+class KVCache:
+    """N cache instances: k, v torch CUDA tensors [N, Hkv, capacity, D] (f32 or bf16)."""
+    k: object
+    v: object
+
+    @property
+    def struct(self) -> _Cache:
+        k = self.k
+        if k.dim() != 4 or self.v.shape != k.shape or self.v.dtype != k.dtype:
+            raise KvaError(KVA_EINVAL, "cache k/v must be matching [N, Hkv, W, D] tensors")
+        if not (k.is_contiguous() and self.v.is_contiguous()):
+            raise KvaError(KVA_EINVAL, "cache tensors must be contiguous")
+        N, Hkv, W, D = k.shape
+        return _Cache(k.data_ptr(), self.v.data_ptr(), _dtype_code(k), Hkv, D, W, Hkv * W * D)
+
+    @property
+    def n_kv_heads(self):
+        return self.k.shape[1]
+
+    @property
+    def head_dim(self):
+        return self.k.shape[3]
+
+    @property
+    def capacity(self):
+        return self.k.shape[2]
+
+
+@dataclasses.dataclass
+class Rope:
+    """kind: 'none' | '1d' | 'sections' | '2d'; sections for 'sections' (sum D/2)."""
+    kind: str = "1d"
+    base: float = 1e6
+    sections: Sequence[int] = ()
+
+    @property
+    def n_axes(self) -> int:
+        return {"none": 0, "1d": 1, "2d": 2}.get(self.kind, len(self.sections))
+
+    @property
+    def struct(self) -> _Rope:
+        secs = (C.c_int32 * 4)(*(list(self.sections) + [0] * (4 - len(self.sections))))
+        return _Rope(ROPE_KINDS[self.kind], self.n_axes, secs, float(self.base))
+
+
+def kv_cache_append_rope_qknorm(q, k, v, pos, slot, slot_host, cache: KVCache, q_out, rope: Rope,
+                                q_norm_w=None, k_norm_w=None, eps: float = 1e-6,
+                                norm_after_rope: bool = False, norm_inst_stride: int = 0,
+                                pos_inst_stride: Optional[int] = None,
+                                slot_inst_stride: Optional[int] = None, stream=None):
+    """q [N,T,Hq,D], k/v [N,T,Hkv,D] (CUDA, f32|bf16); pos [N|1,T,n_axes] int32 CUDA;
+    slot [N|1,T] int32 CUDA with host mirror slot_host; q_out [N,T,Hq,D] CUDA f32|bf16.
+    Instance strides of pos/slot default to T*n_axes / T when the leading dim is N, else 0."""
+    N, T, Hq, _ = q.shape
+    if pos_inst_stride is None:
+        pos_inst_stride = 0 if (pos is None or pos.dim() < 3 or pos.shape[0] == 1) else pos.shape[1] * pos.shape[2]
+    if slot_inst_stride is None:
+        slot_inst_stride = 0 if (slot.dim() < 2 or slot.shape[0] == 1) else slot.shape[1]
+    sh = _host_i32(slot_host)
+    norm = _Norm(_ptr(q_norm_w), _ptr(k_norm_w), norm_inst_stride, eps, 1 if norm_after_rope else 0)
+    _check(lib().kv_cache_append_rope_qknorm(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), N, T, Hq,
+        _ptr(pos), pos_inst_stride, _ptr(slot), slot_inst_stride, sh.ctypes.data,
+        norm, rope.struct, _ptr(q_out), _dtype_code(q_out), cache.struct, _stream(stream)))
+
+
+def kv_attn_prefill(q, cache: KVCache, out, mask: str = "causal", segment=None, segment_host=None,
+                    row_of_slot=None, scale: float = 0.0, stream=None):
+    """q [N,S,Hq,D] (CUDA, dtype of the cache); out [N,S,Hq,D] float32 CUDA."""
+    N, S, Hq, _ = q.shape
+    segh = _host_i32(segment_host) if segment_host is not None else None
+    _check(lib().kv_attn_prefill(
+        _ptr(q), _dtype_code(q), cache.struct, N, S, Hq, MASKS[mask],
+        _ptr(segment), segh.ctypes.data if segh is not None else None, _ptr(row_of_slot),
+        float(scale), _ptr(out), _stream(stream)))
+
+
+def decode_workspace_bytes(B: int, n_kv_heads: int, n_q_heads: int, max_len: int, head_dim: int) -> int:
+    return int(lib().kva_decode_workspace_size(B, n_kv_heads, n_q_heads, max_len, head_dim))
+
+
+def lmhead_workspace_bytes(B: int) -> int:
+    return int(lib().kva_lmhead_workspace_size(B))
+
+
+def kv_attn_decode(q, cache: KVCache, lengths, lengths_host, out, workspace, scale: float = 0.0,
+                   stream=None):
+    """q [B,Hq,D] CUDA; lengths [B] int32 CUDA + host mirror; out [B,Hq,D] float32 CUDA;
+    workspace: uint8 CUDA tensor (zeroed once before first use)."""
+    B, Hq, _ = q.shape
+    lh = _host_i32(lengths_host)
+    _check(lib().kv_attn_decode(
+        _ptr(q), _dtype_code(q), cache.struct, _ptr(lengths), lh.ctypes.data, B, Hq, float(scale),
+        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lmhead_argmax(h, W, out_ids, workspace, V: Optional[int] = None, out_max=None, logits=None,
+                  stream=None):
+    """h [B,H] float32 CUDA; W [V_rows,H] bf16|f32 CUDA; out_ids [B] int32 CUDA."""
+    B, H = h.shape
+    V_rows = W.shape[0]
+    V = V_rows if V is None else V
+    _check(lib().lmhead_argmax(
+        _ptr(h), _ptr(W), _dtype_code(W), B, H, V, V_rows, _ptr(out_ids), _ptr(out_max),
+        _ptr(logits), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def launch_count() -> int:
+    return int(lib().kva_launch_count())
+
+
+def version() -> int:
+    return int(lib().kva_version())
+
+
+# Raw C entry points for callers that marshal pointers themselves (tests of the ABI).
+def raw():
+    return lib()

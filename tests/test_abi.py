@@ -1,0 +1,132 @@
+"""The C-ABI library loads, exports every function include/kv_attn.h declares, and its host-side
+validation rejects bad arguments with the documented status before launching anything (these
+calls never reach the GPU, so they run without one)."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def K():
+    from kv_cache_gqa_gb300 import build
+    build.build_library(verbose=False)
+    import kv_cache_gqa_gb300.kv_attn as K
+    K.lib()
+    return K
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kv_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", src)) - {"sizeof"})
+
+
+def test_exports_every_declared_symbol(K):
+    names = declared_functions()
+    assert {"kv_cache_append_rope_qknorm", "kv_attn_prefill", "kv_attn_decode", "lmhead_argmax"} <= set(names)
+    for n in names:
+        assert hasattr(K.lib(), n), f"libkv_attn.so does not export {n}"
+
+
+def test_strerror_and_version(K):
+    L = K.lib()
+    for s in range(7):
+        assert L.kva_strerror(s)
+    assert L.kva_strerror(0) == b"ok"
+    assert L.kva_version() >= 100
+    assert L.kva_launch_count() >= 0
+
+
+def _cache(ptr=16, dtype=1, hkv=8, d=128, cap=1024, stride=None):
+    import kv_cache_gqa_gb300.kv_attn as K
+    return K._Cache(ptr, ptr, dtype, hkv, d, cap, stride if stride is not None else hkv * cap * d)
+
+
+def _rope(kind=1, base=1e6, secs=(0, 0, 0, 0), n_axes=1):
+    import kv_cache_gqa_gb300.kv_attn as K
+    return K._Rope(kind, n_axes, (C.c_int32 * 4)(*secs), base)
+
+
+def _norm(q=0, k=0, eps=1e-6):
+    import kv_cache_gqa_gb300.kv_attn as K
+    return K._Norm(q or None, k or None, 0, eps, 0)
+
+
+FAKE = 1 << 20   # a 16-byte aligned dummy address: never dereferenced, validation fails first
+
+
+def append(K, *, N=1, T=1, Hq=16, slot_host=None, cache=None, rope=None, norm=None, q=FAKE, in_dtype=0):
+    sh = np.zeros(max(1, N * T), np.int32) if slot_host is None else np.asarray(slot_host, np.int32)
+    return K.lib().kv_cache_append_rope_qknorm(
+        q, FAKE, FAKE, in_dtype, N, T, Hq, FAKE, 0, FAKE, T, sh.ctypes.data,
+        norm or _norm(), rope or _rope(), FAKE, 1, cache or _cache(FAKE), None)
+
+
+def test_append_validation(K):
+    assert append(K, N=0) == K.KVA_OK and append(K, T=0) == K.KVA_OK        # empty: no-op
+    assert append(K, N=-1) == K.KVA_EINVAL
+    assert append(K, Hq=12) == K.KVA_EINVAL                                 # not a multiple of Hkv
+    assert append(K, slot_host=[1024]) == K.KVA_ECAPACITY                   # beyond the window
+    assert append(K, slot_host=[-1]) == K.KVA_ECAPACITY
+    assert append(K, q=FAKE + 4) == K.KVA_EALIGN
+    assert append(K, cache=_cache(FAKE, d=100)) == K.KVA_EALIGN              # D % 8
+    assert append(K, cache=_cache(FAKE, d=80)) == K.KVA_EUNSUPPORTED         # D not built
+    assert append(K, rope=_rope(kind=2, secs=(16, 16, 16, 8), n_axes=4)) == K.KVA_EINVAL  # sum != D/2
+    assert append(K, rope=_rope(kind=3, n_axes=1)) == K.KVA_EINVAL
+    assert append(K, rope=_rope(base=-1.0)) == K.KVA_EINVAL
+    assert append(K, norm=_norm(q=FAKE)) == K.KVA_EINVAL                     # q weight without k weight
+    assert append(K, cache=_cache(FAKE, stride=5), N=2, slot_host=[0, 0]) == K.KVA_EINVAL
+    assert b"stride" in K.lib().kva_last_error()
+
+
+def test_prefill_validation(K):
+    L = K.lib()
+    seg_bad = np.array([0, 1, 0], np.int32)
+    def pf(S=3, mask=0, seg=None, segh=None, qd=1, cache=None):
+        return L.kv_attn_prefill(FAKE, qd, cache or _cache(FAKE, cap=4), 1, S, 16, mask, seg, segh,
+                                 None, 0.0, FAKE, None)
+    assert pf(S=0) == K.KVA_OK
+    assert pf(S=5) == K.KVA_ECAPACITY
+    assert pf(qd=0) == K.KVA_EINVAL                                         # q dtype != cache dtype
+    assert pf(mask=2) == K.KVA_EINVAL                                       # segment mask without ids
+    assert pf(mask=2, seg=FAKE, segh=seg_bad.ctypes.data) == K.KVA_EINVAL   # not non-decreasing
+    assert pf(mask=7) == K.KVA_EINVAL
+
+
+def test_decode_validation(K):
+    L = K.lib()
+    def dec(lens, ws=FAKE, ws_bytes=1 << 30, cache=None, Hq=16):
+        lh = np.asarray(lens, np.int32)
+        return L.kv_attn_decode(FAKE, 1, cache or _cache(FAKE, cap=64), FAKE, lh.ctypes.data, len(lens), Hq,
+                                0.0, FAKE, ws, ws_bytes, None)
+    assert L.kv_attn_decode(FAKE, 1, _cache(FAKE), FAKE, None, 0, 16, 0.0, FAKE, FAKE, 0, None) == K.KVA_OK
+    assert dec([0]) == K.KVA_ECAPACITY                                       # empty prefix
+    assert dec([65]) == K.KVA_ECAPACITY                                      # beyond the window
+    assert dec([3], ws=None) == K.KVA_EWORKSPACE
+    assert dec([3], cache=_cache(FAKE, d=64, cap=64)) == K.KVA_EUNSUPPORTED   # decode built for D=128
+    assert dec([3], Hq=64) == K.KVA_EUNSUPPORTED                             # group size 8
+    assert L.kva_decode_workspace_size(4, 8, 16, 1000, 128) > L.kva_decode_workspace_zero_bytes(4, 8) > 0
+
+
+def test_lmhead_validation(K):
+    L = K.lib()
+    def lm(B=1, H=1024, V=100, Vr=100, ws=FAKE, wsb=4096, h=FAKE):
+        return L.lmhead_argmax(h, FAKE, 1, B, H, V, Vr, FAKE, None, None, ws, wsb, None)
+    assert lm(B=0) == K.KVA_OK
+    assert lm(V=101) == K.KVA_EINVAL                                         # vocab beyond the table rows
+    assert lm(H=1020) == K.KVA_EALIGN
+    assert lm(ws=None) == K.KVA_EWORKSPACE
+    assert lm(wsb=8) == K.KVA_EWORKSPACE
+    assert lm(h=FAKE + 8) == K.KVA_EALIGN
+    assert lm(H=8192) == K.KVA_EUNSUPPORTED
+
+
+def test_binding_refuses_cpu_tensors(K):
+    torch = pytest.importorskip("torch")
+    with pytest.raises(K.KvaError):
+        K._ptr(torch.zeros(4))
