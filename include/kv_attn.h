@@ -185,6 +185,29 @@ size_t kva_decode_workspace_size(int32_t B, int32_t n_kv_heads, int32_t n_q_head
 size_t kva_decode_workspace_zero_bytes(int32_t B, int32_t n_kv_heads);
 
 /* ---------------------------------------------------------------------------------
+ * kv_attn_decode_static
+ *   The same decode as kv_attn_decode for callers that cannot allocate device memory
+ *   (a host framework that owns every allocation, code that must not touch an allocator
+ *   in its hot loop): there is no workspace argument.  The split-KV scratch lives in a
+ *   fixed 4 MiB array inside this library's device image; every GPU that loads the
+ *   library holds it until the process exits.  The reference pages have no counterpart
+ *   of this call.
+ *  Arguments and errors: as kv_attn_decode.  A batch whose partials cannot fit the fixed
+ *   scratch even as one chunk per instance (B * n_q_heads * (head_dim + 2) * 4 bytes plus
+ *   the counters above 4 MiB) returns KVA_EWORKSPACE; otherwise larger chunks are chosen
+ *   until the partials fit.
+ *  The call allocates nothing (no cudaMalloc, no cudaFree).  The first call on a device
+ *   looks up the array's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture.  Every call clears the merge counters it needs on `stream`.
+ *  All calls share the one array, which keeps the last call's contents: calls that
+ *   overlap on the GPU (different streams, or concurrent graphs) race on it and must be
+ *   serialised by the caller. */
+kva_status kv_attn_decode_static(
+    const void* q, kva_dtype q_dtype, kva_cache cache,
+    const int32_t* lengths, const int32_t* lengths_host, int32_t B, int32_t n_q_heads,
+    float scale, float* out, kva_stream stream);
+
+/* ---------------------------------------------------------------------------------
  * lmhead_argmax
  *   Greedy tied lm_head: z[b, v] = sum_k W[v, k] h[b, k] for v < V, ids[b] = argmax_v z[b, v]
  *   (Youtu-VL-4B ncnn port, step 6: final-norm hidden dotted with every vocab row,

@@ -133,6 +133,9 @@ int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len) {
 }
 
 }  // namespace
+
+void set_last_error(const char* msg) { std::snprintf(g_msg, sizeof(g_msg), "%s", msg); }
+
 }  // namespace kva
 
 using namespace kva;

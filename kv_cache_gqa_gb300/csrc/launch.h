@@ -99,5 +99,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, kva_dtype dtype, cudaStream_t s
 
 // Launch bookkeeping (kernel launches issued by this library).
 void count_launches(unsigned n);
+// Record the message kva_last_error() returns on this host thread.
+void set_last_error(const char* msg);
 
 }  // namespace kva

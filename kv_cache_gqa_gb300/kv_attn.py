@@ -63,6 +63,8 @@ def lib() -> C.CDLL:
         L.kv_attn_prefill.argtypes = [vp, C.c_int, _Cache, i32, i32, i32, C.c_int, vp, vp, vp,
                                       C.c_float, vp, vp]
         L.kv_attn_decode.argtypes = [vp, C.c_int, _Cache, vp, vp, i32, i32, C.c_float, vp, vp, sz, vp]
+        L.kv_attn_decode_static.argtypes = [vp, C.c_int, _Cache, vp, vp, i32, i32, C.c_float, vp, vp]
+        L.kv_attn_decode_static.restype = C.c_int
         L.lmhead_argmax.argtypes = [vp, vp, C.c_int, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
         L.kva_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.kva_decode_workspace_size.restype = sz
