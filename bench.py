@@ -188,7 +188,7 @@ class Qwen3Job:
         self.len_d = torch.from_numpy(np.stack(self.len_host)).to(dev)
         self.ids = torch.empty((TOKENS_PER_JOB,), dtype=torch.int32, device=dev)
         self.dec_ws = torch.zeros(K.decode_workspace_bytes(LAYERS, HKV, HQ, WINDOW, D), dtype=torch.uint8, device=dev)
-        self.lm_ws = torch.zeros(K.lmhead_workspace_bytes(1), dtype=torch.uint8, device=dev)
+        self.lm_ws = torch.zeros(K.lmhead_workspace_bytes(1, HIDDEN), dtype=torch.uint8, device=dev)
         self.events = None
 
     def _ev(self, key):

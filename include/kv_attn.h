@@ -218,9 +218,13 @@ kva_status kv_attn_decode_static(
  *  h          [B,H] float32 (device);  W [V_rows, H] of w_dtype (device)
  *  out_ids    [B] int32 (device);  out_max [B] float32 max logit (device, nullable)
  *  logits     [B,V] float32 (device, nullable): every logit, for inspection
- *  workspace  device scratch of at least kva_lmhead_workspace_size(B) bytes, zero before the
- *             first call; every call leaves it zero.  Calls sharing one workspace must not
- *             overlap on the GPU.
+ *  workspace  device scratch of at least kva_lmhead_workspace_size(B, H) bytes whose first
+ *             kva_lmhead_workspace_zero_bytes(B) bytes are zero before the first call; every
+ *             call leaves them zero again.  Calls sharing one workspace must not overlap on
+ *             the GPU.
+ *  B == 1 streams the table with CUDA-core dot products; 2 <= B <= 128 (bf16 table, H a
+ *  multiple of 64) runs on the tensor cores with h split into two bf16 halves (h_hi + h_lo
+ *  carries ~16 significant bits), fp32 accumulation.
  *  Errors: KVA_EINVAL, KVA_EALIGN (H % 8), KVA_EWORKSPACE, KVA_ECUDA.  B == 0 is a no-op. */
 kva_status lmhead_argmax(
     const float* h, const void* W, kva_dtype w_dtype,
@@ -228,7 +232,8 @@ kva_status lmhead_argmax(
     int32_t* out_ids, float* out_max, float* logits,
     void* workspace, size_t workspace_bytes, kva_stream stream);
 
-size_t kva_lmhead_workspace_size(int32_t B);
+size_t kva_lmhead_workspace_size(int32_t B, int32_t H);
+size_t kva_lmhead_workspace_zero_bytes(int32_t B);
 
 /* ---------------------------------------------------------------------------------
  * Introspection */

@@ -48,12 +48,14 @@ __device__ __forceinline__ void rope_cos_sin(int32_t p, double inv, float* c, fl
 }
 
 template <int D, typename InT, typename QOutT, typename CacheT>
-__global__ void __launch_bounds__(APPEND_THREADS)
+__global__ void __launch_bounds__(APPEND_THREADS, 3)
 append_kernel(const __grid_constant__ AppendArgs a) {
   constexpr int LPR = D / 8;            // lanes per row
   constexpr int RPW = 32 / LPR;         // rows per warp
   constexpr int HALF = D / 2;
   constexpr int QUARTER = D / 4;
+  constexpr int ROWS_PER_PASS = APPEND_WARPS * RPW;
+  constexpr int MAXP = 2;               // passes whose loads are in flight together
 
   __shared__ float s_cos[D / 2];
   __shared__ float s_sin[D / 2];
@@ -63,18 +65,6 @@ append_kernel(const __grid_constant__ AppendArgs a) {
   const int n = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-
-  // ---- rotary angles of this token ----
-  if (a.rope.kind != KVA_ROPE_NONE) {
-    const int32_t* pos = a.pos + (int64_t)n * a.pos_stride + (int64_t)t * a.rope.n_axes;
-    for (int j = tid; j < D / 2; j += APPEND_THREADS)
-      rope_cos_sin(pos[a.rope.axis[j]], a.rope.inv[j], &s_cos[j], &s_sin[j]);
-  }
-  __syncthreads();
-
-  const int32_t slot = a.slot[(int64_t)n * a.slot_stride + t];
-  const bool slot_ok = slot >= 0 && slot < a.capacity;
-
   const int sub = lane / LPR;            // row within the warp's group
   const int e0 = (lane % LPR) * 8;       // first element owned by this lane
   const bool lane_on = sub < RPW;
@@ -83,92 +73,110 @@ append_kernel(const __grid_constant__ AppendArgs a) {
   const float* kw = a.k_w ? a.k_w + (int64_t)n * a.w_stride : nullptr;
   float* rowbuf = &s_row[warp][sub < RPW ? sub * D : 0];
 
-  for (int r0 = warp * RPW; r0 < n_rows; r0 += APPEND_WARPS * RPW) {
-    const int r = r0 + sub;
-    const bool active = lane_on && r < n_rows;
-    const int kind = !active ? 3 : (r < a.Hq ? 0 : (r < a.Hq + a.Hkv ? 1 : 2));  // q, k, v, idle
-    const int head = kind == 0 ? r : (kind == 1 ? r - a.Hq : r - a.Hq - a.Hkv);
+  // ---- independent loads first: slot, this token's position ids, weights ----
+  const int32_t slot = a.slot[(int64_t)n * a.slot_stride + t];
+  int32_t p_ang = 0;
+  if (a.rope.kind != KVA_ROPE_NONE && tid < D / 2)
+    p_ang = a.pos[(int64_t)n * a.pos_stride + (int64_t)t * a.rope.n_axes + a.rope.axis[tid]];
+  float wq[8], wk[8];
+  if (qw && lane_on) { load8(qw + e0, wq); load8(kw + e0, wk); }
 
-    float x[8];
-    if (kind == 0) {
-      load8(reinterpret_cast<const InT*>(a.q) + (((int64_t)n * a.T + t) * a.Hq + head) * D + e0, x);
-    } else if (kind == 1) {
-      load8(reinterpret_cast<const InT*>(a.k) + (((int64_t)n * a.T + t) * a.Hkv + head) * D + e0, x);
-    } else if (kind == 2) {
-      load8(reinterpret_cast<const InT*>(a.v) + (((int64_t)n * a.T + t) * a.Hkv + head) * D + e0, x);
-    } else {
+  for (int pg = 0; pg < n_rows; pg += MAXP * ROWS_PER_PASS) {
+    // ---- row loads of up to MAXP passes, all in flight together ----
+    float x[MAXP][8];
+    int kind[MAXP], head[MAXP];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = 0.f;
-    }
-    const float* w = kind == 0 ? qw : (kind == 1 ? kw : nullptr);
-    const bool norm = w != nullptr;
-
-    // ---- QK-Norm before RoPE (Qwen3 order) ----
-    if (!a.after_rope) {
-      float ss = 0.f;
+    for (int p = 0; p < MAXP; ++p) {
+      const int r = pg + p * ROWS_PER_PASS + warp * RPW + sub;
+      const bool active = lane_on && r < n_rows;
+      kind[p] = !active ? 3 : (r < a.Hq ? 0 : (r < a.Hq + a.Hkv ? 1 : 2));   // q, k, v, idle
+      head[p] = kind[p] == 0 ? r : (kind[p] == 1 ? r - a.Hq : r - a.Hq - a.Hkv);
+      if (kind[p] == 0) {
+        load8(reinterpret_cast<const InT*>(a.q) + (((int64_t)n * a.T + t) * a.Hq + head[p]) * D + e0, x[p]);
+      } else if (kind[p] == 1) {
+        load8(reinterpret_cast<const InT*>(a.k) + (((int64_t)n * a.T + t) * a.Hkv + head[p]) * D + e0, x[p]);
+      } else if (kind[p] == 2) {
+        load8(reinterpret_cast<const InT*>(a.v) + (((int64_t)n * a.T + t) * a.Hkv + head[p]) * D + e0, x[p]);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
-      ss = row_sum<LPR>(ss, lane);
-      if (norm) {
-        const float rinv = 1.0f / sqrtf(ss / (float)D + a.eps);
-        float wv[8];
-        load8(w + e0, wv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = x[i] * rinv * wv[i];
+        for (int i = 0; i < 8; ++i) x[p][i] = 0.f;
       }
     }
 
-    // ---- RoPE: partner elements exchanged through the warp's row buffer ----
-    if (a.rope.kind != KVA_ROPE_NONE) {
-      if (lane_on) {
+    // ---- rotary angles of this token (once; shared by every rotated row) ----
+    if (pg == 0) {
+      if (a.rope.kind != KVA_ROPE_NONE && tid < D / 2) rope_cos_sin(p_ang, a.rope.inv[tid], &s_cos[tid], &s_sin[tid]);
+      __syncthreads();
+    }
+
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rowbuf[e0 + i] = x[i];
-      }
-      __syncwarp();
-      if (kind <= 1) {
-        float y[8];
+    for (int p = 0; p < MAXP; ++p) {
+      if (pg + p * ROWS_PER_PASS >= n_rows) break;       // uniform across the CTA
+      const bool norm = qw != nullptr && kind[p] <= 1;
+
+      // ---- QK-Norm before RoPE (Qwen3 order) ----
+      if (!a.after_rope) {
+        float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int d = e0 + i;
-          int j, partner;
-          float sgn;
-          if (a.rope.kind == KVA_ROPE_2D) {
-            const int b = d / HALF, dd = d - b * HALF;
-            if (dd < QUARTER) { j = b * QUARTER + dd; partner = d + QUARTER; sgn = -1.f; }
-            else { j = b * QUARTER + dd - QUARTER; partner = d - QUARTER; sgn = 1.f; }
-          } else {
-            if (d < HALF) { j = d; partner = d + HALF; sgn = -1.f; }
-            else { j = d - HALF; partner = d - HALF; sgn = 1.f; }
-          }
-          y[i] = x[i] * s_cos[j] + sgn * rowbuf[partner] * s_sin[j];
+        for (int i = 0; i < 8; ++i) ss += x[p][i] * x[p][i];
+        ss = row_sum<LPR>(ss, lane);
+        if (norm) {
+          const float rinv = 1.0f / sqrtf(ss / (float)D + a.eps);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[p][i] = x[p][i] * rinv * (kind[p] == 0 ? wq[i] : wk[i]);
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = y[i];
       }
-      __syncwarp();
-    }
 
-    // ---- QK-Norm after RoPE (HunyuanOCR order) ----
-    if (a.after_rope) {
-      float ss = 0.f;
+      // ---- RoPE: partner elements exchanged through the warp's row buffer ----
+      if (a.rope.kind != KVA_ROPE_NONE) {
+        if (lane_on) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
-      ss = row_sum<LPR>(ss, lane);
-      if (norm) {
-        const float rinv = 1.0f / sqrtf(ss / (float)D + a.eps);
-        float wv[8];
-        load8(w + e0, wv);
+          for (int i = 0; i < 8; ++i) rowbuf[e0 + i] = x[p][i];
+        }
+        __syncwarp();
+        if (kind[p] <= 1) {
+          float y[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = x[i] * rinv * wv[i];
+          for (int i = 0; i < 8; ++i) {
+            const int d = e0 + i;
+            int j, partner;
+            float sgn;
+            if (a.rope.kind == KVA_ROPE_2D) {
+              const int b = d / HALF, dd = d - b * HALF;
+              if (dd < QUARTER) { j = b * QUARTER + dd; partner = d + QUARTER; sgn = -1.f; }
+              else { j = b * QUARTER + dd - QUARTER; partner = d - QUARTER; sgn = 1.f; }
+            } else {
+              if (d < HALF) { j = d; partner = d + HALF; sgn = -1.f; }
+              else { j = d - HALF; partner = d - HALF; sgn = 1.f; }
+            }
+            y[i] = x[p][i] * s_cos[j] + sgn * rowbuf[partner] * s_sin[j];
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[p][i] = y[i];
+        }
+        __syncwarp();
       }
-    }
 
-    // ---- stores ----
-    if (kind == 0) {
-      store8(reinterpret_cast<QOutT*>(a.q_out) + (((int64_t)n * a.T + t) * a.Hq + head) * D + e0, x);
-    } else if ((kind == 1 || kind == 2) && slot_ok) {
-      CacheT* base = reinterpret_cast<CacheT*>(kind == 1 ? a.kc : a.vc);
-      store8(base + (int64_t)n * a.inst_stride + ((int64_t)head * a.capacity + slot) * D + e0, x);
+      // ---- QK-Norm after RoPE (HunyuanOCR order) ----
+      if (a.after_rope) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss += x[p][i] * x[p][i];
+        ss = row_sum<LPR>(ss, lane);
+        if (norm) {
+          const float rinv = 1.0f / sqrtf(ss / (float)D + a.eps);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[p][i] = x[p][i] * rinv * (kind[p] == 0 ? wq[i] : wk[i]);
+        }
+      }
+
+      // ---- stores ----
+      if (kind[p] == 0) {
+        store8(reinterpret_cast<QOutT*>(a.q_out) + (((int64_t)n * a.T + t) * a.Hq + head[p]) * D + e0, x[p]);
+      } else if ((kind[p] == 1 || kind[p] == 2) && slot >= 0 && slot < a.capacity) {
+        CacheT* base = reinterpret_cast<CacheT*>(kind[p] == 1 ? a.kc : a.vc);
+        store8(base + (int64_t)n * a.inst_stride + ((int64_t)head[p] * a.capacity + slot) * D + e0, x[p]);
+      }
     }
   }
 }

@@ -29,8 +29,8 @@ constexpr int WARPS = THREADS / 32;
 constexpr int NSTAGE = 3;
 
 template <typename CacheT> struct DecodeTile;
-template <> struct DecodeTile<bf16_t> { static constexpr int KT = DECODE_SUBTILE_BF16; };
-template <> struct DecodeTile<float> { static constexpr int KT = DECODE_SUBTILE_F32; };
+template <> struct DecodeTile<bf16_t> { static constexpr int KT = 64; };
+template <> struct DecodeTile<float> { static constexpr int KT = 32; };
 
 __device__ __forceinline__ float load_q(const void* q, kva_dtype dt, int64_t i) {
   if (dt == KVA_BF16)
@@ -321,7 +321,7 @@ cudaError_t launch_t(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
 }  // namespace
 
 int decode_subtile(kva_dtype cache_dtype) {
-  return cache_dtype == KVA_BF16 ? DECODE_SUBTILE_BF16 : DECODE_SUBTILE_F32;
+  return cache_dtype == KVA_BF16 ? DecodeTile<bf16_t>::KT : DecodeTile<float>::KT;
 }
 
 int decode_num_sms() {

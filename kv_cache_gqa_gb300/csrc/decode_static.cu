@@ -87,12 +87,10 @@ kva_status kv_attn_decode_static(
     return static_fail(KVA_EALIGN, "pointers and the instance stride must be 16-byte aligned");
   if (B > 65535) return static_fail(KVA_EUNSUPPORTED, "B > 65535");
   int max_len = 0;
-  long long total = 0;
   for (int b = 0; b < B; ++b) {
     const int L = lengths_host[b];
     if (L < 1 || L > cache.capacity) return static_fail(KVA_ECAPACITY, "a length is outside [1, capacity]");
     max_len = std::max(max_len, L);
-    total += L;
   }
 
   // Scratch layout: merge counters (cleared by every call), then (max, sum) and acc partials.
@@ -101,10 +99,8 @@ kva_status kv_attn_decode_static(
   if (zero_bytes + 256 + per_chunk > STATIC_SCRATCH_BYTES)
     return static_fail(KVA_EWORKSPACE, "B * n_q_heads too large for the fixed 4 MiB decode scratch");
   const int fit_chunks = (int)std::min<size_t>(64, (STATIC_SCRATCH_BYTES - zero_bytes - 256) / per_chunk);
-  // Same split rule as kv_attn_decode (about four CTAs per SM, 64-key multiples), then widened
-  // until the partials fit in the fixed scratch.
-  const long long units = std::max(1LL, (long long)4 * decode_num_sms() / Hkv);
-  long long chunk = std::min<long long>((total + units - 1) / units, 4096);
+  // Same split rule as kv_attn_decode, then widened until the partials fit in the fixed scratch.
+  long long chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len);
   chunk = std::max<long long>(chunk, (max_len + fit_chunks - 1) / fit_chunks);
   chunk = std::max<long long>(64, (chunk + 63) / 64 * 64);
   const int max_chunks = (int)((max_len + chunk - 1) / chunk);

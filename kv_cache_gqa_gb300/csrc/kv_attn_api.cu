@@ -103,7 +103,7 @@ kva_status build_rope(const kva_rope& r, int D, RopeTable* t) {
 
 constexpr int DECODE_MAX_CHUNKS = 64;
 constexpr int DECODE_CHUNK_ALIGN = 64;
-constexpr int DECODE_MAX_CHUNK_TARGET = 4096;
+constexpr int DECODE_MAX_CHUNK_TARGET = 8192;
 
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
@@ -118,23 +118,23 @@ int decode_max_chunks_bound(int max_len) {
   return std::max(1, std::min(DECODE_MAX_CHUNKS, (max_len + DECODE_CHUNK_ALIGN - 1) / DECODE_CHUNK_ALIGN));
 }
 
-// Split-KV plan: enough (chunk, head, instance) units for ~4 CTAs per SM, chunks a multiple
-// of 64 keys, at most DECODE_MAX_CHUNKS chunks per instance.
+}  // namespace
+
+void set_last_error(const char* msg) { std::snprintf(g_msg, sizeof(g_msg), "%s", msg); }
+
+// About three waves of resident decode CTAs (two per SM) over all (instance, KV head) pairs.
 int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len) {
   long long total = 0;
   for (int b = 0; b < B; ++b) total += lengths[b];
-  const long long units_per_head = std::max(1LL, (long long)4 * decode_num_sms() / Hkv);
-  long long chunk = (total + units_per_head - 1) / units_per_head;
+  total *= Hkv;                                           // key rows over all (instance, head)
+  const long long target_ctas = 3LL * 2 * decode_num_sms();
+  long long chunk = (total + target_ctas - 1) / target_ctas;
   chunk = std::min<long long>(chunk, DECODE_MAX_CHUNK_TARGET);
   const long long floor_chunk = (max_len + DECODE_MAX_CHUNKS - 1) / DECODE_MAX_CHUNKS;
   chunk = std::max<long long>(chunk, floor_chunk);
   chunk = std::max<long long>(DECODE_CHUNK_ALIGN, round_up((size_t)chunk, DECODE_CHUNK_ALIGN));
   return (int)chunk;
 }
-
-}  // namespace
-
-void set_last_error(const char* msg) { std::snprintf(g_msg, sizeof(g_msg), "%s", msg); }
 
 }  // namespace kva
 
@@ -170,7 +170,15 @@ size_t kva_decode_workspace_zero_bytes(int32_t B, int32_t n_kv_heads) {
   return decode_zero_bytes(B, n_kv_heads);
 }
 
-size_t kva_lmhead_workspace_size(int32_t B) { return lmhead_workspace_bytes(B); }
+size_t kva_lmhead_workspace_size(int32_t B, int32_t H) {
+  if (B <= 0 || H <= 0) return 0;
+  return lmhead_workspace_bytes(B, H);
+}
+
+size_t kva_lmhead_workspace_zero_bytes(int32_t B) {
+  if (B <= 0) return 0;
+  return lmhead_zero_bytes(B);
+}
 
 kva_status kv_cache_append_rope_qknorm(
     const void* q, const void* k, const void* v, kva_dtype in_dtype,
@@ -333,18 +341,19 @@ kva_status lmhead_argmax(
   if (!aligned16(h) || !aligned16(W)) return fail(KVA_EALIGN, "h and W must be 16-byte aligned");
   if (!workspace) return fail(KVA_EWORKSPACE, "lm_head: workspace is NULL");
   if (!aligned16(workspace)) return fail(KVA_EALIGN, "workspace must be 16-byte aligned");
-  if (workspace_bytes < lmhead_workspace_bytes(B))
+  if (workspace_bytes < lmhead_workspace_bytes(B, H))
     return fail(KVA_EWORKSPACE, "lm_head workspace %zu bytes < %zu needed", workspace_bytes,
-                lmhead_workspace_bytes(B));
+                lmhead_workspace_bytes(B, H));
   if (B > 65535 * 8) return fail(KVA_EUNSUPPORTED, "lm_head: batch too large");
   LmheadArgs a{};
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   a.counter = reinterpret_cast<unsigned*>(ws);
-  a.best = reinterpret_cast<unsigned long long*>(ws + 256);
+  a.best = reinterpret_cast<unsigned long long*>(ws + 256);   // see lmhead_zero_bytes
   a.h = h; a.W = W; a.out_ids = out_ids; a.out_max = out_max; a.logits = logits;
   a.B = B; a.H = H; a.V = V;
-  cudaError_t e = launch_lmhead(a, w_dtype, (cudaStream_t)stream);
-  if (e == cudaSuccess) count_launches(1);
+  unsigned n_launch = 0;
+  cudaError_t e = launch_lmhead(a, w_dtype, ws + lmhead_zero_bytes(B), (cudaStream_t)stream, &n_launch);
+  if (e == cudaSuccess) count_launches(n_launch);
   return cuda_status(e, "lm_head launch");
 }
 

@@ -60,11 +60,11 @@ struct DecodeArgs {
 };
 
 constexpr int DECODE_HEAD_DIM = 128;
-// Chunk granularity: keys per pipeline stage.
-constexpr int DECODE_SUBTILE_BF16 = 64;
-constexpr int DECODE_SUBTILE_F32 = 32;
-int decode_subtile(kva_dtype cache_dtype);
+int decode_subtile(kva_dtype cache_dtype);   // keys per pipeline stage
 int decode_num_sms();
+// Split-KV plan: `chunk` = target keys per CTA (instance b is cut into ceil(L_b / chunk)
+// nearly equal chunks), a multiple of 64, with at most 64 chunks per instance.
+int decode_plan_chunk(const int32_t* lengths_host, int B, int Hkv, int max_len);
 cudaError_t launch_decode(const DecodeArgs& a, kva_dtype q_dtype, kva_dtype cache_dtype,
                           cudaStream_t s);
 
@@ -79,8 +79,11 @@ struct LmheadArgs {
   unsigned int* counter;     // [1] zero on entry, zero on exit
   int B, H, V;
 };
-size_t lmhead_workspace_bytes(int B);
-cudaError_t launch_lmhead(const LmheadArgs& a, kva_dtype w_dtype, cudaStream_t s);
+size_t lmhead_workspace_bytes(int B, int H);
+size_t lmhead_zero_bytes(int B);
+// Launches the lm_head for `a`; *n_launches receives the number of kernels enqueued.
+cudaError_t launch_lmhead(const LmheadArgs& a, kva_dtype w_dtype, void* hb_scratch, cudaStream_t s,
+                          unsigned* n_launches);
 
 // ---------------------------------------------------------------------------------
 struct PrefillArgs {

@@ -11,6 +11,8 @@
 // tied table (Youtu-VL-4B ncnn port, step 6 and "decoding and sampling"; one
 // [vocab, hidden] copy: HunyuanOCR v1.5 ncnn port, section 3.4); the vocab is clamped to
 // the logits length (Penguin-VL ncnn port, section 4.1).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -119,6 +121,120 @@ lmhead_kernel(const __grid_constant__ LmheadArgs a) {
   if (tid == 0) *a.counter = 0u;
 }
 
+// ---------------------------------------------------------------------------------
+// Batch-1 fast path: a grid-stride GEMV over groups of 4 consecutive vocabulary rows per
+// warp.  All 16-byte loads of a group (4 rows x H/256 chunks per lane) are issued before
+// any arithmetic, so each lane keeps 4*H/128 bytes in flight; h lives in registers.
+// ---------------------------------------------------------------------------------
+constexpr int FAST_ROWS = 4;              // rows per warp iteration
+constexpr int FAST_THREADS = 256;
+constexpr int FAST_WARPS = FAST_THREADS / 32;
+
+template <int H>
+__global__ void __launch_bounds__(FAST_THREADS)
+lmhead_b1_kernel(const __grid_constant__ LmheadArgs a) {
+  constexpr int NCH = H / 256;            // 16-byte bf16 chunks per lane per row
+  __shared__ unsigned long long s_best[FAST_WARPS];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  float hv[NCH][8];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>(a.h) + (c * 32 + lane) * 2);
+    const float4 w = __ldg(reinterpret_cast<const float4*>(a.h) + (c * 32 + lane) * 2 + 1);
+    hv[c][0] = u.x; hv[c][1] = u.y; hv[c][2] = u.z; hv[c][3] = u.w;
+    hv[c][4] = w.x; hv[c][5] = w.y; hv[c][6] = w.z; hv[c][7] = w.w;
+  }
+
+  float best_v = -INFINITY;
+  int best_i = 0x7fffffff;
+  const int n_groups = (a.V + FAST_ROWS - 1) / FAST_ROWS;
+  const int gw = blockIdx.x * FAST_WARPS + warp, n_warps = gridDim.x * FAST_WARPS;
+  const uint4* W = reinterpret_cast<const uint4*>(a.W);
+  for (int grp = gw; grp < n_groups; grp += n_warps) {
+    const int r0 = grp * FAST_ROWS;
+    uint4 w[FAST_ROWS][NCH];
+#pragma unroll
+    for (int r = 0; r < FAST_ROWS; ++r) {
+      const int row = min(r0 + r, a.V - 1);          // clamp the ragged last group (value unused)
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) w[r][c] = __ldcs(W + (int64_t)row * (H / 8) + c * 32 + lane);
+    }
+    float dot[FAST_ROWS];
+#pragma unroll
+    for (int r = 0; r < FAST_ROWS; ++r) {
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const uint4 u = w[r][c];
+        acc = fmaf(bf16_lo(u.x), hv[c][0], acc); acc = fmaf(bf16_hi(u.x), hv[c][1], acc);
+        acc = fmaf(bf16_lo(u.y), hv[c][2], acc); acc = fmaf(bf16_hi(u.y), hv[c][3], acc);
+        acc = fmaf(bf16_lo(u.z), hv[c][4], acc); acc = fmaf(bf16_hi(u.z), hv[c][5], acc);
+        acc = fmaf(bf16_lo(u.w), hv[c][6], acc); acc = fmaf(bf16_hi(u.w), hv[c][7], acc);
+      }
+      dot[r] = acc;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int r = 0; r < FAST_ROWS; ++r) dot[r] += __shfl_xor_sync(FULL_MASK, dot[r], o);
+#pragma unroll
+    for (int r = 0; r < FAST_ROWS; ++r) {
+      const int row = r0 + r;
+      if (row < a.V) {
+        if (dot[r] > best_v) { best_v = dot[r]; best_i = row; }   // rows ascend within a warp
+        if (a.logits && lane == r) a.logits[row] = dot[r];
+      }
+    }
+  }
+
+  if (lane == 0) s_best[warp] = best_i == 0x7fffffff ? 0ull : argmax_key(best_v, (uint32_t)best_i);
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long k = 0ull;
+    for (int w2 = 0; w2 < FAST_WARPS; ++w2) k = max(k, s_best[w2]);
+    if (k) atomicMax(&a.best[0], k);
+    __threadfence();
+    s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  if (tid == 0) {
+    __threadfence();
+    const unsigned long long k = atomicExch(&a.best[0], 0ull);
+    a.out_ids[0] = (int32_t)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+    if (a.out_max) a.out_max[0] = float_from_order_bits((uint32_t)(k >> 32));
+    *a.counter = 0u;
+  }
+}
+
+int num_sms_lm() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+template <int H>
+cudaError_t launch_b1(const LmheadArgs& a, cudaStream_t s) {
+  static int per_sm = 0;   // resident CTAs per SM: the grid-stride grid fills the GPU exactly once
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lmhead_b1_kernel<H>, FAST_THREADS, 0) !=
+            cudaSuccess || per_sm <= 0)
+      per_sm = 2;
+  }
+  const int groups = (a.V + FAST_ROWS - 1) / FAST_ROWS;
+  const int want = (groups + FAST_WARPS - 1) / FAST_WARPS;
+  const int grid = std::max(1, std::min(want, num_sms_lm() * per_sm));
+  lmhead_b1_kernel<H><<<grid, FAST_THREADS, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename WT>
 cudaError_t launch_t(const LmheadArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(float) * (size_t)BG * a.H;
@@ -137,13 +253,38 @@ cudaError_t launch_t(const LmheadArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-size_t lmhead_workspace_bytes(int B) {
-  return 256 + sizeof(unsigned long long) * (size_t)(B > 0 ? B : 0);
+bool lmhead_tc_supports(int B, int H);
+size_t lmhead_tc_hb_bytes(int B, int H);
+cudaError_t launch_lmhead_tc(const LmheadArgs& a, uint16_t* hb, cudaStream_t s);
+
+// Workspace: [counter, 256 B][packed best keys, 8 B per batch row, rounded to 256 B]
+//            [bf16 hi/lo copy of h for the batched tensor-core path]
+size_t lmhead_zero_bytes(int B) {
+  return 256 + (sizeof(unsigned long long) * (size_t)(B > 0 ? B : 0) + 255) / 256 * 256;
+}
+
+size_t lmhead_workspace_bytes(int B, int H) {
+  return lmhead_zero_bytes(B) + (B >= 2 ? lmhead_tc_hb_bytes(B, H) : 0);
 }
 
 int lmhead_max_hidden() { return MAX_H; }
 
-cudaError_t launch_lmhead(const LmheadArgs& a, kva_dtype w_dtype, cudaStream_t s) {
+cudaError_t launch_lmhead(const LmheadArgs& a, kva_dtype w_dtype, void* hb_scratch, cudaStream_t s,
+                          unsigned* n_launches) {
+  *n_launches = 1;
+  if (w_dtype == KVA_BF16 && a.B == 1) {
+    switch (a.H) {
+      case 1024: return launch_b1<1024>(a, s);
+      case 2048: return launch_b1<2048>(a, s);
+      case 2560: return launch_b1<2560>(a, s);
+      case 4096: return launch_b1<4096>(a, s);
+      default: break;
+    }
+  }
+  if (w_dtype == KVA_BF16 && hb_scratch && lmhead_tc_supports(a.B, a.H)) {
+    *n_launches = 2;
+    return launch_lmhead_tc(a, static_cast<uint16_t*>(hb_scratch), s);
+  }
   if (w_dtype == KVA_BF16) return launch_t<bf16_t>(a, s);
   return launch_t<float>(a, s);
 }

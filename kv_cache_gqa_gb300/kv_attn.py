@@ -70,8 +70,10 @@ def lib() -> C.CDLL:
         L.kva_decode_workspace_size.restype = sz
         L.kva_decode_workspace_zero_bytes.argtypes = [i32, i32]
         L.kva_decode_workspace_zero_bytes.restype = sz
-        L.kva_lmhead_workspace_size.argtypes = [i32]
+        L.kva_lmhead_workspace_size.argtypes = [i32, i32]
         L.kva_lmhead_workspace_size.restype = sz
+        L.kva_lmhead_workspace_zero_bytes.argtypes = [i32]
+        L.kva_lmhead_workspace_zero_bytes.restype = sz
         L.kva_strerror.argtypes = [C.c_int]
         L.kva_strerror.restype = C.c_char_p
         L.kva_last_error.restype = C.c_char_p
@@ -202,8 +204,8 @@ def decode_workspace_bytes(B: int, n_kv_heads: int, n_q_heads: int, max_len: int
     return int(lib().kva_decode_workspace_size(B, n_kv_heads, n_q_heads, max_len, head_dim))
 
 
-def lmhead_workspace_bytes(B: int) -> int:
-    return int(lib().kva_lmhead_workspace_size(B))
+def lmhead_workspace_bytes(B: int, H: int = 1024) -> int:
+    return int(lib().kva_lmhead_workspace_size(B, H))
 
 
 def kv_attn_decode(q, cache: KVCache, lengths, lengths_host, out, workspace, scale: float = 0.0,

@@ -115,13 +115,15 @@ def test_decode_validation(K):
 
 def test_lmhead_validation(K):
     L = K.lib()
-    def lm(B=1, H=1024, V=100, Vr=100, ws=FAKE, wsb=4096, h=FAKE):
+    def lm(B=1, H=1024, V=100, Vr=100, ws=FAKE, wsb=1 << 20, h=FAKE):
         return L.lmhead_argmax(h, FAKE, 1, B, H, V, Vr, FAKE, None, None, ws, wsb, None)
     assert lm(B=0) == K.KVA_OK
     assert lm(V=101) == K.KVA_EINVAL                                         # vocab beyond the table rows
     assert lm(H=1020) == K.KVA_EALIGN
     assert lm(ws=None) == K.KVA_EWORKSPACE
     assert lm(wsb=8) == K.KVA_EWORKSPACE
+    assert lm(B=64, wsb=L.kva_lmhead_workspace_size(64, 1024) - 1) == K.KVA_EWORKSPACE
+    assert L.kva_lmhead_workspace_size(64, 1024) > L.kva_lmhead_workspace_zero_bytes(64) > 0
     assert lm(h=FAKE + 8) == K.KVA_EALIGN
     assert lm(H=8192) == K.KVA_EUNSUPPORTED
 

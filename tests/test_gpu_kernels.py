@@ -262,7 +262,9 @@ def test_decode_equals_prefill_last_row_fp32(K):
 # ----------------------------------------------------------------------------
 @pytest.mark.parametrize("B,H,V,Vrows,wdt", [(1, 1024, 1000, 1000, "bf16"), (3, 1024, 1001, 1013, "bf16"),
                                              (9, 64, 37, 37, "f32"), (64, 1024, 5000, 5000, "bf16"),
-                                             (1, 8, 300, 300, "f32")])
+                                             (1, 8, 300, 300, "f32"), (1, 1024, 151936, 151936, "bf16"),
+                                             (17, 2048, 3001, 3001, "bf16"), (128, 1024, 1290, 1290, "bf16"),
+                                             (2, 1032, 700, 700, "bf16"), (1, 2560, 999, 1000, "bf16")])
 def test_lmhead_parity(K, B, H, V, Vrows, wdt):
     torch = T()
     rng = np.random.default_rng(B * 1000 + V)
@@ -270,7 +272,8 @@ def test_lmhead_parity(K, B, H, V, Vrows, wdt):
     W = WL.f32_to_bf16_bits(Wf) if wdt == "bf16" else Wf
     h = rng.standard_normal((B, H)).astype(np.float32)
     Wd = dev(W)
-    ws = torch.zeros(K.lmhead_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(K.lmhead_workspace_bytes(B, H), dtype=torch.uint8, device="cuda")
+    zero = K.lib().kva_lmhead_workspace_zero_bytes(B)
     for rep in range(2):
         ids = torch.full((B,), -1, dtype=torch.int32, device="cuda")
         mx = torch.empty((B,), device="cuda")
@@ -287,7 +290,7 @@ def test_lmhead_parity(K, B, H, V, Vrows, wdt):
             else:                            # near-tie: any id within the margin is a valid pick
                 assert z[b, got[b]] >= ref_max[b] - ARGMAX_MARGIN
             assert abs(float(mx[b]) - ref_max[b]) <= 1e-5 * max(1.0, abs(ref_max[b]))
-        assert int(ws.sum()) == 0
+        assert int(ws[:zero].sum()) == 0                 # counter and keys left at zero
 
 
 def test_lmhead_ties_lowest_id_last_row_and_clamp(K):
@@ -299,7 +302,7 @@ def test_lmhead_ties_lowest_id_last_row_and_clamp(K):
     h[1] = -1.0                            # batch 1: every row ties at 0 except the negatives
     W[4098] = 1.0                          # last row: wins for batch 2 / 3 unless clamped
     Wd = dev(W)
-    ws = torch.zeros(K.lmhead_workspace_bytes(4), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(K.lmhead_workspace_bytes(4, H), dtype=torch.uint8, device="cuda")
     ids = torch.empty((4,), dtype=torch.int32, device="cuda")
     K.lmhead_argmax(dev(h), Wd, ids, ws, V=Vrows)
     torch.cuda.synchronize()

@@ -116,7 +116,7 @@ def test_qwen3_28_layers_full(K):
     Wlm = WL.lm_head_weights(1)
     Wd = dev(Wlm)
     hs = WL.hidden_states(2, S_dec + 1)
-    lm_ws = torch.zeros(K.lmhead_workspace_bytes(1), dtype=torch.uint8, device="cuda")
+    lm_ws = torch.zeros(K.lmhead_workspace_bytes(1, 1024), dtype=torch.uint8, device="cuda")
     dec_ws = torch.zeros(K.decode_workspace_bytes(NL, Hkv, Hq, W, D), dtype=torch.uint8, device="cuda")
     ids = torch.empty((S_dec + 1,), dtype=torch.int32, device="cuda")
     K.lmhead_argmax(dev(hs[0]), Wd, ids[0:1], lm_ws)
@@ -280,7 +280,7 @@ def test_batched_serving_decode(K):
     Wlm = WL.lm_head_weights(1)
     Wd = dev(Wlm)
     dec_ws = torch.zeros(K.decode_workspace_bytes(B, Hkv, Hq, W, D), dtype=torch.uint8, device="cuda")
-    lm_ws = torch.zeros(K.lmhead_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    lm_ws = torch.zeros(K.lmhead_workspace_bytes(B, 1024), dtype=torch.uint8, device="cuda")
     sample_steps = (0, 1, 63, 127)
     lm_steps = (0, 127)
     outs, lm_ids, inputs = {}, {}, []
