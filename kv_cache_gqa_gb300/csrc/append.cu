@@ -55,6 +55,11 @@ append_kernel(const __grid_constant__ AppendArgs a) {
   constexpr int HALF = D / 2;
   constexpr int QUARTER = D / 4;
   constexpr int ROWS_PER_PASS = APPEND_WARPS * RPW;
+  constexpr bool POW2 = (LPR & (LPR - 1)) == 0;
+  constexpr bool SHFL_1D = POW2 && HALF % 8 == 0;      // partner lane = lane ^ X1D
+  constexpr int X1D = HALF / 8;
+  constexpr bool SHFL_2D = POW2 && QUARTER % 8 == 0;   // partner lane = lane ^ X2D
+  constexpr int X2D = QUARTER > 8 ? QUARTER / 8 : 1;
   constexpr int MAXP = 2;               // passes whose loads are in flight together
 
   __shared__ float s_cos[D / 2];
@@ -127,8 +132,31 @@ append_kernel(const __grid_constant__ AppendArgs a) {
         }
       }
 
-      // ---- RoPE: partner elements exchanged through the warp's row buffer ----
-      if (a.rope.kind != KVA_ROPE_NONE) {
+      // ---- RoPE ----
+      // Partner of element d is d +- W/2 inside its rotated block of width W.  When W/2 is a
+      // multiple of 8 it sits in lane ^ (W/16) at the same register index (rows are aligned
+      // groups of a power-of-two lane count): one shuffle per element.  Otherwise (D = 72)
+      // the partner goes through the warp's row buffer.
+      const bool two_d = a.rope.kind == KVA_ROPE_2D;
+      if (a.rope.kind != KVA_ROPE_NONE && ((!two_d && SHFL_1D) || (two_d && SHFL_2D))) {
+        const int xm = two_d ? X2D : X1D;
+        const int wh = two_d ? QUARTER : HALF;      // half width of the rotated block
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float pv = __shfl_xor_sync(FULL_MASK, x[p][i], xm);
+          const int d = e0 + i;
+          const int blk = two_d ? d / HALF : 0;
+          const int dd = d - blk * HALF;
+          const bool lo_half = dd < wh;
+          const int j = blk * QUARTER + (lo_half ? dd : dd - wh);   // 1D: blk = 0, j = d mod HALF
+          y[i] = x[p][i] * s_cos[j] + (lo_half ? -pv : pv) * s_sin[j];
+        }
+        if (kind[p] <= 1) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[p][i] = y[i];
+        }
+      } else if (a.rope.kind != KVA_ROPE_NONE) {
         if (lane_on) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) rowbuf[e0 + i] = x[p][i];

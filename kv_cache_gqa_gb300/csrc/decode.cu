@@ -1,4 +1,5 @@
-// Kernel (c): split-KV single-token decode attention over the fixed-window cache.
+// Kernel (c), CUDA-core form (fp32 caches; bf16 caches use decode_mma.cu when TMA is
+// available): split-KV single-token decode attention over the fixed-window cache.
 //
 // Work unit = (chunk c, KV head g, instance b).  A CTA streams its chunk of the K and V
 // rows of head g through a 3-stage shared-memory ring filled by 1-D bulk async copies
@@ -335,8 +336,13 @@ int decode_num_sms() {
   return n;
 }
 
+bool decode_mma_supported();
+cudaError_t launch_decode_mma(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s);
+
+// bf16 caches: tensor-core tiles (decode_mma.cu); fp32 caches: the CUDA-core kernel above.
 cudaError_t launch_decode(const DecodeArgs& a, kva_dtype q_dtype, kva_dtype cache_dtype,
                           cudaStream_t s) {
+  if (cache_dtype == KVA_BF16 && decode_mma_supported()) return launch_decode_mma(a, q_dtype, s);
   if (cache_dtype == KVA_BF16) return launch_t<bf16_t>(a, q_dtype, s);
   return launch_t<float>(a, q_dtype, s);
 }

@@ -1,0 +1,325 @@
+// Kernel (c), bf16-cache form: split-KV decode with the two per-tile contractions on tensor
+// cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+//
+// Work unit = (chunk c, KV head g, instance b): instance b's L_b keys are cut into
+// ceil(L_b / chunk) nearly equal chunks (at most max_chunks), one CTA each.  The CTA's four
+// warps are independent: warp w takes the 16-key tiles w, w+4, ... of the chunk and streams
+// them through a private 3-stage shared-memory ring.  Lane 0 issues the TMA copies (each
+// tile = K and V as two [16 keys x 64 dims] boxes with 128-byte swizzle, so ldmatrix reads
+// are bank-conflict free) and the warp waits on its own mbarriers.  Per tile:
+//   S = q K^T      16 rows (the G query heads of the group, rest zero) x 16 keys, 16 MMAs
+//   online softmax per row in registers (two xor-shuffles across the row's 4 lanes)
+//   O += P V       P reused from the S accumulator as the A fragment, 16 MMAs
+// About 6 instructions per key and KV head instead of ~40 for CUDA-core dot products, so the
+// kernel is limited by HBM, not by issue.  The warps merge (max, sum, O) in shared memory;
+// with several chunks the CTA writes a partial and the last CTA of (b, g) merges them.
+//
+// Method: one query against the valid prefix of the cache window (Youtu-VL-4B ncnn port,
+// step 8), GQA by repeat-interleave grouping (Penguin-VL ncnn port, section 3), softmax as
+// max/subtract/exp/sum/divide (Youtu-VL-4B ncnn port, implementation difficulty 3), bf16
+// storage with fp32 accumulation (HunyuanOCR v1.5 ncnn port, section 3.7).
+#include <mutex>
+
+#include "launch.h"
+#include "tc.cuh"
+
+namespace kva {
+
+namespace {
+
+constexpr int D = DECODE_HEAD_DIM;
+constexpr int WARPS = 4;
+constexpr int THREADS = WARPS * 32;
+constexpr int KT = 16;                          // keys per warp tile
+constexpr int NS = 3;                           // ring stages per warp
+constexpr int BOX = KT * 128;                   // one [16 keys x 64 dims] swizzled box, 2 KB
+constexpr int STAGE = 4 * BOX;                  // K lo, K hi, V lo, V hi
+constexpr int RING = NS * STAGE;                // per warp
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+// D = A B + D, A rows g and g+8 (a1 = a3 = 0: only rows < 8 carry query heads)
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+// byte offset of 16-byte chunk `ch` of key row `key` inside a 128-byte-swizzled box
+__device__ __forceinline__ uint32_t swz(int key, int ch) { return key * 128 + ((ch ^ (key & 7)) << 4); }
+
+template <int G>
+__global__ void __launch_bounds__(THREADS, 2)
+decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, kva_dtype q_dtype) {
+  static_assert(G >= 1 && G <= 8, "query heads per KV head");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = a.lengths[b];
+  const int n_chunks = min(a.max_chunks, (L + a.chunk - 1) / a.chunk);
+  if (c >= n_chunks) return;
+  const int k0 = (int)(((int64_t)L * c) / n_chunks);
+  const int k1 = (int)(((int64_t)L * (c + 1)) / n_chunks);
+  const int n_tiles = (k1 - k0 + KT - 1) / KT;
+
+  unsigned char* ring = smem + warp * RING;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + WARPS * RING) + warp * NS;
+  const int n_mine = n_tiles > warp ? (n_tiles - 1 - warp) / WARPS + 1 : 0;
+  auto issue = [&](int u) {                    // lane 0: tile t = warp + u*WARPS
+    const int ks = k0 + (warp + u * WARPS) * KT;
+    unsigned char* st = ring + (u % NS) * STAGE;
+    mbar_arrive_expect_tx(&bar[u % NS], STAGE);
+    tc::tma_load_4d(st, &tmK, 0, ks, g, b, &bar[u % NS]);
+    tc::tma_load_4d(st + BOX, &tmK, 64, ks, g, b, &bar[u % NS]);
+    tc::tma_load_4d(st + 2 * BOX, &tmV, 0, ks, g, b, &bar[u % NS]);
+    tc::tma_load_4d(st + 3 * BOX, &tmV, 64, ks, g, b, &bar[u % NS]);
+  };
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+    for (int u = 0; u < NS && u < n_mine; ++u) issue(u);
+  }
+  __syncwarp();
+
+  // ---- query A fragments: row r = lane/4 (< G carries head g*G + r), k pairs 2t, 2t+8 ----
+  const int r = lane >> 2, t = lane & 3;
+  uint32_t qa0[8], qa2[8];
+  {
+    const bool on = r < G;
+    const int64_t qb = ((int64_t)b * a.Hq + g * G + (on ? r : 0)) * D;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t lo = 0, hi = 0;
+      if (on) {
+        const int d0 = 16 * kk + 2 * t;
+        if (q_dtype == KVA_BF16) {
+          lo = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(a.q) + qb + d0);
+          hi = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(a.q) + qb + d0 + 8);
+        } else {
+          const float* qf = reinterpret_cast<const float*>(a.q) + qb;
+          lo = pack_bf16x2(qf[d0], qf[d0 + 1]);
+          hi = pack_bf16x2(qf[d0 + 8], qf[d0 + 9]);
+        }
+      }
+      qa0[kk] = lo; qa2[kk] = hi;
+    }
+  }
+
+  float o[16][4];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m = -INFINITY, l = 0.f;                 // statistics of row r (this lane's query head)
+  bool ok = true;
+
+  for (int u = 0; u < n_mine; ++u) {
+    if (!__all_sync(FULL_MASK, mbar_wait_bounded(&bar[u % NS], (uint32_t)((u / NS) & 1)))) { ok = false; break; }
+    unsigned char* st = ring + (u % NS) * STAGE;
+    const int ks = k0 + (warp + u * WARPS) * KT;
+    const int nk = min(KT, k1 - ks);
+    if (nk < KT) {                              // keys past the chunk: zero V so 0 * V stays 0
+      for (int i = lane; i < (KT - nk) * 16; i += 32) {
+        const int key = nk + i / 16, half = (i / 8) & 1, ch = i & 7;
+        *reinterpret_cast<uint4*>(st + (2 + half) * BOX + swz(key, ch)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    const uint32_t sK = smem_u32(st), sV = sK + 2 * BOX;
+
+    // ---- S = q K^T: n-tile 0 = keys 0..7, n-tile 1 = keys 8..15 ----
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int key = rr + 8 * (mi >> 1);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int half = kk >> 2, ch = ((kk & 3) << 1) + (mi & 1);
+        uint32_t bf[4];
+        ldsm_x4(sK + half * BOX + swz(key, ch), bf);
+        mma16816(s0, qa0[kk], qa2[kk], bf[0], bf[1]);
+        mma16816(s1, qa0[kk], qa2[kk], bf[2], bf[3]);
+      }
+    }
+    // ---- online softmax of row r over this tile's keys 2t, 2t+1, 8+2t, 9+2t ----
+    float x[4] = {s0[0] * a.scale_log2, s0[1] * a.scale_log2, s1[0] * a.scale_log2, s1[1] * a.scale_log2};
+    {
+      const int kx[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) if (kx[i] >= nk) x[i] = -INFINITY;
+    }
+    float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    mt = fmaxf(mt, __shfl_xor_sync(FULL_MASK, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(FULL_MASK, mt, 2));
+    const float m_new = fmaxf(m, mt);           // finite: every tile has a valid key
+    const float alpha = exp2f(m - m_new);       // 0 on the first tile
+    float p[4], ps = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { p[i] = exp2f(x[i] - m_new); }
+    const uint32_t pa0 = pack_bf16x2(p[0], p[1]);     // keys 2t, 2t+1
+    const uint32_t pa2 = pack_bf16x2(p[2], p[3]);     // keys 8+2t, 9+2t
+    ps = bf16_lo(pa0) + bf16_hi(pa0) + bf16_lo(pa2) + bf16_hi(pa2);   // the weights P V uses
+    ps += __shfl_xor_sync(FULL_MASK, ps, 1);
+    ps += __shfl_xor_sync(FULL_MASK, ps, 2);
+    l = l * alpha + ps;
+    m = m_new;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) { o[n][0] *= alpha; o[n][1] *= alpha; }
+
+    // ---- O += P V: 16 n-tiles of 8 dims; ldmatrix.trans gives V as the B fragment ----
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int key = rr + 8 * (mi & 1);
+#pragma unroll
+      for (int nd = 0; nd < 8; ++nd) {
+        const int half = nd >> 2, ch = ((nd & 3) << 1) + (mi >> 1);
+        uint32_t bf[4];
+        ldsm_x4_t(sV + half * BOX + swz(key, ch), bf);
+        mma16816(o[2 * nd], pa0, pa2, bf[0], bf[1]);
+        mma16816(o[2 * nd + 1], pa0, pa2, bf[2], bf[3]);
+      }
+    }
+    __syncwarp();                               // all lanes are done with this stage
+    if (lane == 0 && u + NS < n_mine) {
+      fence_proxy_async_smem();                 // order this stage's generic accesses before the refill
+      issue(u + NS);
+    }
+  }
+
+  // ---- merge the warps (rows r < G live in lanes 4r..4r+3) ----
+  __syncthreads();                              // rings drained: reuse them for the merge
+  float* sm_m = reinterpret_cast<float*>(smem);           // [WARPS][G]
+  float* sm_l = sm_m + WARPS * G;                         // [WARPS][G]
+  float* sm_o = sm_l + WARPS * G;                         // [WARPS][G][D]
+  if (r < G) {
+    if (t == 0) { sm_m[warp * G + r] = ok ? m : NAN; sm_l[warp * G + r] = ok ? l : NAN; }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      sm_o[(warp * G + r) * D + 8 * n + 2 * t] = o[n][0];
+      sm_o[(warp * G + r) * D + 8 * n + 2 * t + 1] = o[n][1];
+    }
+  }
+  __syncthreads();
+  __shared__ float s_M[G], s_L[G];
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sm_m[w * G + tid]);
+    float Ls = 0.f;
+    for (int w = 0; w < WARPS; ++w) {
+      const float mw = sm_m[w * G + tid];
+      Ls += (mw == -INFINITY) ? 0.f : exp2f(mw - M) * sm_l[w * G + tid];
+    }
+    s_M[tid] = M; s_L[tid] = Ls;
+  }
+  __syncthreads();
+  const bool single = (n_chunks == 1);
+  for (int idx = tid; idx < G * D; idx += THREADS) {
+    const int hh = idx / D, d = idx % D;
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float mw = sm_m[w * G + hh];
+      if (mw != -INFINITY) tot += exp2f(mw - s_M[hh]) * sm_o[(w * G + hh) * D + d];
+    }
+    const int h = g * G + hh;
+    if (single) {
+      a.out[((int64_t)b * a.Hq + h) * D + d] = tot / s_L[hh];
+    } else {
+      const int64_t pidx = ((int64_t)b * a.Hq + h) * a.max_chunks + c;
+      a.part_acc[pidx * D + d] = tot;
+      if (d == 0) { a.part_ml[2 * pidx] = s_M[hh]; a.part_ml[2 * pidx + 1] = s_L[hh]; }
+    }
+  }
+  if (single) return;
+
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (tid == 0) s_last = (atomicAdd(&a.counters[b * a.Hkv + g], 1u) == (unsigned)(n_chunks - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int idx = tid; idx < G * D; idx += THREADS) {
+    const int hh = idx / D, d = idx % D;
+    const int64_t p0 = ((int64_t)b * a.Hq + g * G + hh) * a.max_chunks;
+    float M = -INFINITY;
+    for (int cc = 0; cc < n_chunks; ++cc) M = fmaxf(M, __ldcg(&a.part_ml[2 * (p0 + cc)]));
+    float num = 0.f, den = 0.f;
+    for (int cc = 0; cc < n_chunks; ++cc) {
+      const float w = exp2f(__ldcg(&a.part_ml[2 * (p0 + cc)]) - M);
+      num = fmaf(w, __ldcg(&a.part_acc[(p0 + cc) * D + d]), num);
+      den = fmaf(w, __ldcg(&a.part_ml[2 * (p0 + cc) + 1]), den);
+    }
+    a.out[((int64_t)b * a.Hq + g * G + hh) * D + d] = num / den;
+  }
+  if (tid == 0) a.counters[b * a.Hkv + g] = 0u;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn_dec() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Whole cache as (head_dim, slot, kv head, instance); boxes of [16 slots x 64 dims].
+cudaError_t make_map(CUtensorMap* map, const void* base, const DecodeArgs& a) {
+  EncodeTiledFn fn = encode_fn_dec();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.capacity, (cuuint64_t)a.Hkv, (cuuint64_t)a.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)a.capacity * D * 2, (cuuint64_t)a.inst_stride * 2};
+  const cuuint32_t box[4] = {64, KT, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int G>
+cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
+  const size_t smem = (size_t)WARPS * RING + WARPS * NS * 8 + 1024;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  CUtensorMap mk, mv;
+  cudaError_t e = make_map(&mk, a.kc, a);
+  if (e != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.vc, a)) != cudaSuccess) return e;
+  dim3 grid(a.max_chunks, a.Hkv, a.B);
+  decode_mma_kernel<G><<<grid, THREADS, smem, s>>>(a, mk, mv, q_dtype);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_mma_supported() { return encode_fn_dec() != nullptr; }
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_g<1>(a, q_dtype, s);
+    case 2: return launch_g<2>(a, q_dtype, s);
+    case 4: return launch_g<4>(a, q_dtype, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kva

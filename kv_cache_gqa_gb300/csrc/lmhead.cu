@@ -209,6 +209,107 @@ lmhead_b1_kernel(const __grid_constant__ LmheadArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------------
+// Batch-1 pipelined path: one CTA per SM owns a contiguous slice of the table and streams it
+// through a 4-stage shared-memory ring, one 32 KB bulk copy per stage (the slice's rows are
+// contiguous in memory).  Bytes in flight cost no registers, so each SM keeps ~96 KB moving.
+// The 8 warps reduce the staged rows with conflict-free 128-bit shared-memory reads.
+// ---------------------------------------------------------------------------------
+constexpr int PIPE_STAGE_BYTES = 32768;
+constexpr int PIPE_STAGES = 4;
+constexpr int PIPE_THREADS = 256;
+constexpr int PIPE_WARPS = PIPE_THREADS / 32;
+
+template <int H>
+__global__ void __launch_bounds__(PIPE_THREADS, 1)
+lmhead_b1_pipe_kernel(const __grid_constant__ LmheadArgs a, int rows_per_cta) {
+  constexpr int ROWB = H * 2;
+  constexpr int RPS = PIPE_STAGE_BYTES / ROWB;         // rows per stage
+  constexpr int NCH = H / 256;                         // 16-byte chunks per lane per row
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ __align__(8) uint64_t full[PIPE_STAGES], empty[PIPE_STAGES];
+  __shared__ unsigned long long s_best[PIPE_WARPS];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r0 = blockIdx.x * rows_per_cta;
+  const int r1 = min(a.V, r0 + rows_per_cta);
+  const int n_st = r1 > r0 ? (r1 - r0 + RPS - 1) / RPS : 0;
+  const unsigned char* W = reinterpret_cast<const unsigned char*>(a.W);
+  auto issue = [&](int it) {
+    const int rs = r0 + it * RPS;
+    const uint32_t bytes = (uint32_t)(min(RPS, r1 - rs) * ROWB);
+    mbar_arrive_expect_tx(&full[it % PIPE_STAGES], bytes);
+    bulk_g2s(ring + (it % PIPE_STAGES) * PIPE_STAGE_BYTES, W + (int64_t)rs * ROWB, bytes, &full[it % PIPE_STAGES]);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < PIPE_STAGES; ++st) { mbar_init(&full[st], 1); mbar_init(&empty[st], PIPE_WARPS); }
+    fence_mbar_init();
+    for (int it = 0; it < PIPE_STAGES && it < n_st; ++it) issue(it);
+  }
+  float hv[NCH][8];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>(a.h) + (c * 32 + lane) * 2);
+    const float4 w = __ldg(reinterpret_cast<const float4*>(a.h) + (c * 32 + lane) * 2 + 1);
+    hv[c][0] = u.x; hv[c][1] = u.y; hv[c][2] = u.z; hv[c][3] = u.w;
+    hv[c][4] = w.x; hv[c][5] = w.y; hv[c][6] = w.z; hv[c][7] = w.w;
+  }
+  __syncthreads();
+
+  float best_v = -INFINITY;
+  int best_i = 0x7fffffff;
+  bool ok = true;
+  for (int it = 0; it < n_st; ++it) {
+    const int st = it % PIPE_STAGES;
+    if (!__all_sync(FULL_MASK, mbar_wait_bounded(&full[st], (uint32_t)((it / PIPE_STAGES) & 1)))) { ok = false; break; }
+    const int rs = r0 + it * RPS;
+    const int nr = min(RPS, r1 - rs);
+    const unsigned char* base = ring + st * PIPE_STAGE_BYTES;
+    for (int rr = warp; rr < nr; rr += PIPE_WARPS) {
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(base + rr * ROWB + (c * 32 + lane) * 16);
+        acc = fmaf(bf16_lo(u.x), hv[c][0], acc); acc = fmaf(bf16_hi(u.x), hv[c][1], acc);
+        acc = fmaf(bf16_lo(u.y), hv[c][2], acc); acc = fmaf(bf16_hi(u.y), hv[c][3], acc);
+        acc = fmaf(bf16_lo(u.z), hv[c][4], acc); acc = fmaf(bf16_hi(u.z), hv[c][5], acc);
+        acc = fmaf(bf16_lo(u.w), hv[c][6], acc); acc = fmaf(bf16_hi(u.w), hv[c][7], acc);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
+      const int row = rs + rr;
+      if (acc > best_v) { best_v = acc; best_i = row; }          // rows ascend within a warp
+      if (a.logits && lane == 0) a.logits[row] = acc;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    if (tid == 0 && it + PIPE_STAGES < n_st) {
+      // refill this stage once every warp has released it
+      if (!mbar_wait_bounded(&empty[st], (uint32_t)((it / PIPE_STAGES) & 1))) { ok = false; }
+      else issue(it + PIPE_STAGES);
+    }
+  }
+
+  if (lane == 0) s_best[warp] = (!ok || best_i == 0x7fffffff) ? 0ull : argmax_key(best_v, (uint32_t)best_i);
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long k = 0ull;
+    for (int w2 = 0; w2 < PIPE_WARPS; ++w2) k = max(k, s_best[w2]);
+    if (k) atomicMax(&a.best[0], k);
+    __threadfence();
+    s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  if (tid == 0) {
+    __threadfence();
+    const unsigned long long k = atomicExch(&a.best[0], 0ull);
+    a.out_ids[0] = k ? (int32_t)(0xffffffffu - (uint32_t)(k & 0xffffffffull)) : -1;
+    if (a.out_max) a.out_max[0] = float_from_order_bits((uint32_t)(k >> 32));
+    *a.counter = 0u;
+  }
+}
+
 int num_sms_lm() {
   static int n = 0;
   if (n == 0) {
@@ -268,6 +369,21 @@ size_t lmhead_workspace_bytes(int B, int H) {
 }
 
 int lmhead_max_hidden() { return MAX_H; }
+
+template <int H>
+cudaError_t launch_b1_pipe(const LmheadArgs& a, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(lmhead_b1_pipe_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PIPE_STAGES * PIPE_STAGE_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = num_sms_lm();
+  const int rows_per_cta = (a.V + grid - 1) / grid;
+  lmhead_b1_pipe_kernel<H><<<grid, PIPE_THREADS, PIPE_STAGES * PIPE_STAGE_BYTES, s>>>(a, rows_per_cta);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_lmhead(const LmheadArgs& a, kva_dtype w_dtype, void* hb_scratch, cudaStream_t s,
                           unsigned* n_launches) {

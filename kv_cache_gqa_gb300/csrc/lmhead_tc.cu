@@ -274,7 +274,7 @@ cudaError_t launch_bp(const LmheadArgs& a, uint16_t* hb, cudaStream_t s) {
 }  // namespace
 
 bool lmhead_tc_supports(int B, int H) {
-  return B >= 2 && B <= 64 && H % KC == 0 && encode_fn_lm() != nullptr;
+  return B >= 2 && B <= MAX_N / 2 && H % KC == 0 && encode_fn_lm() != nullptr;
 }
 
 // Bytes of the bf16 hi/lo copy of h the batched path keeps in the workspace.
