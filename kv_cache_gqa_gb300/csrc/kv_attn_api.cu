@@ -103,7 +103,6 @@ kva_status build_rope(const kva_rope& r, int D, RopeTable* t) {
 
 constexpr int DECODE_MAX_CHUNKS = 64;
 constexpr int DECODE_CHUNK_ALIGN = 64;
-constexpr int DECODE_MAX_CHUNK_TARGET = 8192;
 
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
@@ -122,18 +121,43 @@ int decode_max_chunks_bound(int max_len) {
 
 void set_last_error(const char* msg) { std::snprintf(g_msg, sizeof(g_msg), "%s", msg); }
 
-// About three waves of resident decode CTAs (two per SM) over all (instance, KV head) pairs.
+// Split-KV plan.  Instance b is cut into ceil(L_b / chunk) chunks, one CTA each.  Candidate
+// chunk sizes are ceil(max_len / k) (k = 1..64, rounded up to 64 keys); each is scored with a
+// simple cost model and the cheapest wins:
+//   one wave:   fixed cost + max(all bytes / HBM bandwidth, one chunk / one CTA's share)
+//   more waves: waves x fixed cost + all bytes / HBM bandwidth + one chunk / share (the tail)
+// (fixed cost = a CTA's first DRAM round trip and its merge)
+// Short contexts thus get one wave of whole-instance CTAs (no partials to merge); long, ragged
+// contexts get a few waves of equal chunks so that no CTA runs long past the others.
 int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len) {
+  constexpr double T_FIX_US = 3.0;           // per-wave fixed cost
+  constexpr double BW = 6.5e6;               // bytes per microsecond (HBM)
+  constexpr double ROW = 512.0;              // bytes per key and KV head (bf16 K + V, D = 128)
+  const double slots = 2.0 * decode_num_sms();
   long long total = 0;
   for (int b = 0; b < B; ++b) total += lengths[b];
-  total *= Hkv;                                           // key rows over all (instance, head)
-  const long long target_ctas = 3LL * 2 * decode_num_sms();
-  long long chunk = (total + target_ctas - 1) / target_ctas;
-  chunk = std::min<long long>(chunk, DECODE_MAX_CHUNK_TARGET);
-  const long long floor_chunk = (max_len + DECODE_MAX_CHUNKS - 1) / DECODE_MAX_CHUNKS;
-  chunk = std::max<long long>(chunk, floor_chunk);
-  chunk = std::max<long long>(DECODE_CHUNK_ALIGN, round_up((size_t)chunk, DECODE_CHUNK_ALIGN));
-  return (int)chunk;
+  const double total_bytes = (double)total * Hkv * ROW;
+  int best_chunk = 0;
+  double best_t = 1e300;
+  int prev = -1;
+  const int k_max = B > 4096 ? 1 : DECODE_MAX_CHUNKS;       // keep host planning cheap
+  for (int k = 1; k <= k_max; ++k) {
+    int chunk = (max_len + k - 1) / k;
+    chunk = std::max(DECODE_CHUNK_ALIGN, (int)round_up((size_t)chunk, DECODE_CHUNK_ALIGN));
+    if (chunk == prev) continue;
+    prev = chunk;
+    long long ctas = 0;
+    for (int b = 0; b < B; ++b) ctas += (lengths[b] + chunk - 1) / chunk;
+    ctas *= Hkv;
+    const double waves = std::ceil((double)ctas / slots);
+    const double share = BW / std::min((double)ctas, slots);
+    const double chunk_t = (double)chunk * ROW / share;  // one CTA's chunk at its bandwidth share
+    const double t = waves <= 1.0 ? T_FIX_US + std::max(total_bytes / BW, chunk_t)
+                                  : waves * T_FIX_US + total_bytes / BW + chunk_t;   // + tail of the last wave
+    if (t < best_t - 1e-9) { best_t = t; best_chunk = chunk; }
+  }
+  const int floor_chunk = (max_len + DECODE_MAX_CHUNKS - 1) / DECODE_MAX_CHUNKS;
+  return std::max(best_chunk, (int)round_up((size_t)std::max(floor_chunk, 1), DECODE_CHUNK_ALIGN));
 }
 
 }  // namespace kva

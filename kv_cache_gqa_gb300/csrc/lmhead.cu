@@ -390,10 +390,10 @@ cudaError_t launch_lmhead(const LmheadArgs& a, kva_dtype w_dtype, void* hb_scrat
   *n_launches = 1;
   if (w_dtype == KVA_BF16 && a.B == 1) {
     switch (a.H) {
-      case 1024: return launch_b1<1024>(a, s);
-      case 2048: return launch_b1<2048>(a, s);
+      case 1024: return launch_b1_pipe<1024>(a, s);
+      case 2048: return launch_b1_pipe<2048>(a, s);
       case 2560: return launch_b1<2560>(a, s);
-      case 4096: return launch_b1<4096>(a, s);
+      case 4096: return launch_b1_pipe<4096>(a, s);
       default: break;
     }
   }
