@@ -4,8 +4,9 @@
 One benchmark step = one whole generation job through the C ABI:
   * prefill: fused QK-Norm+RoPE+cache append of 512 tokens into 28 layer caches, then causal
     flash prefill attention of all 28 layers, then the lm_head argmax;
-  * 256 decode steps, each: append of the new token into the 28 caches, split-KV decode
-    attention of the 28 layers over the 1024-slot window, lm_head argmax (151936 x 1024 bf16).
+  * 256 decode steps, each: one launch that appends the new token to the 28 layer caches and
+    runs split-KV decode attention of the 28 layers over the valid prefix of the 1024-slot
+    window, then the lm_head argmax (151936 x 1024 bf16).
 Inputs are synthetic (seeded), resident in HBM; the job is captured once as a CUDA graph.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead (the only
@@ -52,8 +53,10 @@ def prefill_flops():
 
 
 def decode_bytes(L):
+    """One fused decode step over L valid slots (the new token's included): bf16 K and V rows
+    read, fp32 q/k/v of the new token in, its bf16 K/V row written, fp32 attention out."""
     kv = LAYERS * HKV * L * D * 2 * 2
-    return kv + LAYERS * HQ * D * (2 + 4)          # + bf16 q in, fp32 out
+    return kv + LAYERS * ((HQ + 2 * HKV) * D * 4 + 2 * HKV * D * 2 + HQ * D * 4)
 
 
 def lmhead_bytes(B=1):
@@ -156,7 +159,7 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 class Qwen3Job:
     """Resident inputs, caches and workspaces of one generation job; `record(stream)` enqueues
-    the job's 771 kernel launches (optionally bracketing each with timing events)."""
+    the job's 515 kernel launches (optionally bracketing each with timing events)."""
 
     def __init__(self, seed=0):
         import torch
@@ -177,12 +180,10 @@ class Qwen3Job:
         self.rope = K.Rope("1d", 1e6)
         self.q_pre = torch.empty((LAYERS, PROMPT, HQ, D), device=dev, dtype=torch.bfloat16)
         self.out_pre = torch.empty((LAYERS, PROMPT, HQ, D), device=dev)
-        self.q_dec = torch.empty((STEPS, LAYERS, 1, HQ, D), device=dev, dtype=torch.bfloat16)
         self.out_dec = torch.empty((STEPS, LAYERS, HQ, D), device=dev)
         self.pre_slot = np.arange(PROMPT, dtype=np.int32)[None]
         self.pre_slot_d = torch.from_numpy(self.pre_slot).to(dev)
         self.pre_pos_d = torch.arange(PROMPT, dtype=torch.int32, device=dev)[None, :, None].contiguous()
-        self.step_slot = [np.array([[PROMPT + s]], np.int32) for s in range(STEPS)]
         self.step_slot_d = torch.arange(PROMPT, PROMPT + STEPS, dtype=torch.int32, device=dev).view(STEPS, 1, 1)
         self.len_host = [np.full(LAYERS, PROMPT + s + 1, np.int32) for s in range(STEPS)]
         self.len_d = torch.from_numpy(np.stack(self.len_host)).to(dev)
@@ -213,18 +214,16 @@ class Qwen3Job:
         K.lmhead_argmax(self.h[0], self.W, self.ids[0:1], self.lm_ws)
         self._ev("lm_head")
         for s in range(STEPS):
-            K.kv_cache_append_rope_qknorm(self.dq[s], self.dk[s], self.dv[s], self.step_slot_d[s:s + 1],
-                                          self.step_slot_d[s], self.step_slot[s], c, self.q_dec[s], self.rope,
-                                          q_norm_w=self.qw, k_norm_w=self.kw, eps=1e-6, norm_inst_stride=D)
-            self._ev("append_dec")
-            K.kv_attn_decode(self.q_dec[s, :, 0], c, self.len_d[s], self.len_host[s], self.out_dec[s], self.dec_ws)
+            K.kv_attn_decode_step(self.dq[s, :, 0], self.dk[s, :, 0], self.dv[s, :, 0], self.step_slot_d[s], c,
+                                  self.len_d[s], self.len_host[s], self.out_dec[s], self.dec_ws, self.rope,
+                                  q_norm_w=self.qw, k_norm_w=self.kw, eps=1e-6, norm_inst_stride=D)
             self._ev("decode")
             K.lmhead_argmax(self.h[s + 1], self.W, self.ids[s + 1:s + 2], self.lm_ws)
             self._ev("lm_head")
 
     def kernel_times_ms(self):
         """Per-kind launch durations (ms) of the last replay, from consecutive events."""
-        order = ["t0", "append_pre", "prefill", "lm_head"] + ["append_dec", "decode", "lm_head"] * STEPS
+        order = ["t0", "append_pre", "prefill", "lm_head"] + ["decode", "lm_head"] * STEPS
         seq, idx = [], {}
         for key in order:
             i = idx.get(key, 0); idx[key] = i + 1
@@ -353,7 +352,7 @@ def run_gpu(args, rank, world, local_rank):
                 "algorithmic_bytes_per_launch": lmhead_bytes(), "avg_launch_us": round(lm_ms * 1e3, 2),
                 "peak_source": f"{peak_src} hbm_gbs"}
         if dominant == "decode":
-            roof.update({"kernel": "kv_attn_decode", "achieved": round(dec_gbs, 1), "frac": round(dec_gbs / hbm, 4),
+            roof.update({"kernel": "kv_attn_decode_step", "achieved": round(dec_gbs, 1), "frac": round(dec_gbs / hbm, 4),
                          "traffic": None, "algorithmic_bytes_per_launch": int(np.mean(dec_bytes)),
                          "avg_launch_us": round(statistics.mean(dec_ms) * 1e3, 2)})
         line = {
@@ -372,13 +371,12 @@ def run_gpu(args, rank, world, local_rank):
             "gpu_launches": int(launches_per_job * args.steps),
             "roofline": roof,
             "kernels": {
-                "decode_attn": {"GB/s": round(dec_gbs, 1), "frac_hbm": round(dec_gbs / hbm, 4),
+                "decode_step": {"GB/s": round(dec_gbs, 1), "frac_hbm": round(dec_gbs / hbm, 4),
                                 "avg_launch_us": round(statistics.mean(dec_ms) * 1e3, 2)},
                 "prefill_attn": {"TFLOP/s": round(pre_tf, 2), "frac_bf16": round(pre_tf / bf16, 4),
                                  "launch_us": round(pre_ms * 1e3, 1), "flops": prefill_flops()},
                 "append_prefill": {"GB/s": round(app_gbs, 1), "frac_hbm": round(app_gbs / hbm, 4),
                                    "launch_us": round(app_ms * 1e3, 1)},
-                "append_decode": {"avg_launch_us": round(statistics.mean(kt["append_dec"]) * 1e3, 2)},
                 "lm_head": {"GB/s": round(lm_gbs, 1), "frac_hbm": round(lm_gbs / hbm, 4),
                             "avg_launch_us": round(lm_ms * 1e3, 2)},
                 "time_share": {k: round(v / sum(totals.values()), 4) for k, v in totals.items()},

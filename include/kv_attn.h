@@ -180,6 +180,31 @@ kva_status kv_attn_decode(
     const int32_t* lengths, const int32_t* lengths_host, int32_t B, int32_t n_q_heads,
     float scale, float* out, void* workspace, size_t workspace_bytes, kva_stream stream);
 
+/* ---------------------------------------------------------------------------------
+ * kv_attn_decode_step
+ *   One decode step in one launch: the append of the new token followed by decode
+ *   attention, i.e. exactly
+ *     kv_cache_append_rope_qknorm(q, k, v, T = 1, slot = L_b - 1, ...)   then
+ *     kv_attn_decode(q_out, lengths, ...)
+ *   (the runtime writes the new k/v into the cache between the qkv and the attention step:
+ *   Youtu-VL-4B ncnn port, step 6; each step attends to the whole prefix: step 8).  Every
+ *   CTA derives the normalised, rotated query rows of its group itself; the CTA that owns the
+ *   last chunk of an instance also writes the new K/V row into slot L_b - 1.
+ *  q        [B,Hq,D], k, v [B,Hkv,D] of in_dtype: the new token's projections (device)
+ *  pos      [.., n_axes] int32 position ids (device); instance b reads pos + b*pos_inst_stride
+ *  lengths  [B] valid slots including the new token (device) + lengths_host (host mirror)
+ *  q_out    nullable [B,Hq,D] of q_out_dtype: the transformed queries, if wanted
+ *  out      [B,Hq,D] float32;  workspace as for kv_attn_decode
+ *  Requires a bf16 cache with head_dim 128 and Hq/Hkv in {1, 2, 4} (else KVA_EUNSUPPORTED:
+ *  call the two entry points).  Errors as the two calls it replaces. */
+kva_status kv_attn_decode_step(
+    const void* q, const void* k, const void* v, kva_dtype in_dtype,
+    const int32_t* pos, int64_t pos_inst_stride,
+    kva_qknorm norm, kva_rope rope, kva_cache cache,
+    const int32_t* lengths, const int32_t* lengths_host, int32_t B, int32_t n_q_heads,
+    float scale, void* q_out, kva_dtype q_out_dtype, float* out,
+    void* workspace, size_t workspace_bytes, kva_stream stream);
+
 size_t kva_decode_workspace_size(int32_t B, int32_t n_kv_heads, int32_t n_q_heads,
                                  int32_t max_len, int32_t head_dim);
 size_t kva_decode_workspace_zero_bytes(int32_t B, int32_t n_kv_heads);

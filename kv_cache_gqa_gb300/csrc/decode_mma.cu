@@ -54,10 +54,66 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2
 // byte offset of 16-byte chunk `ch` of key row `key` inside a 128-byte-swizzled box
 __device__ __forceinline__ uint32_t swz(int key, int ch) { return key * 128 + ((ch ^ (key & 7)) << 4); }
 
-template <int G>
+// Reduce the angle a = pos * inv_freq (float64) into [-pi, pi] before the float32 sin/cos.
+__device__ __forceinline__ void step_cos_sin(int32_t p, double inv, float* c, float* s) {
+  const double x = (double)p * inv;
+  const double k = rint(x * 0.15915494309189535);
+  sincosf((float)fma(-k, 6.283185307179586, x), s, c);
+}
+
+// One 128-wide row of the new token (lane owns dims 4*lane .. 4*lane+3): QK-Norm and RoPE in
+// the configured order for q/k rows (w != null or rope), untouched for v rows.
+__device__ __forceinline__ void step_row(float (&x)[4], const float* w, bool rotate, const StepArgs& st,
+                                         const float* s_cos, const float* s_sin, int lane) {
+  auto rms = [&](void) {
+    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+    return 1.0f / sqrtf(ss / (float)D + st.eps);
+  };
+  if (w && !st.after_rope) {
+    const float r = rms();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = x[i] * r * w[4 * lane + i];
+  }
+  if (rotate) {
+    // partner of dim d: d +- 64 (lane ^ 16) for 1D / sections, d +- 32 inside a half (lane ^ 8) for 2D
+    const bool two_d = st.rope.kind == KVA_ROPE_2D;
+    float y[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float pv = __shfl_xor_sync(FULL_MASK, x[i], two_d ? 8 : 16);
+      const int d = 4 * lane + i;
+      const int blk = two_d ? d / 64 : 0, dd = two_d ? d % 64 : d, wh = two_d ? 32 : 64;
+      const bool lo = dd < wh;
+      const int j = blk * 32 + (lo ? dd : dd - wh);
+      y[i] = x[i] * s_cos[j] + (lo ? -pv : pv) * s_sin[j];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = y[i];
+  }
+  if (w && st.after_rope) {
+    const float r = rms();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = x[i] * r * w[4 * lane + i];
+  }
+}
+
+__device__ __forceinline__ void load4(const void* p, int dt, int64_t i, float (&x)[4]) {
+  if (dt == KVA_BF16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p) + i);
+    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+  } else {
+    const float4 u = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + i);
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+  }
+}
+
+template <int G, bool FUSED>
 __global__ void __launch_bounds__(THREADS, 2)
 decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, kva_dtype q_dtype) {
+                  const __grid_constant__ CUtensorMap tmV, kva_dtype q_dtype,
+                  const __grid_constant__ StepArgs st) {
   static_assert(G >= 1 && G <= 8, "query heads per KV head");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -75,12 +131,12 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   const int n_mine = n_tiles > warp ? (n_tiles - 1 - warp) / WARPS + 1 : 0;
   auto issue = [&](int u) {                    // lane 0: tile t = warp + u*WARPS
     const int ks = k0 + (warp + u * WARPS) * KT;
-    unsigned char* st = ring + (u % NS) * STAGE;
+    unsigned char* dst = ring + (u % NS) * STAGE;
     mbar_arrive_expect_tx(&bar[u % NS], STAGE);
-    tc::tma_load_4d(st, &tmK, 0, ks, g, b, &bar[u % NS]);
-    tc::tma_load_4d(st + BOX, &tmK, 64, ks, g, b, &bar[u % NS]);
-    tc::tma_load_4d(st + 2 * BOX, &tmV, 0, ks, g, b, &bar[u % NS]);
-    tc::tma_load_4d(st + 3 * BOX, &tmV, 64, ks, g, b, &bar[u % NS]);
+    tc::tma_load_4d(dst, &tmK, 0, ks, g, b, &bar[u % NS]);
+    tc::tma_load_4d(dst + BOX, &tmK, 64, ks, g, b, &bar[u % NS]);
+    tc::tma_load_4d(dst + 2 * BOX, &tmV, 0, ks, g, b, &bar[u % NS]);
+    tc::tma_load_4d(dst + 3 * BOX, &tmV, 64, ks, g, b, &bar[u % NS]);
   };
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
@@ -89,10 +145,56 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   }
   __syncwarp();
 
+  // ---- fused step: transform the new token's rows (q of the G heads; k, v in the last chunk) ----
+  __shared__ float s_cos[D / 2], s_sin[D / 2];
+  __shared__ __align__(16) uint16_t s_q[G][D], s_kv[2][D];
+  const bool last_chunk = (c == n_chunks - 1);
+  if constexpr (FUSED) {
+    const bool rotate = st.rope.kind != KVA_ROPE_NONE;
+    if (rotate && tid < D / 2)
+      step_cos_sin(st.pos[(int64_t)b * st.pos_stride + st.rope.axis[tid]], st.rope.inv[tid], &s_cos[tid], &s_sin[tid]);
+    __syncthreads();
+    for (int rr = warp; rr < G + 2; rr += WARPS) {          // rows: G queries, then k, then v
+      if (rr >= G && !last_chunk) continue;                 // only the last chunk owns the new key
+      float x[4];
+      const float* w = nullptr;
+      if (rr < G) {
+        load4(st.q, st.in_dtype, ((int64_t)b * a.Hq + g * G + rr) * D + 4 * lane, x);
+        w = st.q_w ? st.q_w + (int64_t)b * st.w_stride : nullptr;
+      } else {
+        load4(rr == G ? st.k : st.v, st.in_dtype, ((int64_t)b * a.Hkv + g) * D + 4 * lane, x);
+        w = (rr == G && st.k_w) ? st.k_w + (int64_t)b * st.w_stride : nullptr;
+      }
+      step_row(x, w, rotate && rr <= G, st, s_cos, s_sin, lane);
+      const uint32_t p01 = pack_bf16x2(x[0], x[1]), p23 = pack_bf16x2(x[2], x[3]);
+      if (rr < G) {
+        *reinterpret_cast<uint2*>(&s_q[rr][4 * lane]) = make_uint2(p01, p23);
+        if (st.q_out && c == 0) {
+          const int64_t qo = ((int64_t)b * a.Hq + g * G + rr) * D + 4 * lane;
+          if (st.q_out_dtype == KVA_BF16) *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(st.q_out) + qo) = make_uint2(p01, p23);
+          else *reinterpret_cast<float4*>(reinterpret_cast<float*>(st.q_out) + qo) = make_float4(x[0], x[1], x[2], x[3]);
+        }
+      } else {
+        *reinterpret_cast<uint2*>(&s_kv[rr - G][4 * lane]) = make_uint2(p01, p23);
+        // the cache keeps the new row for later steps (slot L-1 of this instance and head)
+        unsigned char* dst = reinterpret_cast<unsigned char*>(rr == G ? const_cast<void*>(a.kc) : const_cast<void*>(a.vc)) +
+                             ((int64_t)b * a.inst_stride + ((int64_t)g * a.capacity + (L - 1)) * D + 4 * lane) * 2;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(p01, p23);
+      }
+    }
+    __syncthreads();
+  }
+
   // ---- query A fragments: row r = lane/4 (< G carries head g*G + r), k pairs 2t, 2t+8 ----
   const int r = lane >> 2, t = lane & 3;
   uint32_t qa0[8], qa2[8];
-  {
+  if constexpr (FUSED) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      qa0[kk] = r < G ? *reinterpret_cast<const uint32_t*>(&s_q[r < G ? r : 0][16 * kk + 2 * t]) : 0u;
+      qa2[kk] = r < G ? *reinterpret_cast<const uint32_t*>(&s_q[r < G ? r : 0][16 * kk + 8 + 2 * t]) : 0u;
+    }
+  } else {
     const bool on = r < G;
     const int64_t qb = ((int64_t)b * a.Hq + g * G + (on ? r : 0)) * D;
 #pragma unroll
@@ -121,17 +223,34 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
 
   for (int u = 0; u < n_mine; ++u) {
     if (!__all_sync(FULL_MASK, mbar_wait_bounded(&bar[u % NS], (uint32_t)((u / NS) & 1)))) { ok = false; break; }
-    unsigned char* st = ring + (u % NS) * STAGE;
+    unsigned char* stg = ring + (u % NS) * STAGE;
     const int ks = k0 + (warp + u * WARPS) * KT;
     const int nk = min(KT, k1 - ks);
     if (nk < KT) {                              // keys past the chunk: zero V so 0 * V stays 0
       for (int i = lane; i < (KT - nk) * 16; i += 32) {
         const int key = nk + i / 16, half = (i / 8) & 1, ch = i & 7;
-        *reinterpret_cast<uint4*>(st + (2 + half) * BOX + swz(key, ch)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(stg + (2 + half) * BOX + swz(key, ch)) = make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
     }
-    const uint32_t sK = smem_u32(st), sV = sK + 2 * BOX;
+    if constexpr (FUSED) {
+      // the tile holding slot L-1 gets the freshly computed row (the TMA may have read the
+      // cache before this CTA's own global write landed)
+      const int row = (L - 1) - ks;
+      if (last_chunk && row >= 0 && row < nk) {
+        if (lane < 16) {
+          const int half = lane >> 3, ch = lane & 7;
+          *reinterpret_cast<uint4*>(stg + half * BOX + swz(row, ch)) =
+              *reinterpret_cast<const uint4*>(&s_kv[0][half * 64 + ch * 8]);
+        } else {
+          const int half = (lane - 16) >> 3, ch = lane & 7;
+          *reinterpret_cast<uint4*>(stg + (2 + half) * BOX + swz(row, ch)) =
+              *reinterpret_cast<const uint4*>(&s_kv[1][half * 64 + ch * 8]);
+        }
+        __syncwarp();
+      }
+    }
+    const uint32_t sK = smem_u32(stg), sV = sK + 2 * BOX;
 
     // ---- S = q K^T: n-tile 0 = keys 0..7, n-tile 1 = keys 8..15 ----
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -291,12 +410,13 @@ cudaError_t make_map(CUtensorMap* map, const void* base, const DecodeArgs& a) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int G>
-cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
+template <int G, bool FUSED>
+cudaError_t launch_g(const DecodeArgs& a, const StepArgs& st, kva_dtype q_dtype, cudaStream_t s) {
   const size_t smem = (size_t)WARPS * RING + WARPS * NS * 8 + 1024;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -305,7 +425,7 @@ cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if ((e = make_map(&mv, a.vc, a)) != cudaSuccess) return e;
   dim3 grid(a.max_chunks, a.Hkv, a.B);
-  decode_mma_kernel<G><<<grid, THREADS, smem, s>>>(a, mk, mv, q_dtype);
+  decode_mma_kernel<G, FUSED><<<grid, THREADS, smem, s>>>(a, mk, mv, q_dtype, st);
   return cudaGetLastError();
 }
 
@@ -314,10 +434,22 @@ cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
 bool decode_mma_supported() { return encode_fn_dec() != nullptr; }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
+  const StepArgs none{};
   switch (a.Hq / a.Hkv) {
-    case 1: return launch_g<1>(a, q_dtype, s);
-    case 2: return launch_g<2>(a, q_dtype, s);
-    case 4: return launch_g<4>(a, q_dtype, s);
+    case 1: return launch_g<1, false>(a, none, q_dtype, s);
+    case 2: return launch_g<2, false>(a, none, q_dtype, s);
+    case 4: return launch_g<4, false>(a, none, q_dtype, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+bool decode_step_supported(int G) { return G == 1 || G == 2 || G == 4; }
+
+cudaError_t launch_decode_step(const DecodeArgs& a, const StepArgs& st, cudaStream_t s) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_g<1, true>(a, st, KVA_BF16, s);
+    case 2: return launch_g<2, true>(a, st, KVA_BF16, s);
+    case 4: return launch_g<4, true>(a, st, KVA_BF16, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -349,6 +349,73 @@ kva_status kv_attn_decode(
   return cuda_status(e, "decode launch");
 }
 
+kva_status kv_attn_decode_step(
+    const void* q, const void* k, const void* v, kva_dtype in_dtype,
+    const int32_t* pos, int64_t pos_inst_stride,
+    kva_qknorm norm, kva_rope rope, kva_cache cache,
+    const int32_t* lengths, const int32_t* lengths_host, int32_t B, int32_t n_q_heads,
+    float scale, void* q_out, kva_dtype q_out_dtype, float* out,
+    void* workspace, size_t workspace_bytes, kva_stream stream) {
+  if (B < 0) return fail(KVA_EINVAL, "B=%d must be >= 0", B);
+  if (B == 0) return KVA_OK;
+  if (!valid_dtype(in_dtype) || (q_out && !valid_dtype(q_out_dtype))) return fail(KVA_EINVAL, "unknown dtype");
+  kva_status st = check_cache(cache, B);
+  if (st != KVA_OK) return st;
+  const int D = cache.head_dim, Hkv = cache.n_kv_heads;
+  if (n_q_heads <= 0 || n_q_heads % Hkv != 0)
+    return fail(KVA_EINVAL, "n_q_heads %d must be a positive multiple of n_kv_heads %d", n_q_heads, Hkv);
+  if (!q || !k || !v || !out || !lengths || !lengths_host) return fail(KVA_EINVAL, "NULL q/k/v/out/lengths");
+  if (rope.kind != KVA_ROPE_NONE && !pos) return fail(KVA_EINVAL, "RoPE needs positions");
+  if (pos_inst_stride < 0) return fail(KVA_EINVAL, "negative position stride");
+  if ((norm.q_w == nullptr) != (norm.k_w == nullptr))
+    return fail(KVA_EINVAL, "q and k norm weights must both be given or both be NULL");
+  if (norm.q_w && (!(norm.eps >= 0.f) || norm.inst_stride < 0)) return fail(KVA_EINVAL, "bad QK-Norm eps/stride");
+  const int G = n_q_heads / Hkv;
+  if (cache.dtype != KVA_BF16 || D != DECODE_HEAD_DIM || !decode_step_supported(G))
+    return fail(KVA_EUNSUPPORTED, "fused step needs a bf16 cache, head_dim 128, Hq/Hkv in {1,2,4}");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (q_out && !aligned16(q_out)))
+    return fail(KVA_EALIGN, "q/k/v/out/q_out must be 16-byte aligned");
+  if (norm.q_w && (!aligned16(norm.q_w) || !aligned16(norm.k_w) || (norm.inst_stride * 4) % 16 != 0))
+    return fail(KVA_EALIGN, "norm weights must be 16-byte aligned with a 16-byte instance stride");
+  if (!workspace) return fail(KVA_EWORKSPACE, "decode step: workspace is NULL");
+  if (!aligned16(workspace)) return fail(KVA_EALIGN, "workspace must be 16-byte aligned");
+  if (B > 65535) return fail(KVA_EUNSUPPORTED, "decode step: B > 65535");
+  StepArgs sa{};
+  st = build_rope(rope, D, &sa.rope);
+  if (st != KVA_OK) return st;
+  int max_len = 0;
+  for (int b = 0; b < B; ++b) {
+    const int L = lengths_host[b];
+    if (L < 1 || L > cache.capacity)
+      return fail(KVA_ECAPACITY, "length %d of instance %d outside [1, %d]", L, b, cache.capacity);
+    max_len = std::max(max_len, L);
+  }
+  const int chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len);
+  const int max_chunks = (max_len + chunk - 1) / chunk;
+  const size_t need = decode_ws_bytes(B, Hkv, n_q_heads, max_chunks, D);
+  if (workspace_bytes < need)
+    return fail(KVA_EWORKSPACE, "decode step workspace %zu bytes < %zu needed", workspace_bytes, need);
+  DecodeArgs a{};
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.counters = reinterpret_cast<unsigned*>(ws);
+  a.part_ml = reinterpret_cast<float*>(ws + decode_zero_bytes(B, Hkv));
+  a.part_acc = reinterpret_cast<float*>(ws + decode_zero_bytes(B, Hkv) +
+                                        round_up(sizeof(float) * (size_t)B * n_q_heads * max_chunks * 2, 256));
+  a.q = nullptr; a.kc = cache.k; a.vc = cache.v; a.lengths = lengths; a.out = out;
+  a.B = B; a.Hq = n_q_heads; a.Hkv = Hkv; a.capacity = cache.capacity;
+  a.chunk = chunk; a.max_chunks = max_chunks; a.inst_stride = cache.inst_stride;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+  a.scale_log2 = sc * 1.4426950408889634f;
+  sa.q = q; sa.k = k; sa.v = v; sa.in_dtype = (int)in_dtype;
+  sa.pos = pos; sa.pos_stride = pos_inst_stride;
+  sa.q_w = norm.q_w; sa.k_w = norm.k_w; sa.w_stride = norm.inst_stride; sa.eps = norm.eps;
+  sa.after_rope = norm.after_rope ? 1 : 0;
+  sa.q_out = q_out; sa.q_out_dtype = (int)q_out_dtype;
+  cudaError_t e = launch_decode_step(a, sa, (cudaStream_t)stream);
+  if (e == cudaSuccess) count_launches(1);
+  return cuda_status(e, "decode step launch");
+}
+
 kva_status lmhead_argmax(
     const float* h, const void* W, kva_dtype w_dtype,
     int32_t B, int32_t H, int32_t V, int32_t V_rows,

@@ -59,6 +59,24 @@ struct DecodeArgs {
   float scale_log2;       // softmax scale * log2(e)
 };
 
+// Raw inputs of the new token for the fused append + decode step (kv_attn_decode_step).
+struct StepArgs {
+  const void* q;          // [B, Hq, D] projections of the new token
+  const void* k;          // [B, Hkv, D]
+  const void* v;          // [B, Hkv, D]
+  int in_dtype;           // kva_dtype of q, k, v
+  const int32_t* pos;     // instance b reads pos + b * pos_stride (n_axes ids)
+  int64_t pos_stride;
+  const float* q_w;       // QK-Norm weights or null
+  const float* k_w;
+  int64_t w_stride;
+  float eps;
+  int after_rope;
+  void* q_out;            // optional [B, Hq, D] transformed queries
+  int q_out_dtype;
+  RopeTable rope;
+};
+
 constexpr int DECODE_HEAD_DIM = 128;
 int decode_subtile(kva_dtype cache_dtype);   // keys per pipeline stage
 int decode_num_sms();
@@ -67,6 +85,9 @@ int decode_num_sms();
 int decode_plan_chunk(const int32_t* lengths_host, int B, int Hkv, int max_len);
 cudaError_t launch_decode(const DecodeArgs& a, kva_dtype q_dtype, kva_dtype cache_dtype,
                           cudaStream_t s);
+// Fused append + decode (bf16 cache, D = 128, G in {1, 2, 4}); false if this build cannot.
+bool decode_step_supported(int G);
+cudaError_t launch_decode_step(const DecodeArgs& a, const StepArgs& st, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------
 struct LmheadArgs {

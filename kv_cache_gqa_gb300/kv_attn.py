@@ -63,6 +63,9 @@ def lib() -> C.CDLL:
         L.kv_attn_prefill.argtypes = [vp, C.c_int, _Cache, i32, i32, i32, C.c_int, vp, vp, vp,
                                       C.c_float, vp, vp]
         L.kv_attn_decode.argtypes = [vp, C.c_int, _Cache, vp, vp, i32, i32, C.c_float, vp, vp, sz, vp]
+        L.kv_attn_decode_step.argtypes = [vp, vp, vp, C.c_int, vp, i64, _Norm, _Rope, _Cache, vp, vp, i32, i32,
+                                          C.c_float, vp, C.c_int, vp, vp, sz, vp]
+        L.kv_attn_decode_step.restype = C.c_int
         L.kv_attn_decode_static.argtypes = [vp, C.c_int, _Cache, vp, vp, i32, i32, C.c_float, vp, vp]
         L.kv_attn_decode_static.restype = C.c_int
         L.lmhead_argmax.argtypes = [vp, vp, C.c_int, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
@@ -217,6 +220,25 @@ def kv_attn_decode(q, cache: KVCache, lengths, lengths_host, out, workspace, sca
     _check(lib().kv_attn_decode(
         _ptr(q), _dtype_code(q), cache.struct, _ptr(lengths), lh.ctypes.data, B, Hq, float(scale),
         _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kv_attn_decode_step(q, k, v, pos, cache: KVCache, lengths, lengths_host, out, workspace, rope: Rope,
+                        q_norm_w=None, k_norm_w=None, eps: float = 1e-6, norm_after_rope: bool = False,
+                        norm_inst_stride: int = 0, pos_inst_stride: Optional[int] = None, q_out=None,
+                        scale: float = 0.0, stream=None):
+    """Fused append + decode of one new token per instance.  q [B,Hq,D], k/v [B,Hkv,D] raw
+    projections (CUDA f32|bf16); pos [B|1, n_axes] int32 CUDA; lengths [B] int32 CUDA (valid
+    slots incl. the new token, which is written to slot L-1) + host mirror; out [B,Hq,D] f32."""
+    B, Hq, _ = q.shape
+    if pos_inst_stride is None:
+        pos_inst_stride = 0 if (pos is None or pos.dim() < 2 or pos.shape[0] == 1) else pos.shape[-1]
+    lh = _host_i32(lengths_host)
+    norm = _Norm(_ptr(q_norm_w), _ptr(k_norm_w), norm_inst_stride, eps, 1 if norm_after_rope else 0)
+    _check(lib().kv_attn_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(pos), pos_inst_stride, norm, rope.struct, cache.struct,
+        _ptr(lengths), lh.ctypes.data, B, Hq, float(scale), _ptr(q_out),
+        _dtype_code(q_out) if q_out is not None else 0, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def lmhead_argmax(h, W, out_ids, workspace, V: Optional[int] = None, out_max=None, logits=None,

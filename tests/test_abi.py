@@ -113,6 +113,27 @@ def test_decode_validation(K):
     assert L.kva_decode_workspace_size(4, 8, 16, 1000, 128) > L.kva_decode_workspace_zero_bytes(4, 8) > 0
 
 
+def test_decode_step_validation(K):
+    L = K.lib()
+    def step(lens, ws=FAKE, ws_bytes=1 << 30, cache=None, Hq=16, k=FAKE, rope=None, pos=FAKE, norm=None):
+        lh = np.asarray(lens, np.int32)
+        return L.kv_attn_decode_step(FAKE, k, FAKE, 0, pos, 0, norm or _norm(), rope or _rope(),
+                                     cache or _cache(FAKE, cap=64), FAKE, lh.ctypes.data, len(lens), Hq, 0.0,
+                                     None, 0, FAKE, ws, ws_bytes, None)
+    assert step([]) == K.KVA_OK
+    assert step([0]) == K.KVA_ECAPACITY                                      # no slot for the new token
+    assert step([65]) == K.KVA_ECAPACITY
+    assert step([3], k=None) == K.KVA_EINVAL
+    assert step([3], pos=None) == K.KVA_EINVAL                               # RoPE without positions
+    assert step([3], norm=_norm(k=FAKE)) == K.KVA_EINVAL
+    assert step([3], ws=None) == K.KVA_EWORKSPACE
+    assert step([3], ws_bytes=16) == K.KVA_EWORKSPACE
+    assert step([3], cache=_cache(FAKE, dtype=0, cap=64)) == K.KVA_EUNSUPPORTED   # f32 cache: two calls
+    assert step([3], cache=_cache(FAKE, d=64, cap=64)) == K.KVA_EUNSUPPORTED
+    assert step([3], Hq=64) == K.KVA_EUNSUPPORTED                            # group size 8
+    assert step([3], rope=_rope(kind=2, secs=(16, 16, 16, 8), n_axes=4)) == K.KVA_EINVAL
+
+
 def test_lmhead_validation(K):
     L = K.lib()
     def lm(B=1, H=1024, V=100, Vr=100, ws=FAKE, wsb=1 << 20, h=FAKE):
