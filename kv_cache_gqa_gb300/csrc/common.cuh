@@ -88,6 +88,16 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization may
+// start while the grid before it on the stream is still running: it sets up shared memory,
+// then griddep_wait() blocks until that grid has completed and its writes are visible.  No
+// global memory may be read or written before the wait.  griddep_launch_dependents() lets the
+// grid after this one start its own set-up (it still waits for this grid to complete).
+// Without the launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -63,18 +63,18 @@ __device__ __forceinline__ void step_cos_sin(int32_t p, double inv, float* c, fl
 
 // One 128-wide row of the new token (lane owns dims 4*lane .. 4*lane+3): QK-Norm and RoPE in
 // the configured order for q/k rows (w != null or rope), untouched for v rows.
-__device__ __forceinline__ void step_row(float (&x)[4], const float* w, bool rotate, const StepArgs& st,
-                                         const float* s_cos, const float* s_sin, int lane) {
+__device__ __forceinline__ void step_row(float (&x)[4], const float (&w)[4], bool has_w, bool rotate,
+                                         const StepArgs& st, const float* s_cos, const float* s_sin, int lane) {
   auto rms = [&](void) {
     float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
     return 1.0f / sqrtf(ss / (float)D + st.eps);
   };
-  if (w && !st.after_rope) {
+  if (has_w && !st.after_rope) {
     const float r = rms();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = x[i] * r * w[4 * lane + i];
+    for (int i = 0; i < 4; ++i) x[i] = x[i] * r * w[i];
   }
   if (rotate) {
     // partner of dim d: d +- 64 (lane ^ 16) for 1D / sections, d +- 32 inside a half (lane ^ 8) for 2D
@@ -92,10 +92,10 @@ __device__ __forceinline__ void step_row(float (&x)[4], const float* w, bool rot
 #pragma unroll
     for (int i = 0; i < 4; ++i) x[i] = y[i];
   }
-  if (w && st.after_rope) {
+  if (has_w && st.after_rope) {
     const float r = rms();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = x[i] * r * w[4 * lane + i];
+    for (int i = 0; i < 4; ++i) x[i] = x[i] * r * w[i];
   }
 }
 
@@ -119,15 +119,42 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char* ring = smem + warp * RING;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + WARPS * RING) + warp * NS;
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+    if (warp == 0) { tc::tma_prefetch_desc(&tmK); tc::tma_prefetch_desc(&tmV); }
+  }
+  griddep_wait();                               // inputs of this launch are complete from here on
+  griddep_launch_dependents();
   const int L = a.lengths[b];
+  // fused step: the new token's rows (G queries, then k, then v; warp w takes rows w and w + 4)
+  // and position are loaded here, so their latency overlaps that of the lengths load
+  constexpr int ROWS = FUSED ? (G + 2 + WARPS - 1) / WARPS : 1;
+  float xr[ROWS][4], wr[ROWS][4];
+  int32_t pj = 0;
+  if constexpr (FUSED) {
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      const int rr = warp + i * WARPS;
+      wr[i][0] = wr[i][1] = wr[i][2] = wr[i][3] = 1.f;
+      if (rr < G) {
+        load4(st.q, st.in_dtype, ((int64_t)b * a.Hq + g * G + rr) * D + 4 * lane, xr[i]);
+        if (st.q_w) load4(st.q_w + (int64_t)b * st.w_stride, KVA_F32, 4 * lane, wr[i]);
+      } else if (rr < G + 2) {
+        load4(rr == G ? st.k : st.v, st.in_dtype, ((int64_t)b * a.Hkv + g) * D + 4 * lane, xr[i]);
+        if (rr == G && st.k_w) load4(st.k_w + (int64_t)b * st.w_stride, KVA_F32, 4 * lane, wr[i]);
+      }
+    }
+    if (st.rope.kind != KVA_ROPE_NONE && tid < D / 2) pj = st.pos[(int64_t)b * st.pos_stride + st.rope.axis[tid]];
+  }
   const int n_chunks = min(a.max_chunks, (L + a.chunk - 1) / a.chunk);
   if (c >= n_chunks) return;
   const int k0 = (int)(((int64_t)L * c) / n_chunks);
   const int k1 = (int)(((int64_t)L * (c + 1)) / n_chunks);
   const int n_tiles = (k1 - k0 + KT - 1) / KT;
 
-  unsigned char* ring = smem + warp * RING;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + WARPS * RING) + warp * NS;
   const int n_mine = n_tiles > warp ? (n_tiles - 1 - warp) / WARPS + 1 : 0;
   auto issue = [&](int u) {                    // lane 0: tile t = warp + u*WARPS
     const int ks = k0 + (warp + u * WARPS) * KT;
@@ -138,11 +165,8 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
     tc::tma_load_4d(dst + 2 * BOX, &tmV, 0, ks, g, b, &bar[u % NS]);
     tc::tma_load_4d(dst + 3 * BOX, &tmV, 64, ks, g, b, &bar[u % NS]);
   };
-  if (lane == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
-    fence_mbar_init();
+  if (lane == 0)
     for (int u = 0; u < NS && u < n_mine; ++u) issue(u);
-  }
   __syncwarp();
 
   // ---- fused step: transform the new token's rows (q of the G heads; k, v in the last chunk) ----
@@ -151,21 +175,15 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   const bool last_chunk = (c == n_chunks - 1);
   if constexpr (FUSED) {
     const bool rotate = st.rope.kind != KVA_ROPE_NONE;
-    if (rotate && tid < D / 2)
-      step_cos_sin(st.pos[(int64_t)b * st.pos_stride + st.rope.axis[tid]], st.rope.inv[tid], &s_cos[tid], &s_sin[tid]);
+    if (rotate && tid < D / 2) step_cos_sin(pj, st.rope.inv[tid], &s_cos[tid], &s_sin[tid]);
     __syncthreads();
-    for (int rr = warp; rr < G + 2; rr += WARPS) {          // rows: G queries, then k, then v
-      if (rr >= G && !last_chunk) continue;                 // only the last chunk owns the new key
-      float x[4];
-      const float* w = nullptr;
-      if (rr < G) {
-        load4(st.q, st.in_dtype, ((int64_t)b * a.Hq + g * G + rr) * D + 4 * lane, x);
-        w = st.q_w ? st.q_w + (int64_t)b * st.w_stride : nullptr;
-      } else {
-        load4(rr == G ? st.k : st.v, st.in_dtype, ((int64_t)b * a.Hkv + g) * D + 4 * lane, x);
-        w = (rr == G && st.k_w) ? st.k_w + (int64_t)b * st.w_stride : nullptr;
-      }
-      step_row(x, w, rotate && rr <= G, st, s_cos, s_sin, lane);
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      const int rr = warp + i * WARPS;
+      if (rr >= G + 2 || (rr >= G && !last_chunk)) continue;   // only the last chunk owns the new key
+      float (&x)[4] = xr[i];
+      const bool has_w = rr < G ? st.q_w != nullptr : (rr == G && st.k_w != nullptr);
+      step_row(x, wr[i], has_w, rotate && rr <= G, st, s_cos, s_sin, lane);
       const uint32_t p01 = pack_bf16x2(x[0], x[1]), p23 = pack_bf16x2(x[2], x[3]);
       if (rr < G) {
         *reinterpret_cast<uint2*>(&s_q[rr][4 * lane]) = make_uint2(p01, p23);
@@ -425,8 +443,7 @@ cudaError_t launch_g(const DecodeArgs& a, const StepArgs& st, kva_dtype q_dtype,
   if (e != cudaSuccess) return e;
   if ((e = make_map(&mv, a.vc, a)) != cudaSuccess) return e;
   dim3 grid(a.max_chunks, a.Hkv, a.B);
-  decode_mma_kernel<G, FUSED><<<grid, THREADS, smem, s>>>(a, mk, mv, q_dtype, st);
-  return cudaGetLastError();
+  return launch_pdl(decode_mma_kernel<G, FUSED>, grid, dim3(THREADS), smem, s, a, mk, mv, q_dtype, st);
 }
 
 }  // namespace

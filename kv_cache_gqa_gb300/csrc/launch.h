@@ -121,6 +121,25 @@ struct PrefillArgs {
 int lmhead_max_hidden();
 cudaError_t launch_prefill(const PrefillArgs& a, kva_dtype dtype, cudaStream_t s);
 
+// Launch `kern` with programmatic stream serialization: its set-up overlaps the tail of the
+// kernel before it on the stream.  The kernel must call griddep_wait() before its first global
+// memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Launch bookkeeping (kernel launches issued by this library).
 void count_launches(unsigned n);
 // Record the message kva_last_error() returns on this host thread.

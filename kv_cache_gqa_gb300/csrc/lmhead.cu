@@ -244,8 +244,11 @@ lmhead_b1_pipe_kernel(const __grid_constant__ LmheadArgs a, int rows_per_cta) {
   if (tid == 0) {
     for (int st = 0; st < PIPE_STAGES; ++st) { mbar_init(&full[st], 1); mbar_init(&empty[st], PIPE_WARPS); }
     fence_mbar_init();
-    for (int it = 0; it < PIPE_STAGES && it < n_st; ++it) issue(it);
   }
+  griddep_wait();                               // h (and the table) are complete from here on
+  griddep_launch_dependents();
+  if (tid == 0)
+    for (int it = 0; it < PIPE_STAGES && it < n_st; ++it) issue(it);
   float hv[NCH][8];
 #pragma unroll
   for (int c = 0; c < NCH; ++c) {
@@ -381,8 +384,8 @@ cudaError_t launch_b1_pipe(const LmheadArgs& a, cudaStream_t s) {
   }
   const int grid = num_sms_lm();
   const int rows_per_cta = (a.V + grid - 1) / grid;
-  lmhead_b1_pipe_kernel<H><<<grid, PIPE_THREADS, PIPE_STAGES * PIPE_STAGE_BYTES, s>>>(a, rows_per_cta);
-  return cudaGetLastError();
+  return launch_pdl(lmhead_b1_pipe_kernel<H>, dim3(grid), dim3(PIPE_THREADS), (size_t)(PIPE_STAGES * PIPE_STAGE_BYTES), s,
+                    a, rows_per_cta);
 }
 
 cudaError_t launch_lmhead(const LmheadArgs& a, kva_dtype w_dtype, void* hb_scratch, cudaStream_t s,
