@@ -88,6 +88,28 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// cos and sin of the rotary angle a = p * inv, with inv = ih + il split into a float pair on
+// the host.  For |p| < 2^24 the position is exact in float and the product is carried as
+// hi + lo (the rounding error of p * ih recovered with an fma), then reduced by 2 pi in the
+// Cody-Waite way with a two-part constant (the first product k * C1 cancels exactly), so
+// the float sin/cos see an argument in [-pi, pi] that is accurate to a few float ulps of
+// pi.  Larger positions take the same steps in float64.
+__device__ __forceinline__ void rope_cos_sin(int32_t p, float ih, float il, double inv, float* c, float* s) {
+  if (p > -(1 << 24) && p < (1 << 24)) {
+    const float pf = (float)p;
+    const float hi = pf * ih;
+    const float lo = fmaf(pf, ih, -hi) + pf * il;
+    const float k = rintf(hi * 0.159154943f);
+    float r = fmaf(-k, 6.28318548f, hi);                  // C1 = float(2 pi): exact
+    r = fmaf(-k, -1.74845553e-7f, r) + lo;                // C2 = 2 pi - C1
+    sincosf(r, s, c);
+  } else {
+    const double a = (double)p * inv;
+    const double k = rint(a * 0.15915494309189535);
+    sincosf((float)fma(-k, 6.283185307179586, a), s, c);
+  }
+}
+
 // Programmatic dependent launch.  A kernel launched with programmatic stream serialization may
 // start while the grid before it on the stream is still running: it sets up shared memory,
 // then griddep_wait() blocks until that grid has completed and its writes are visible.  No

@@ -54,13 +54,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2
 // byte offset of 16-byte chunk `ch` of key row `key` inside a 128-byte-swizzled box
 __device__ __forceinline__ uint32_t swz(int key, int ch) { return key * 128 + ((ch ^ (key & 7)) << 4); }
 
-// Reduce the angle a = pos * inv_freq (float64) into [-pi, pi] before the float32 sin/cos.
-__device__ __forceinline__ void step_cos_sin(int32_t p, double inv, float* c, float* s) {
-  const double x = (double)p * inv;
-  const double k = rint(x * 0.15915494309189535);
-  sincosf((float)fma(-k, 6.283185307179586, x), s, c);
-}
-
 // One 128-wide row of the new token (lane owns dims 4*lane .. 4*lane+3): QK-Norm and RoPE in
 // the configured order for q/k rows (w != null or rope), untouched for v rows.
 __device__ __forceinline__ void step_row(float (&x)[4], const float (&w)[4], bool has_w, bool rotate,
@@ -126,6 +119,14 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
     fence_mbar_init();
     if (warp == 0) { tc::tma_prefetch_desc(&tmK); tc::tma_prefetch_desc(&tmV); }
   }
+  // rotary table entry of angle slot tid (fused step): parameter reads with per-thread indices
+  // serialise, so they are issued before the wait, overlapping the previous kernel
+  float r_ih = 0.f, r_il = 0.f;
+  double r_inv = 0.0;
+  int r_axis = 0;
+  if (FUSED && tid < D / 2) {
+    r_ih = st.rope.inv_hi[tid]; r_il = st.rope.inv_lo[tid]; r_inv = st.rope.inv[tid]; r_axis = st.rope.axis[tid];
+  }
   griddep_wait();                               // inputs of this launch are complete from here on
   griddep_launch_dependents();
   const int L = a.lengths[b];
@@ -147,7 +148,7 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
         if (rr == G && st.k_w) load4(st.k_w + (int64_t)b * st.w_stride, KVA_F32, 4 * lane, wr[i]);
       }
     }
-    if (st.rope.kind != KVA_ROPE_NONE && tid < D / 2) pj = st.pos[(int64_t)b * st.pos_stride + st.rope.axis[tid]];
+    if (st.rope.kind != KVA_ROPE_NONE && tid < D / 2) pj = st.pos[(int64_t)b * st.pos_stride + r_axis];
   }
   const int n_chunks = min(a.max_chunks, (L + a.chunk - 1) / a.chunk);
   if (c >= n_chunks) return;
@@ -175,7 +176,7 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   const bool last_chunk = (c == n_chunks - 1);
   if constexpr (FUSED) {
     const bool rotate = st.rope.kind != KVA_ROPE_NONE;
-    if (rotate && tid < D / 2) step_cos_sin(pj, st.rope.inv[tid], &s_cos[tid], &s_sin[tid]);
+    if (rotate && tid < D / 2) rope_cos_sin(pj, r_ih, r_il, r_inv, &s_cos[tid], &s_sin[tid]);
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < ROWS; ++i) {

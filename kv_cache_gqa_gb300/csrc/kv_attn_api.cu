@@ -101,6 +101,16 @@ kva_status build_rope(const kva_rope& r, int D, RopeTable* t) {
   }
 }
 
+kva_status build_rope_table(const kva_rope& r, int D, RopeTable* t) {
+  const kva_status st = build_rope(r, D, t);
+  if (st != KVA_OK) return st;
+  for (int j = 0; j < MAX_ROPE_FREQ; ++j) {
+    t->inv_hi[j] = (float)t->inv[j];
+    t->inv_lo[j] = (float)(t->inv[j] - (double)t->inv_hi[j]);
+  }
+  return KVA_OK;
+}
+
 constexpr int DECODE_MAX_CHUNKS = 64;
 constexpr int DECODE_CHUNK_ALIGN = 64;
 
@@ -235,7 +245,7 @@ kva_status kv_cache_append_rope_qknorm(
     return fail(KVA_EALIGN, "norm weights must be 16-byte aligned with a 16-byte instance stride");
 
   AppendArgs a{};
-  st = build_rope(rope, D, &a.rope);
+  st = build_rope_table(rope, D, &a.rope);
   if (st != KVA_OK) return st;
   for (int n = 0; n < N; ++n)
     for (int t = 0; t < T; ++t) {
@@ -381,7 +391,7 @@ kva_status kv_attn_decode_step(
   if (!aligned16(workspace)) return fail(KVA_EALIGN, "workspace must be 16-byte aligned");
   if (B > 65535) return fail(KVA_EUNSUPPORTED, "decode step: B > 65535");
   StepArgs sa{};
-  st = build_rope(rope, D, &sa.rope);
+  st = build_rope_table(rope, D, &sa.rope);
   if (st != KVA_OK) return st;
   int max_len = 0;
   for (int b = 0; b < B; ++b) {

@@ -16,6 +16,8 @@ struct RopeTable {
   int kind;
   int n_axes;
   double inv[MAX_ROPE_FREQ];
+  float inv_hi[MAX_ROPE_FREQ];   // float(inv[j]) and float(inv[j] - inv_hi[j]): inv as a float pair
+  float inv_lo[MAX_ROPE_FREQ];
   unsigned char axis[MAX_ROPE_FREQ];
 };
 

@@ -102,6 +102,62 @@ def test_append_parity(K, D, kind, secs, norm, in_dt, qo_dt, c_dt):
         assert np.all(kc_h[n][:, ~written] == 7.0) and np.all(vc_h[n][:, ~written] == 7.0)
 
 
+STREAM_CASES = [
+    # D, rope kind, sections, norm, in, q_out, cache: long appends (>= 2 work items per SM) with a
+    # ragged last token block take the streaming (bulk-copy ring) form of the append kernel
+    (128, "1d", (), "before", "f32", "bf16", "bf16"),
+    (128, "sections", (16, 16, 16, 16), "after", "f32", "f32", "f32"),
+    (128, "2d", (), None, "bf16", "bf16", "bf16"),
+    (64, "1d", (), "before", "f32", "bf16", "f32"),
+    (256, "1d", (), "after", "f32", "bf16", "bf16"),
+]
+
+
+@pytest.mark.parametrize("D,kind,secs,norm,in_dt,qo_dt,c_dt", STREAM_CASES)
+def test_append_stream_parity(K, D, kind, secs, norm, in_dt, qo_dt, c_dt):
+    torch = T()
+    rng = np.random.default_rng(zlib.crc32(repr(("stream", D, kind, norm, in_dt)).encode()))
+    N, Tt, Hkv, G = 40, 77, 4, 2
+    Hq, W = Hkv * G, 96
+    q = rng.standard_normal((N, Tt, Hq, D)).astype(np.float32) * 3
+    k = rng.standard_normal((N, Tt, Hkv, D)).astype(np.float32) * 3
+    v = rng.standard_normal((N, Tt, Hkv, D)).astype(np.float32)
+    n_axes = {"none": 1, "1d": 1, "sections": 4, "2d": 2}[kind]
+    pos = rng.integers(0, 40000, size=(N, Tt, n_axes)).astype(np.int32)
+    slot = np.stack([rng.permutation(W)[:Tt] for _ in range(N)]).astype(np.int32)
+    qw = (1 + 0.1 * rng.standard_normal((N, D))).astype(np.float32)
+    kw = (1 + 0.1 * rng.standard_normal((N, D))).astype(np.float32)
+    base = 1.11588e7 if kind == "sections" else 1e6
+    kc = torch.full((N, Hkv, W, D), 7.0, device="cuda", dtype=_tdt(c_dt))
+    vc = torch.full_like(kc, 7.0)
+    q_out = torch.empty((N, Tt, Hq, D), device="cuda", dtype=_tdt(qo_dt))
+    K.kv_cache_append_rope_qknorm(
+        dev(q, _tdt(in_dt)), dev(k, _tdt(in_dt)), dev(v, _tdt(in_dt)), dev(pos), dev(slot), slot, K.KVCache(kc, vc),
+        q_out, K.Rope(kind, base, secs), q_norm_w=dev(qw) if norm else None, k_norm_w=dev(kw) if norm else None,
+        eps=1e-6, norm_after_rope=(norm == "after"), norm_inst_stride=D)
+    torch.cuda.synchronize()
+    rope = O.Rope(kind, base, secs if secs else None)
+    kc_h, vc_h = host(kc), host(vc)
+    kb = bf16_bits(kc) if c_dt == "bf16" else None
+    for n in range(0, N, 3):
+        qx, kx, vx = (_widen(a[n], in_dt) for a in (q, k, v))
+        ck = np.full((Hkv, W, D), 7.0); cv = np.full((Hkv, W, D), 7.0)
+        qr = O.cache_append(qx, kx, vx, pos[n], slot[n], qw[n] if norm else None, kw[n] if norm else None, 1e-6,
+                            rope, norm == "after", ck, cv, c_dt)
+        kr = O.qk_transform(kx, pos[n], kw[n] if norm else None, 1e-6, rope, norm == "after")
+        if qo_dt == "f32":
+            assert_fp32_close(host(q_out[n]), qr, f"q_out n={n}")
+        else:
+            assert_bf16_store(bf16_bits(q_out[n]), qr, f"q_out n={n}")
+        written = np.zeros(W, bool); written[slot[n]] = True
+        if c_dt == "f32":
+            assert_fp32_close(kc_h[n][:, written], ck[:, written], f"k cache n={n}")
+        else:
+            assert_bf16_store(kb[n][:, slot[n]], kr.transpose(1, 0, 2), f"k cache n={n}")
+        np.testing.assert_array_equal(vc_h[n][:, written], cv[:, written])
+        assert np.all(kc_h[n][:, ~written] == 7.0) and np.all(vc_h[n][:, ~written] == 7.0)
+
+
 def test_append_shared_positions_and_weights(K):
     """Instance strides of 0 share positions/slots/weights across instances (layers)."""
     torch = T()
