@@ -92,8 +92,9 @@ __device__ __forceinline__ void fence_mbar_init() {
 // the host.  For |p| < 2^24 the position is exact in float and the product is carried as
 // hi + lo (the rounding error of p * ih recovered with an fma), then reduced by 2 pi in the
 // Cody-Waite way with a two-part constant (the first product k * C1 cancels exactly), so
-// the float sin/cos see an argument in [-pi, pi] that is accurate to a few float ulps of
-// pi.  Larger positions take the same steps in float64.
+// the float sin/cos see a short argument (within pi, or 2 pi when the float estimate of k
+// is off by one for very large angles) accurate to a few float ulps of pi.  Larger
+// positions take the same steps in float64.
 __device__ __forceinline__ void rope_cos_sin(int32_t p, float ih, float il, double inv, float* c, float* s) {
   if (p > -(1 << 24) && p < (1 << 24)) {
     const float pf = (float)p;
