@@ -125,7 +125,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, kva_dtype dtype, cudaStream_t s
 
 // Launch `kern` with programmatic stream serialization: its set-up overlaps the tail of the
 // kernel before it on the stream.  The kernel must call griddep_wait() before its first global
-// memory access.
+// memory access.  A kernel that allocates tensor memory must do so before it calls
+// griddep_launch_dependents(): a dependent CTA may allocate during its own set-up, so every CTA
+// of the earlier grid must already hold its columns by then.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args&&... args) {
