@@ -253,6 +253,41 @@ def decode(q, cache_k, cache_v, length: int, scale=None):
 
 
 # ----------------------------------------------------------------------------
+# Speculative-decoding verify block (DFlash)
+# ----------------------------------------------------------------------------
+def verify_block(q_rows, cache_k, cache_v, length: int, scale=None):
+    """One verify forward of a k-token block: q_rows [k, Hq, D] are the queries of the tokens
+    stored in the last k valid slots (length - k .. length - 1), and row i attends to the keys
+    of slots 0 .. length - k + i (a multi-token causal mask over the existing cache: HunyuanOCR
+    v1.5 port, section 3.8, target verification)."""
+    q_rows = np.asarray(q_rows, dtype=F64)
+    k = q_rows.shape[0]
+    if not 1 <= k <= length:
+        raise ValueError("block of k tokens needs 1 <= k <= length")
+    allowed = np.zeros((k, cache_k.shape[1]), dtype=bool)
+    for i in range(k):
+        allowed[i, :length - k + i + 1] = True
+    return attend(q_rows, cache_k, cache_v, allowed, scale)
+
+
+def verify_accept(posterior, block_tokens, length: int):
+    """Acceptance and commit of a verify block (HunyuanOCR v1.5 port, section 3.8): the block
+    holds the current token and k - 1 draft candidates (block_tokens [k], in slots
+    length - k .. length - 1); posterior [k] is the target's greedy id after each of them.
+    Candidate i + 1 is accepted while posterior[i] equals it, stopping at the first mismatch;
+    the target's id after the accepted prefix is kept (the correction, or the next token when
+    every candidate matched).  The cache is cut back to the current token plus the accepted
+    candidates.  Returns (accepted a, next token, committed length)."""
+    posterior = np.asarray(posterior)
+    block_tokens = np.asarray(block_tokens)
+    k = block_tokens.shape[0]
+    a = 0
+    while a < k - 1 and posterior[a] == block_tokens[a + 1]:
+        a += 1
+    return a, int(posterior[a]), length - k + a + 1
+
+
+# ----------------------------------------------------------------------------
 # Greedy lm_head
 # ----------------------------------------------------------------------------
 def lm_logits(h, W, V: int) -> np.ndarray:

@@ -399,3 +399,68 @@ def test_qwen3_constants_match_pages():
     assert WL.QWEN3_ROPE_THETA == g["rope_theta"] and WL.QWEN3_RMS_EPS == g["rms_eps"]
     assert GOLDEN["xdrope"]["value"]["effective_base"] == WL.XDROPE_BASE
     assert tuple(GOLDEN["xdrope"]["value"]["sections"]) == WL.XDROPE_SECTIONS
+
+
+# ----------------------------------------------------------------------------
+# speculative-decoding verify block (HunyuanOCR v1.5 port, section 3.8)
+# ----------------------------------------------------------------------------
+def test_verify_block_equals_prefill_rows_and_decode():
+    """Row i of a k-token verify block is row L-k+i of a causal prefill over the same L slots;
+    a 1-token block is a decode step."""
+    rng = np.random.default_rng(11)
+    L, k, Hq, Hkv, D = 23, 5, 4, 2, 8
+    q_all = rng.standard_normal((L, Hq, D))
+    ck = rng.standard_normal((Hkv, L + 3, D))
+    cv = rng.standard_normal((Hkv, L + 3, D))
+    pre = O.prefill(q_all, ck, cv, L, "causal")
+    ver = O.verify_block(q_all[L - k:], ck, cv, L)
+    np.testing.assert_allclose(ver, pre[L - k:], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(O.verify_block(q_all[L - 1:], ck, cv, L)[0], O.decode(q_all[L - 1], ck, cv, L),
+                               rtol=1e-13, atol=1e-15)
+
+
+def test_verify_block_brute_force_tiny():
+    """L = 3, k = 2, one head, D = 2: row 0 sees keys 0..1, row 1 sees keys 0..2 (scalar sums)."""
+    q = np.array([[[0.3, -1.2]], [[0.7, 0.4]]])
+    K = np.array([[[1.0, 0.0], [0.5, -0.5], [-1.0, 2.0]]])
+    V = np.array([[[1.0, 2.0], [3.0, -1.0], [0.0, 4.0]]])
+    got = O.verify_block(q, K, V, 3)
+    for i, n_keys in ((0, 2), (1, 3)):
+        logits = [(q[i, 0, 0] * K[0, j, 0] + q[i, 0, 1] * K[0, j, 1]) / math.sqrt(2) for j in range(n_keys)]
+        w = [math.exp(x) for x in logits]
+        tot = math.fsum(w)
+        for d in range(2):
+            assert abs(got[i, 0, d] - math.fsum(w[j] * V[0, j, d] for j in range(n_keys)) / tot) < 1e-14
+
+
+def test_verify_accept_hand_cases():
+    # block = [current, c1, c2, c3]; posterior[i] is the target's id after block[i]
+    assert O.verify_accept([5, 7, 9, 2], [1, 5, 7, 3], 40) == (2, 9, 39)      # c1, c2 accepted, c3 corrected
+    assert O.verify_accept([5, 7, 3, 8], [1, 5, 7, 3], 40) == (3, 8, 40)      # all accepted, next token 8
+    assert O.verify_accept([6, 7, 3, 8], [1, 5, 7, 3], 40) == (0, 6, 37)      # first candidate rejected
+    assert O.verify_accept([4], [1], 17) == (0, 4, 17)                        # k = 1: a greedy decode step
+
+
+def test_verify_accept_is_lossless_for_greedy():
+    """Over many blocks with random drafts, the emitted tokens equal the target's own greedy
+    sequence and the committed length counts exactly the tokens whose K/V stay cached."""
+    rng = np.random.default_rng(3)
+    vocab = 13
+    nxt = rng.integers(0, vocab, size=vocab)          # a deterministic toy target: greedy id after t
+    for _ in range(200):
+        t0 = int(rng.integers(vocab))
+        t, length, emitted = t0, 10, []
+        for _ in range(6):
+            k = int(rng.integers(1, 7))
+            draft = [t]
+            for _ in range(k - 1):                     # drafts: the true continuation, sometimes wrong
+                draft.append(int(nxt[draft[-1]]) if rng.random() < 0.7 else int(rng.integers(vocab)))
+            posterior = [int(nxt[x]) for x in draft]
+            a, new_t, committed = O.verify_accept(posterior, draft, length + k)   # block appended
+            emitted += draft[1:a + 1] + [new_t]
+            assert committed == length + 1 + a         # current token + accepted candidates
+            t, length = new_t, committed
+        chain = [int(nxt[t0])]
+        while len(chain) < len(emitted):
+            chain.append(int(nxt[chain[-1]]))
+        assert emitted == chain
