@@ -267,6 +267,35 @@ def graph_avg_ms(torch, stream, launch, n, reps=4):
     return e0.elapsed_time(e1) / (n * reps)
 
 
+VERIFY_B, VERIFY_L, VERIFY_K = 64, 2048, 16
+
+
+def verify_bench(torch, K, stream):
+    """Average duration of kv_attn_verify on VERIFY_B sequences of VERIFY_L valid slots with
+    VERIFY_K-token blocks (Qwen3 heads), as a graph of 8 back-to-back launches."""
+    B, L, k = VERIFY_B, VERIFY_L, VERIFY_K
+    g = torch.Generator(device="cuda"); g.manual_seed(7)
+    kc = torch.randn((B, HKV, L, D), device="cuda", generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, HKV, L, D), device="cuda", generator=g).to(torch.bfloat16)
+    q = torch.randn((B, k, HQ, D), device="cuda", generator=g).to(torch.bfloat16)
+    out = torch.empty((B, k, HQ, D), device="cuda")
+    lengths = np.full(B, L, np.int32)
+    ld = torch.from_numpy(lengths).cuda()
+    ws = torch.zeros(K.verify_workspace_bytes(B, HKV, HQ, k, L, D), dtype=torch.uint8, device="cuda")
+    cache = K.KVCache(kc, vc)
+    with torch.cuda.stream(stream):
+        K.kv_attn_verify(q, cache, ld, lengths, out, ws)          # configures the kernel before capture
+    torch.cuda.synchronize()
+    ms = graph_avg_ms(torch, stream, lambda: K.kv_attn_verify(q, cache, ld, lengths, out, ws), 8, reps=2)
+    kv_bytes = B * HKV * L * D * 2 * 2
+    io_bytes = B * k * HQ * D * (2 + 4)
+    del kc, vc
+    return {"config": f"{B} sequences x {L} slots, {k}-token blocks, {HQ}/{HKV} heads, D={D}, bf16 cache",
+            "avg_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": kv_bytes + io_bytes,
+            "GB/s": round((kv_bytes + io_bytes) / (ms / 1e3) / 1e9, 1),
+            "block_tokens_per_s": round(B * k / (ms / 1e3), 1)}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import kv_cache_gqa_gb300 as K
@@ -335,6 +364,10 @@ def run_gpu(args, rank, world, local_rank):
     # the dominant kernel alone: 32 back-to-back launches in one graph (its 311 MB table is larger
     # than L2, so every launch streams it from HBM as inside the job)
     lm_iso_ms = graph_avg_ms(torch, stream, lambda: K.lmhead_argmax(job.h[1], job.W, job.ids[1:2], job.lm_ws), 32)
+
+    # speculative-decoding verify block on a cache larger than L2: 64 sequences x 2048 slots,
+    # 16-token blocks (each launch streams 537 MB of K/V once for all 16 block rows)
+    vb = verify_bench(torch, K, stream)
 
     # ---- end to end: inputs from pinned host memory, ids back to the host, every step ----
     host_in = {n: getattr(job, n).cpu().pin_memory() for n in ("q", "k", "v", "dq", "dk", "dv", "h")}
@@ -415,10 +448,12 @@ def run_gpu(args, rank, world, local_rank):
                                    "launch_us": round(in_job["append_pre"] * 1e3, 1)},
                 "lm_head": {"GB/s": round(lm_gbs, 1), "frac_hbm": round(lm_gbs / hbm, 4),
                             "avg_launch_us": round(lm_iso_ms * 1e3, 2)},
+                "verify_block": dict(vb, frac_hbm=round(vb["GB/s"] / hbm, 4)),
                 "time_share": {k: round(v / sum(totals.values()), 4) for k, v in totals.items()},
                 "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": peak_src},
                 "timing": ("lm_head: graph of 32 back-to-back launches; prefill, append: " + kt_source +
-                           "; decode step: (timed job - prefill - append - 257 lm_head) / 256"),
+                           "; decode step: (timed job - prefill - append - 257 lm_head) / 256; verify block: "
+                           "graph of 8 back-to-back launches (outside the job)"),
                 "event_node_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in kt.items()},
             },
             "clocks": clk,

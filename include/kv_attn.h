@@ -205,6 +205,40 @@ kva_status kv_attn_decode_step(
     float scale, void* q_out, kva_dtype q_out_dtype, float* out,
     void* workspace, size_t workspace_bytes, kva_stream stream);
 
+/* ---------------------------------------------------------------------------------
+ * kv_attn_verify  (speculative-decoding verify block)
+ *   The target-verification forward of a draft block (HunyuanOCR v1.5 ncnn port, section 3.8):
+ *   the block's k tokens (the current token and k-1 draft candidates) already sit in the last
+ *   k valid slots, L-k .. L-1, of each instance (appended like any tokens), and block row i
+ *   attends to slots 0 .. L-k+i with the same GQA grouping and softmax as kv_attn_decode.
+ *  q        [B,k,Hq,D] of q_dtype: the block's transformed queries (device)
+ *  lengths  [B] valid slots L including the block (device); lengths_host: host copy or an
+ *           upper bound of it (used for validation and work planning; L >= k required)
+ *  out      [B,k,Hq,D] float32
+ *  workspace as for kv_attn_decode, sized by kva_verify_workspace_size; merge counters are
+ *  left at zero.  Requires a bf16 cache with head_dim 128 (else KVA_EUNSUPPORTED) and
+ *  1 <= k <= KVA_VERIFY_MAX_BLOCK. */
+#define KVA_VERIFY_MAX_BLOCK 64
+kva_status kv_attn_verify(
+    const void* q, kva_dtype q_dtype, kva_cache cache,
+    const int32_t* lengths, const int32_t* lengths_host, int32_t B, int32_t k, int32_t n_q_heads,
+    float scale, float* out, void* workspace, size_t workspace_bytes, kva_stream stream);
+size_t kva_verify_workspace_size(int32_t B, int32_t n_kv_heads, int32_t n_q_heads, int32_t k,
+                                 int32_t max_len, int32_t head_dim);
+
+/* ---------------------------------------------------------------------------------
+ * kv_verify_commit
+ *   Acceptance and commit of a verify block (HunyuanOCR v1.5 ncnn port, section 3.8), on the
+ *   device so no host round trip is needed: for instance b, block_tokens[b,0..k) are the block's
+ *   tokens and posterior[b,0..k) the target's greedy id after each of them (lmhead_argmax over
+ *   the block's rows).  Candidate i+1 is accepted while posterior[b,i] == block_tokens[b,i+1];
+ *   accepted[b] = the accepted count a, next_token[b] = posterior[b,a] (the target's correction,
+ *   or its next token when every candidate matched), and lengths[b] is cut from L to
+ *   L - k + a + 1 (the current token and the accepted candidates keep their K/V; the slots
+ *   after them are free for the next block).  All pointers are device int32 arrays. */
+kva_status kv_verify_commit(const int32_t* posterior, const int32_t* block_tokens, int32_t B, int32_t k,
+                            int32_t* lengths, int32_t* accepted, int32_t* next_token, kva_stream stream);
+
 size_t kva_decode_workspace_size(int32_t B, int32_t n_kv_heads, int32_t n_q_heads,
                                  int32_t max_len, int32_t head_dim);
 size_t kva_decode_workspace_zero_bytes(int32_t B, int32_t n_kv_heads);

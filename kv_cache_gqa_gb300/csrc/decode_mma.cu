@@ -451,6 +451,12 @@ cudaError_t launch_g(const DecodeArgs& a, const StepArgs& st, kva_dtype q_dtype,
 
 bool decode_mma_supported() { return encode_fn_dec() != nullptr; }
 
+cudaError_t decode_cache_map(CUtensorMap* map, const void* base, int capacity, int Hkv, int B, int64_t inst_stride) {
+  DecodeArgs a{};
+  a.capacity = capacity; a.Hkv = Hkv; a.B = B; a.inst_stride = inst_stride;
+  return make_map(map, base, a);
+}
+
 cudaError_t launch_decode_mma(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
   const StepArgs none{};
   switch (a.Hq / a.Hkv) {

@@ -426,6 +426,76 @@ kva_status kv_attn_decode_step(
   return cuda_status(e, "decode step launch");
 }
 
+static int verify_row_tiles(int G, int k) { return (G * k + 15) / 16; }
+
+size_t kva_verify_workspace_size(int32_t B, int32_t n_kv_heads, int32_t n_q_heads, int32_t k, int32_t max_len,
+                                 int32_t head_dim) {
+  if (B <= 0 || n_kv_heads <= 0 || n_q_heads <= 0 || k <= 0 || max_len <= 0 || head_dim <= 0 ||
+      n_q_heads % n_kv_heads != 0)
+    return 0;
+  const int RT = verify_row_tiles(n_q_heads / n_kv_heads, k);
+  return decode_ws_bytes(B, n_kv_heads * RT, n_kv_heads * RT * 16, decode_max_chunks_bound(max_len), head_dim);
+}
+
+kva_status kv_attn_verify(
+    const void* q, kva_dtype q_dtype, kva_cache cache,
+    const int32_t* lengths, const int32_t* lengths_host, int32_t B, int32_t k, int32_t n_q_heads,
+    float scale, float* out, void* workspace, size_t workspace_bytes, kva_stream stream) {
+  if (B < 0) return fail(KVA_EINVAL, "B=%d must be >= 0", B);
+  if (B == 0) return KVA_OK;
+  if (k < 1 || k > KVA_VERIFY_MAX_BLOCK) return fail(KVA_EINVAL, "block size k=%d outside [1, %d]", k, KVA_VERIFY_MAX_BLOCK);
+  if (!valid_dtype(q_dtype)) return fail(KVA_EINVAL, "unknown q dtype");
+  kva_status st = check_cache(cache, B);
+  if (st != KVA_OK) return st;
+  const int D = cache.head_dim, Hkv = cache.n_kv_heads;
+  if (n_q_heads <= 0 || n_q_heads % Hkv != 0)
+    return fail(KVA_EINVAL, "n_q_heads %d must be a positive multiple of n_kv_heads %d", n_q_heads, Hkv);
+  if (!q || !out || !lengths || !lengths_host) return fail(KVA_EINVAL, "NULL q/out/lengths");
+  if (cache.dtype != KVA_BF16 || D != DECODE_HEAD_DIM)
+    return fail(KVA_EUNSUPPORTED, "verify: needs a bf16 cache with head_dim 128");
+  if (!workspace) return fail(KVA_EWORKSPACE, "verify: workspace is NULL");
+  if (!aligned16(workspace)) return fail(KVA_EALIGN, "workspace must be 16-byte aligned");
+  const int G = n_q_heads / Hkv, RT = verify_row_tiles(G, k);
+  if (B > 65535 || Hkv * RT > 65535) return fail(KVA_EUNSUPPORTED, "verify: B or Hkv * row tiles > 65535");
+  int max_len = 0;
+  for (int b = 0; b < B; ++b) {
+    const int L = lengths_host[b];
+    if (L < k || L > cache.capacity)
+      return fail(KVA_ECAPACITY, "length %d of instance %d outside [k=%d, %d]", L, b, k, cache.capacity);
+    max_len = std::max(max_len, L);
+  }
+  const int chunk = decode_plan_chunk(lengths_host, B, Hkv * RT, max_len);
+  const int max_chunks = (max_len + chunk - 1) / chunk;
+  const size_t need = decode_ws_bytes(B, Hkv * RT, Hkv * RT * 16, max_chunks, D);
+  if (workspace_bytes < need)
+    return fail(KVA_EWORKSPACE, "verify workspace %zu bytes < %zu needed", workspace_bytes, need);
+  VerifyArgs a{};
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  const size_t zero = decode_zero_bytes(B, Hkv * RT);
+  a.counters = reinterpret_cast<unsigned*>(ws);
+  a.part_ml = reinterpret_cast<float*>(ws + zero);
+  a.part_acc = reinterpret_cast<float*>(ws + zero + round_up(sizeof(float) * (size_t)B * Hkv * RT * 16 * max_chunks * 2, 256));
+  a.q = q; a.kc = cache.k; a.vc = cache.v; a.lengths = lengths; a.out = out;
+  a.B = B; a.k = k; a.Hq = n_q_heads; a.Hkv = Hkv; a.RT = RT; a.capacity = cache.capacity;
+  a.chunk = chunk; a.max_chunks = max_chunks; a.inst_stride = cache.inst_stride;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+  a.scale_log2 = sc * 1.4426950408889634f;
+  cudaError_t e = launch_verify(a, q_dtype, (cudaStream_t)stream);
+  if (e == cudaSuccess) count_launches(1);
+  return cuda_status(e, "verify launch");
+}
+
+kva_status kv_verify_commit(const int32_t* posterior, const int32_t* block_tokens, int32_t B, int32_t k,
+                            int32_t* lengths, int32_t* accepted, int32_t* next_token, kva_stream stream) {
+  if (B < 0 || k < 1) return fail(KVA_EINVAL, "B=%d must be >= 0 and k=%d >= 1", B, k);
+  if (B == 0) return KVA_OK;
+  if (!posterior || !block_tokens || !lengths || !accepted || !next_token)
+    return fail(KVA_EINVAL, "NULL posterior/block_tokens/lengths/accepted/next_token");
+  cudaError_t e = launch_verify_commit(posterior, block_tokens, B, k, lengths, accepted, next_token, (cudaStream_t)stream);
+  if (e == cudaSuccess) count_launches(1);
+  return cuda_status(e, "verify commit launch");
+}
+
 kva_status lmhead_argmax(
     const float* h, const void* W, kva_dtype w_dtype,
     int32_t B, int32_t H, int32_t V, int32_t V_rows,

@@ -1,6 +1,7 @@
 // Internal interface between the host entry points (kv_attn_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -60,6 +61,29 @@ struct DecodeArgs {
   int64_t inst_stride;
   float scale_log2;       // softmax scale * log2(e)
 };
+
+// Multi-query verify block (kv_attn_verify): k query rows per instance, row i attending to
+// slots [0, L - k + i].  Rows are (block position i, head j of the group) -> r = i * G + j,
+// 16 per CTA; RT = ceil(G * k / 16) row tiles per (instance, KV head).
+struct VerifyArgs {
+  const void* q;          // [B, k, Hq, D]
+  const void* kc;
+  const void* vc;
+  const int32_t* lengths; // [B] valid slots, the block's k tokens included
+  float* out;             // [B, k, Hq, D]
+  unsigned int* counters; // [B, Hkv, RT] zero on entry, zero on exit
+  float* part_acc;        // [B, Hkv, RT, 16, max_chunks, D]
+  float* part_ml;         // [B, Hkv, RT, 16, max_chunks, 2]
+  int B, k, Hq, Hkv, RT, capacity, chunk, max_chunks;
+  int64_t inst_stride;
+  float scale_log2;
+};
+cudaError_t launch_verify(const VerifyArgs& a, kva_dtype q_dtype, cudaStream_t s);
+// (D=128 bf16 cache) 4-D TMA map over a cache with boxes of [16 slots x 64 dims].
+cudaError_t decode_cache_map(CUtensorMap* map, const void* base, int capacity, int Hkv, int B, int64_t inst_stride);
+// Acceptance and commit of verify blocks (one thread per instance).
+cudaError_t launch_verify_commit(const int32_t* posterior, const int32_t* block_tokens, int B, int k,
+                                 int32_t* lengths, int32_t* accepted, int32_t* next_token, cudaStream_t s);
 
 // Raw inputs of the new token for the fused append + decode step (kv_attn_decode_step).
 struct StepArgs {

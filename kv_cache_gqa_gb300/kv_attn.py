@@ -66,6 +66,12 @@ def lib() -> C.CDLL:
         L.kv_attn_decode_step.argtypes = [vp, vp, vp, C.c_int, vp, i64, _Norm, _Rope, _Cache, vp, vp, i32, i32,
                                           C.c_float, vp, C.c_int, vp, vp, sz, vp]
         L.kv_attn_decode_step.restype = C.c_int
+        L.kv_attn_verify.argtypes = [vp, C.c_int, _Cache, vp, vp, i32, i32, i32, C.c_float, vp, vp, sz, vp]
+        L.kv_attn_verify.restype = C.c_int
+        L.kva_verify_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        L.kva_verify_workspace_size.restype = sz
+        L.kv_verify_commit.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp]
+        L.kv_verify_commit.restype = C.c_int
         L.kv_attn_decode_static.argtypes = [vp, C.c_int, _Cache, vp, vp, i32, i32, C.c_float, vp, vp]
         L.kv_attn_decode_static.restype = C.c_int
         L.lmhead_argmax.argtypes = [vp, vp, C.c_int, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
@@ -239,6 +245,28 @@ def kv_attn_decode_step(q, k, v, pos, cache: KVCache, lengths, lengths_host, out
         _ptr(lengths), lh.ctypes.data, B, Hq, float(scale), _ptr(q_out),
         _dtype_code(q_out) if q_out is not None else 0, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def verify_workspace_bytes(B: int, n_kv_heads: int, n_q_heads: int, k: int, max_len: int, head_dim: int) -> int:
+    return int(lib().kva_verify_workspace_size(B, n_kv_heads, n_q_heads, k, max_len, head_dim))
+
+
+def kv_attn_verify(q, cache: KVCache, lengths, lengths_host, out, workspace, scale: float = 0.0, stream=None):
+    """q [B,k,Hq,D] (CUDA, f32|bf16): the block's queries, its tokens already in the last k valid
+    slots; lengths [B] int32 CUDA (slots incl. the block) + host copy; out [B,k,Hq,D] f32."""
+    B, k, Hq, _ = q.shape
+    lh = _host_i32(lengths_host)
+    _check(lib().kv_attn_verify(_ptr(q), _dtype_code(q), cache.struct, _ptr(lengths), lh.ctypes.data, B, k, Hq,
+                                float(scale), _ptr(out), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kv_verify_commit(posterior, block_tokens, lengths, accepted, next_token, stream=None):
+    """posterior, block_tokens [B,k] int32 CUDA; lengths [B] int32 CUDA (updated in place);
+    accepted, next_token [B] int32 CUDA outputs."""
+    B, k = block_tokens.shape
+    _check(lib().kv_verify_commit(_ptr(posterior), _ptr(block_tokens), B, k, _ptr(lengths), _ptr(accepted),
+                                  _ptr(next_token), _stream(stream)))
 
 
 def lmhead_argmax(h, W, out_ids, workspace, V: Optional[int] = None, out_max=None, logits=None,

@@ -134,6 +134,27 @@ def test_decode_step_validation(K):
     assert step([3], rope=_rope(kind=2, secs=(16, 16, 16, 8), n_axes=4)) == K.KVA_EINVAL
 
 
+def test_verify_validation(K):
+    L = K.lib()
+    def ver(lens, k=2, ws=FAKE, ws_bytes=1 << 30, cache=None, Hq=16):
+        lh = np.asarray(lens, np.int32)
+        return L.kv_attn_verify(FAKE, 1, cache or _cache(FAKE, cap=64), FAKE, lh.ctypes.data, len(lens), k, Hq,
+                                0.0, FAKE, ws, ws_bytes, None)
+    assert ver([]) == K.KVA_OK
+    assert ver([3], k=0) == K.KVA_EINVAL
+    assert ver([3], k=65) == K.KVA_EINVAL                                    # beyond the largest block
+    assert ver([1], k=2) == K.KVA_ECAPACITY                                  # fewer slots than block tokens
+    assert ver([65]) == K.KVA_ECAPACITY
+    assert ver([3], ws=None) == K.KVA_EWORKSPACE
+    assert ver([3], ws_bytes=16) == K.KVA_EWORKSPACE
+    assert ver([3], cache=_cache(FAKE, dtype=0, cap=64)) == K.KVA_EUNSUPPORTED
+    assert ver([3], Hq=12) == K.KVA_EINVAL
+    assert L.kva_verify_workspace_size(4, 8, 16, 16, 1000, 128) > L.kva_verify_workspace_size(4, 8, 16, 1, 1000, 128)
+    assert L.kv_verify_commit(FAKE, FAKE, 0, 4, FAKE, FAKE, FAKE, None) == K.KVA_OK
+    assert L.kv_verify_commit(None, FAKE, 2, 4, FAKE, FAKE, FAKE, None) == K.KVA_EINVAL
+    assert L.kv_verify_commit(FAKE, FAKE, 2, 0, FAKE, FAKE, FAKE, None) == K.KVA_EINVAL
+
+
 def test_lmhead_validation(K):
     L = K.lib()
     def lm(B=1, H=1024, V=100, Vr=100, ws=FAKE, wsb=1 << 20, h=FAKE):
