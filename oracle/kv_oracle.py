@@ -311,6 +311,32 @@ def argmax_lowest(z) -> tuple[int, float, float]:
     return i, float(top), margin
 
 
+def topk_lowest(z, k: int):
+    """The k largest entries of z as (ids [k], values [k]), ordered by value descending and, among
+    equal values, by id ascending (the argmax tie rule extended to a ranking).  A plain sort on
+    (-value, id)."""
+    z = np.asarray(z, dtype=F64)
+    order = sorted(range(z.shape[0]), key=lambda v: (-z[v], v))[:k]
+    return np.asarray(order, dtype=np.int64), z[order]
+
+
+def lmhead_topk(h, W, V: int, k: int, norm_w=None, eps: float = 1e-6):
+    """Greedy step with the final RMSNorm in front of the tied lm_head (Youtu-VL-4B port,
+    "decoding and sampling": every step takes final RMSNorm, then lm_head logits over the whole
+    vocabulary, then the highest-probability token; step 8), returning the k best ids and their
+    logits per row of h [B, H] (top_k is one of the generation options of the published
+    interface, HunyuanOCR v1.5 port, section 3.6; k = 1 is the greedy id).  norm_w None skips
+    the norm."""
+    h = np.atleast_2d(np.asarray(h, dtype=F64))
+    if norm_w is not None:
+        h = np.stack([rms_norm(row, norm_w, eps) for row in h])
+    ids, vals = [], []
+    for row in h:
+        i, v = topk_lowest(lm_logits(row, W, V), k)
+        ids.append(i); vals.append(v)
+    return np.stack(ids), np.stack(vals)
+
+
 def lmhead_argmax(h, W, V: int):
     """For each row of h [B, H]: (ids [B], max [B], margin [B]).  Only the first V
     rows are candidates: the selector clamps the vocab to the logits length

@@ -464,3 +464,43 @@ def test_verify_accept_is_lossless_for_greedy():
         while len(chain) < len(emitted):
             chain.append(int(nxt[chain[-1]]))
         assert emitted == chain
+
+
+# ----------------------------------------------------------------------------
+# final RMSNorm + lm_head top-k
+# ----------------------------------------------------------------------------
+def test_topk_hand_ties_and_order():
+    z = np.array([0.5, 2.0, -1.0, 2.0, 0.5, 3.0, 0.5])
+    ids, vals = O.topk_lowest(z, 5)
+    assert ids.tolist() == [5, 1, 3, 0, 4]             # 3.0; 2.0 twice (lower id first); 0.5 x3 -> 0, 4
+    assert vals.tolist() == [3.0, 2.0, 2.0, 0.5, 0.5]
+    # brute force: repeatedly take the first maximum and remove it
+    rng = np.random.default_rng(2)
+    for _ in range(50):
+        z = rng.integers(-3, 4, size=40).astype(np.float64)   # many ties
+        k = int(rng.integers(1, 12))
+        rest, picked = list(range(40)), []
+        for _ in range(k):
+            best = max(rest, key=lambda v: (z[v], -v))
+            picked.append(best); rest.remove(best)
+        assert O.topk_lowest(z, k)[0].tolist() == picked
+
+
+def test_lmhead_topk_top1_is_argmax_and_norm_is_scale_invariant():
+    rng = np.random.default_rng(4)
+    H, V = 64, 300
+    W = WL.f32_to_bf16_bits((0.02 * rng.standard_normal((V, H))).astype(np.float32))
+    h = rng.standard_normal((3, H))
+    ids1, vals1 = O.lmhead_topk(h, W, V, 1)
+    a_ids, a_max, _ = O.lmhead_argmax(h, W, V)
+    assert ids1[:, 0].tolist() == a_ids.tolist() and np.allclose(vals1[:, 0], a_max, rtol=0, atol=0)
+    w = 1 + 0.1 * rng.standard_normal(H)
+    ids_n, vals_n = O.lmhead_topk(h, W, V, 7, norm_w=w)
+    ids_s, vals_s = O.lmhead_topk(5.0 * h, W, V, 7, norm_w=w)          # RMSNorm removes the scale
+    assert ids_n.tolist() == ids_s.tolist()
+    np.testing.assert_allclose(vals_n, vals_s, rtol=1e-6)
+    # the norm is applied: equal to logits of the explicitly normalised rows
+    hn = np.stack([O.rms_norm(r, w, 1e-6) for r in h])
+    ref_ids, ref_vals = O.lmhead_topk(hn, W, V, 7)
+    assert ids_n.tolist() == ref_ids.tolist()
+    np.testing.assert_allclose(vals_n, ref_vals, rtol=1e-13)
