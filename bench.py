@@ -364,6 +364,16 @@ def run_gpu(args, rank, world, local_rank):
     # the dominant kernel alone: 32 back-to-back launches in one graph (its 311 MB table is larger
     # than L2, so every launch streams it from HBM as inside the job)
     lm_iso_ms = graph_avg_ms(torch, stream, lambda: K.lmhead_argmax(job.h[1], job.W, job.ids[1:2], job.lm_ws), 32)
+    # the same with the final RMSNorm fused in front (top 1), and the 8 best ids (logits + ranking)
+    fn_w = 1 + 0.1 * torch.randn(HIDDEN, device="cuda")
+    tk_ws = torch.zeros(K.lmhead_topk_workspace_bytes(1, HIDDEN, VOCAB, 8), dtype=torch.uint8, device="cuda")
+    tk_ids1 = torch.empty((1, 1), dtype=torch.int32, device="cuda")
+    tk_ids8 = torch.empty((1, 8), dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        K.lmhead_topk(job.h[1], job.W, tk_ids8, tk_ws, norm_w=fn_w)   # configures the kernels before capture
+    torch.cuda.synchronize()
+    lm_norm_ms = graph_avg_ms(torch, stream, lambda: K.lmhead_topk(job.h[1], job.W, tk_ids1, tk_ws, norm_w=fn_w), 32)
+    lm_top8_ms = graph_avg_ms(torch, stream, lambda: K.lmhead_topk(job.h[1], job.W, tk_ids8, tk_ws, norm_w=fn_w), 32)
 
     # speculative-decoding verify block on a cache larger than L2: 64 sequences x 2048 slots,
     # 16-token blocks (each launch streams 537 MB of K/V once for all 16 block rows)
@@ -449,6 +459,8 @@ def run_gpu(args, rank, world, local_rank):
                 "lm_head": {"GB/s": round(lm_gbs, 1), "frac_hbm": round(lm_gbs / hbm, 4),
                             "avg_launch_us": round(lm_iso_ms * 1e3, 2)},
                 "verify_block": dict(vb, frac_hbm=round(vb["GB/s"] / hbm, 4)),
+                "lm_head_final_norm_top1_us": round(lm_norm_ms * 1e3, 2),
+                "lm_head_final_norm_top8_us": round(lm_top8_ms * 1e3, 2),
                 "time_share": {k: round(v / sum(totals.values()), 4) for k, v in totals.items()},
                 "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": peak_src},
                 "timing": ("lm_head: graph of 32 back-to-back launches; prefill, append: " + kt_source +

@@ -291,6 +291,26 @@ kva_status lmhead_argmax(
     int32_t* out_ids, float* out_max, float* logits,
     void* workspace, size_t workspace_bytes, kva_stream stream);
 
+/* ---------------------------------------------------------------------------------
+ * lmhead_topk  (final RMSNorm + lm_head, k best ids)
+ *   Every decode step ends with the final RMSNorm, the tied lm_head over the whole vocabulary
+ *   and the pick of the best token (Youtu-VL-4B ncnn port, "decoding and sampling"; step 8);
+ *   top_k is one of the runtime's generation options (HunyuanOCR v1.5 ncnn port, section 3.6).
+ *   h_b' = h_b / sqrt(mean(h_b^2) + eps) * norm_w (skipped when norm_w is NULL), logits
+ *   z_b[v] = W[v] . h_b' for v < V, then the top_k best (id, logit) pairs per row ordered by
+ *   logit descending, equal logits toward the lower id.  The norm is applied inside the lm_head
+ *   kernels as they load h (no separate pass).  top_k = 1 is the greedy id through the fused
+ *   argmax; top_k > 1 writes the logits to the workspace and ranks each row in a second kernel.
+ *  h        [B,H] float32;  norm_w  [H] float32 or NULL;  W [V_rows,H] of w_dtype
+ *  out_ids  [B,top_k] int32;  out_vals [B,top_k] float32 or NULL
+ *  workspace: kva_lmhead_topk_workspace_size(B, H, V, top_k) bytes, counters zeroed once
+ *  (the calls leave them at zero).  1 <= top_k <= 32 and top_k <= V, else KVA_EINVAL. */
+kva_status lmhead_topk(
+    const float* h, const float* norm_w, float eps, const void* W, kva_dtype w_dtype,
+    int32_t B, int32_t H, int32_t V, int32_t V_rows, int32_t top_k,
+    int32_t* out_ids, float* out_vals, void* workspace, size_t workspace_bytes, kva_stream stream);
+size_t kva_lmhead_topk_workspace_size(int32_t B, int32_t H, int32_t V, int32_t top_k);
+
 size_t kva_lmhead_workspace_size(int32_t B, int32_t H);
 size_t kva_lmhead_workspace_zero_bytes(int32_t B);
 

@@ -9,8 +9,10 @@ Entry points (same names as the C ABI):
   kv_attn_verify               a speculative-decoding block: k query rows, causal inside the block
   kv_verify_commit             acceptance of the block's draft tokens and the cache-length commit
   lmhead_argmax                tied lm_head GEMV + greedy argmax (lowest id on ties)
+  lmhead_topk                  final RMSNorm + lm_head, the k best ids (k = 1: fused greedy argmax)
 """
 from .kv_attn import (KVCache, KvaError, Rope, decode_workspace_bytes, kv_attn_decode,  # noqa: F401
                       kv_attn_decode_step, kv_attn_verify, kv_verify_commit, verify_workspace_bytes,
                       kv_attn_prefill, kv_cache_append_rope_qknorm, launch_count, lib,
-                      lmhead_argmax, lmhead_workspace_bytes, version)
+                      lmhead_argmax, lmhead_topk, lmhead_topk_workspace_bytes, lmhead_workspace_bytes,
+                      version)

@@ -528,4 +528,62 @@ kva_status lmhead_argmax(
   return cuda_status(e, "lm_head launch");
 }
 
+size_t kva_lmhead_topk_workspace_size(int32_t B, int32_t H, int32_t V, int32_t top_k) {
+  if (B <= 0 || H <= 0 || V <= 0 || top_k <= 0) return 0;
+  size_t n = lmhead_workspace_bytes(B, H);
+  if (top_k > 1)
+    n += round_up(sizeof(float) * (size_t)B * V, 256) + round_up(sizeof(int32_t) * (size_t)B, 256) +
+         round_up(topk_rows_workspace_bytes(B, V), 256);
+  return n;
+}
+
+kva_status lmhead_topk(
+    const float* h, const float* norm_w, float eps, const void* W, kva_dtype w_dtype,
+    int32_t B, int32_t H, int32_t V, int32_t V_rows, int32_t top_k,
+    int32_t* out_ids, float* out_vals, void* workspace, size_t workspace_bytes, kva_stream stream) {
+  if (B < 0) return fail(KVA_EINVAL, "B=%d must be >= 0", B);
+  if (B == 0) return KVA_OK;
+  if (top_k < 1 || top_k > LMHEAD_TOPK_MAX) return fail(KVA_EINVAL, "top_k=%d outside [1, %d]", top_k, LMHEAD_TOPK_MAX);
+  if (!valid_dtype(w_dtype)) return fail(KVA_EINVAL, "unknown weight dtype");
+  if (H <= 0 || V <= 0 || V_rows <= 0) return fail(KVA_EINVAL, "H, V, V_rows must be positive");
+  if (V > V_rows) return fail(KVA_EINVAL, "vocab V=%d exceeds the table's %d rows", V, V_rows);
+  if (top_k > V) return fail(KVA_EINVAL, "top_k=%d exceeds the vocab %d", top_k, V);
+  if (norm_w && !(eps >= 0.f)) return fail(KVA_EINVAL, "final-norm eps must be >= 0");
+  if (H % 8 != 0) return fail(KVA_EALIGN, "hidden %d is not a multiple of 8", H);
+  if (H > lmhead_max_hidden()) return fail(KVA_EUNSUPPORTED, "hidden %d > %d", H, lmhead_max_hidden());
+  if (!h || !W || !out_ids) return fail(KVA_EINVAL, "NULL h/W/out_ids");
+  if (!aligned16(h) || !aligned16(W) || (norm_w && !aligned16(norm_w)))
+    return fail(KVA_EALIGN, "h, W and norm_w must be 16-byte aligned");
+  if (!workspace) return fail(KVA_EWORKSPACE, "lm_head: workspace is NULL");
+  if (!aligned16(workspace)) return fail(KVA_EALIGN, "workspace must be 16-byte aligned");
+  const size_t need = kva_lmhead_topk_workspace_size(B, H, V, top_k);
+  if (workspace_bytes < need) return fail(KVA_EWORKSPACE, "lm_head top-k workspace %zu bytes < %zu needed", workspace_bytes, need);
+  if (B > 65535) return fail(KVA_EUNSUPPORTED, "lm_head top-k: batch too large");
+  LmheadArgs a{};
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.counter = reinterpret_cast<unsigned*>(ws);
+  a.best = reinterpret_cast<unsigned long long*>(ws + 256);   // see lmhead_zero_bytes
+  a.h = h; a.W = W; a.B = B; a.H = H; a.V = V;
+  a.norm_w = norm_w; a.eps = eps;
+  float* logits = nullptr;
+  if (top_k == 1) {                                   // the greedy id: the fused argmax
+    a.out_ids = out_ids; a.out_max = out_vals;
+  } else {                                            // logits to the workspace, then a row top-k
+    unsigned char* extra = ws + lmhead_workspace_bytes(B, H);
+    logits = reinterpret_cast<float*>(extra);
+    a.logits = logits;
+    a.out_ids = reinterpret_cast<int32_t*>(extra + round_up(sizeof(float) * (size_t)B * V, 256));
+  }
+  unsigned n_launch = 0;
+  cudaError_t e = launch_lmhead(a, w_dtype, ws + lmhead_zero_bytes(B), (cudaStream_t)stream, &n_launch);
+  if (e == cudaSuccess && top_k > 1) {
+    unsigned char* rank_ws = ws + lmhead_workspace_bytes(B, H) + round_up(sizeof(float) * (size_t)B * V, 256) +
+                             round_up(sizeof(int32_t) * (size_t)B, 256);
+    e = launch_topk_rows(logits, B, V, top_k, rank_ws, out_ids, out_vals, (cudaStream_t)stream);
+    ++n_launch;
+  }
+  if (e == cudaSuccess) count_launches(n_launch);
+  return cuda_status(e, "lm_head top-k launch");
+}
+
 }  // extern "C"

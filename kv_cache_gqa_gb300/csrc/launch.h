@@ -124,6 +124,8 @@ struct LmheadArgs {
   float* logits;             // [B, V] or null
   unsigned long long* best;  // [B] zero on entry, zero on exit
   unsigned int* counter;     // [1] zero on entry, zero on exit
+  const float* norm_w;       // [H] final RMSNorm weight applied to h first, or null
+  float eps;
   int B, H, V;
 };
 size_t lmhead_workspace_bytes(int B, int H);
@@ -131,6 +133,14 @@ size_t lmhead_zero_bytes(int B);
 // Launches the lm_head for `a`; *n_launches receives the number of kernels enqueued.
 cudaError_t launch_lmhead(const LmheadArgs& a, kva_dtype w_dtype, void* hb_scratch, cudaStream_t s,
                           unsigned* n_launches);
+// Top-k of each row of logits [B, V] (k <= 32): ids and values ordered by value descending,
+// ties toward the lower id.
+constexpr int LMHEAD_TOPK_MAX = 32;
+// workspace: topk_rows_workspace_bytes(B, V), its first round_up(4 B, 256) bytes (per-row
+// tickets) zero on entry and left at zero.
+size_t topk_rows_workspace_bytes(int B, int V);
+cudaError_t launch_topk_rows(const float* logits, int B, int V, int k, void* workspace, int32_t* out_ids,
+                             float* out_vals, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------
 struct PrefillArgs {

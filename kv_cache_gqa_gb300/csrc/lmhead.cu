@@ -43,6 +43,19 @@ lmhead_kernel(const __grid_constant__ LmheadArgs a) {
 
   for (int i = tid; i < nb * H; i += THREADS) sh[i] = a.h[(int64_t)b0 * H + i];
   __syncthreads();
+  if (a.norm_w) {                                 // final RMSNorm of each staged row
+    __shared__ float s_r[BG];
+    for (int b = warp; b < nb; b += WARPS) {
+      float ss = 0.f;
+      for (int i = lane; i < H; i += 32) ss = fmaf(sh[b * H + i], sh[b * H + i], ss);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+      if (lane == 0) s_r[b] = rsqrtf(ss / (float)H + a.eps);
+    }
+    __syncthreads();
+    for (int i = tid; i < nb * H; i += THREADS) sh[i] *= s_r[i / H] * a.norm_w[i % H];
+    __syncthreads();
+  }
 
   float best_v[BG];
   int best_i[BG];
@@ -121,6 +134,27 @@ lmhead_kernel(const __grid_constant__ LmheadArgs a) {
   if (tid == 0) *a.counter = 0u;
 }
 
+// Final RMSNorm of h held in registers: lane owns elements (c * 32 + lane) * 8 + e, so a warp
+// holds the whole vector and the sum of squares is one warp reduction.
+template <int NCH>
+__device__ __forceinline__ void norm_h_regs(float (&hv)[NCH][8], const float* w, float eps, int H, int lane) {
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(hv[c][e], hv[c][e], ss);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+  const float r = rsqrtf(ss / (float)H + eps);
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>(w) + (c * 32 + lane) * 2);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(w) + (c * 32 + lane) * 2 + 1);
+    hv[c][0] *= r * u.x; hv[c][1] *= r * u.y; hv[c][2] *= r * u.z; hv[c][3] *= r * u.w;
+    hv[c][4] *= r * v.x; hv[c][5] *= r * v.y; hv[c][6] *= r * v.z; hv[c][7] *= r * v.w;
+  }
+}
+
 // ---------------------------------------------------------------------------------
 // Batch-1 fast path: a grid-stride GEMV over groups of 4 consecutive vocabulary rows per
 // warp.  All 16-byte loads of a group (4 rows x H/256 chunks per lane) are issued before
@@ -146,6 +180,7 @@ lmhead_b1_kernel(const __grid_constant__ LmheadArgs a) {
     hv[c][0] = u.x; hv[c][1] = u.y; hv[c][2] = u.z; hv[c][3] = u.w;
     hv[c][4] = w.x; hv[c][5] = w.y; hv[c][6] = w.z; hv[c][7] = w.w;
   }
+  if (a.norm_w) norm_h_regs<NCH>(hv, a.norm_w, a.eps, H, lane);
 
   float best_v = -INFINITY;
   int best_i = 0x7fffffff;
@@ -257,6 +292,7 @@ lmhead_b1_pipe_kernel(const __grid_constant__ LmheadArgs a, int rows_per_cta) {
     hv[c][0] = u.x; hv[c][1] = u.y; hv[c][2] = u.z; hv[c][3] = u.w;
     hv[c][4] = w.x; hv[c][5] = w.y; hv[c][6] = w.z; hv[c][7] = w.w;
   }
+  if (a.norm_w) norm_h_regs<NCH>(hv, a.norm_w, a.eps, H, lane);
   __syncthreads();
 
   float best_v = -INFINITY;

@@ -36,15 +36,32 @@ constexpr int THREADS = 192;
 constexpr int A_BYTES = TM * 128;       // 16 KB
 constexpr int MAX_N = 256;              // 2 * Bp
 
-__global__ void lmhead_split_kernel(const float* __restrict__ h, uint16_t* __restrict__ hb, int B, int Bp, int H) {
-  const int64_t total = (int64_t)2 * Bp * H;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int r = (int)(i / H), k = (int)(i % H);
-    const int b = r < Bp ? r : r - Bp;
+// One CTA per padded batch row b: the row's final RMSNorm (when norm_w is given), then its
+// bf16 high half into row b and the residual's bf16 into row Bp + b (rows >= B are zeros).
+__global__ void __launch_bounds__(256)
+lmhead_split_kernel(const float* __restrict__ h, const float* __restrict__ norm_w, float eps, uint16_t* __restrict__ hb,
+                    int B, int Bp, int H) {
+  const int b = blockIdx.x, tid = threadIdx.x;
+  __shared__ float s_part[8];
+  float r = 1.f;
+  if (norm_w && b < B) {
+    float ss = 0.f;
+    for (int k = tid; k < H; k += 256) { const float x = h[(int64_t)b * H + k]; ss = fmaf(x, x, ss); }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+    if ((tid & 31) == 0) s_part[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += s_part[w];
+    r = rsqrtf(tot / (float)H + eps);
+  }
+  for (int k = tid; k < H; k += 256) {
     float x = b < B ? h[(int64_t)b * H + k] : 0.f;
+    if (norm_w && b < B) x *= r * norm_w[k];
     const uint32_t hi = f32_to_bf16_rne(x);
-    if (r >= Bp) x = x - __uint_as_float(hi << 16);       // residual -> low half
-    hb[i] = (uint16_t)(r < Bp ? hi : f32_to_bf16_rne(x));
+    hb[(int64_t)b * H + k] = (uint16_t)hi;
+    hb[(int64_t)(Bp + b) * H + k] = (uint16_t)f32_to_bf16_rne(x - __uint_as_float(hi << 16));   // residual
   }
 }
 
@@ -258,8 +275,7 @@ cudaError_t launch_bp(const LmheadArgs& a, uint16_t* hb, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int64_t total = (int64_t)N * a.H;
-  lmhead_split_kernel<<<(int)std::min<int64_t>((total + 255) / 256, 1024), 256, 0, s>>>(a.h, hb, a.B, BP, a.H);
+  lmhead_split_kernel<<<BP, 256, 0, s>>>(a.h, a.norm_w, a.eps, hb, a.B, BP, a.H);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mw, mh;

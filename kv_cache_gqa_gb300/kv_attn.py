@@ -72,6 +72,10 @@ def lib() -> C.CDLL:
         L.kva_verify_workspace_size.restype = sz
         L.kv_verify_commit.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp]
         L.kv_verify_commit.restype = C.c_int
+        L.lmhead_topk.argtypes = [vp, vp, C.c_float, vp, C.c_int, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.lmhead_topk.restype = C.c_int
+        L.kva_lmhead_topk_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.kva_lmhead_topk_workspace_size.restype = sz
         L.kv_attn_decode_static.argtypes = [vp, C.c_int, _Cache, vp, vp, i32, i32, C.c_float, vp, vp]
         L.kv_attn_decode_static.restype = C.c_int
         L.lmhead_argmax.argtypes = [vp, vp, C.c_int, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
@@ -267,6 +271,22 @@ def kv_verify_commit(posterior, block_tokens, lengths, accepted, next_token, str
     B, k = block_tokens.shape
     _check(lib().kv_verify_commit(_ptr(posterior), _ptr(block_tokens), B, k, _ptr(lengths), _ptr(accepted),
                                   _ptr(next_token), _stream(stream)))
+
+
+def lmhead_topk_workspace_bytes(B: int, H: int, V: int, top_k: int) -> int:
+    return int(lib().kva_lmhead_topk_workspace_size(B, H, V, top_k))
+
+
+def lmhead_topk(h, W, out_ids, workspace, norm_w=None, eps: float = 1e-6, V=None, out_vals=None, stream=None):
+    """h [B,H] f32 CUDA; W [V_rows,H] f32|bf16 CUDA; norm_w [H] f32 CUDA or None (final RMSNorm);
+    out_ids [B,k] int32 CUDA (k = top_k); out_vals [B,k] f32 CUDA or None."""
+    h2 = h if h.dim() == 2 else h.view(1, -1)
+    B, H = h2.shape
+    k = out_ids.shape[-1] if out_ids.dim() > 1 else 1
+    V_rows = W.shape[0]
+    _check(lib().lmhead_topk(_ptr(h2), _ptr(norm_w), float(eps), _ptr(W), _dtype_code(W), B, H,
+                             V_rows if V is None else int(V), V_rows, k, _ptr(out_ids), _ptr(out_vals),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def lmhead_argmax(h, W, out_ids, workspace, V: Optional[int] = None, out_max=None, logits=None,

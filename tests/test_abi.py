@@ -170,6 +170,21 @@ def test_lmhead_validation(K):
     assert lm(H=8192) == K.KVA_EUNSUPPORTED
 
 
+def test_lmhead_topk_validation(K):
+    L = K.lib()
+    def tk(B=1, H=1024, V=100, Vr=100, k=4, ws=FAKE, wsb=1 << 24, norm=None, eps=1e-6):
+        return L.lmhead_topk(FAKE, norm, eps, FAKE, 1, B, H, V, Vr, k, FAKE, None, ws, wsb, None)
+    assert tk(B=0) == K.KVA_OK
+    assert tk(k=0) == K.KVA_EINVAL
+    assert tk(k=33) == K.KVA_EINVAL
+    assert tk(V=10, Vr=10, k=11) == K.KVA_EINVAL                            # more ranks than vocab
+    assert tk(V=101) == K.KVA_EINVAL
+    assert tk(norm=FAKE, eps=-1.0) == K.KVA_EINVAL
+    assert tk(norm=FAKE + 4) == K.KVA_EALIGN
+    assert tk(wsb=16) == K.KVA_EWORKSPACE
+    assert L.kva_lmhead_topk_workspace_size(2, 1024, 5000, 8) > L.kva_lmhead_topk_workspace_size(2, 1024, 5000, 1)
+
+
 def test_binding_refuses_cpu_tensors(K):
     torch = pytest.importorskip("torch")
     with pytest.raises(K.KvaError):
