@@ -57,7 +57,10 @@ typedef enum { KVA_F32 = 0, KVA_BF16 = 1 } kva_dtype;
 typedef enum {
   KVA_MASK_CAUSAL = 0,  /* key slot j visible to query slot i iff j <= i */
   KVA_MASK_FULL = 1,    /* all S keys visible (bidirectional vision layers) */
-  KVA_MASK_SEGMENT = 2  /* block diagonal: j visible iff segment[j] == segment[i] */
+  KVA_MASK_SEGMENT = 2, /* block diagonal: j visible iff segment[j] == segment[i] */
+  KVA_MASK_CAUSAL_SEGMENT = 3  /* j <= i or segment[j] == segment[i]: causal, with each segment
+                                  (an image span; a text token is its own segment) fully visible
+                                  to its own rows (MNN llm_demo walkthrough, section 3.3) */
 } kva_mask;
 
 typedef enum {
@@ -145,8 +148,9 @@ kva_status kv_cache_append_rope_qknorm(
  *          q row r(i) = row_of_slot[i] (or i when row_of_slot == NULL), and its output
  *          goes to out row r(i): this undoes a window permutation (the vision tower's
  *          window_index grouping: Youtu-VL-4B ncnn port, step 3).
- *  segment [S] int32 (device), non-decreasing window id per slot, for KVA_MASK_SEGMENT
- *          (else NULL); segment_host: its host mirror (validated: non-decreasing).
+ *  segment [S] int32 (device), non-decreasing segment id per slot, for KVA_MASK_SEGMENT
+ *          and KVA_MASK_CAUSAL_SEGMENT (else NULL); segment_host: its host mirror
+ *          (validated: non-decreasing).
  *  scale   softmax scale; <= 0 selects 1/sqrt(D).
  *  out     [N,S,Hq,D] float32 (device).
  *  Errors: KVA_EINVAL, KVA_ECAPACITY (S > capacity), KVA_EALIGN, KVA_EUNSUPPORTED

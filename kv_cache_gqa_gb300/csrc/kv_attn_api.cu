@@ -281,9 +281,9 @@ kva_status kv_attn_prefill(
     return fail(KVA_EINVAL, "n_q_heads %d must be a positive multiple of n_kv_heads %d", n_q_heads, Hkv);
   if (!q || !out) return fail(KVA_EINVAL, "NULL q/out");
   if (S > cache.capacity) return fail(KVA_ECAPACITY, "prefill S=%d > capacity %d", S, cache.capacity);
-  if (mask != KVA_MASK_CAUSAL && mask != KVA_MASK_FULL && mask != KVA_MASK_SEGMENT)
+  if (mask != KVA_MASK_CAUSAL && mask != KVA_MASK_FULL && mask != KVA_MASK_SEGMENT && mask != KVA_MASK_CAUSAL_SEGMENT)
     return fail(KVA_EINVAL, "mask %d unknown", (int)mask);
-  if (mask == KVA_MASK_SEGMENT) {
+  if (mask == KVA_MASK_SEGMENT || mask == KVA_MASK_CAUSAL_SEGMENT) {
     if (!segment || !segment_host) return fail(KVA_EINVAL, "segment mask needs segment ids");
     for (int i = 1; i < S; ++i)
       if (segment_host[i] < segment_host[i - 1])
@@ -293,7 +293,7 @@ kva_status kv_attn_prefill(
   if (N > 65535 || n_q_heads > 65535) return fail(KVA_EUNSUPPORTED, "prefill: N or Hq > 65535");
   PrefillArgs a{};
   a.q = q; a.kc = cache.k; a.vc = cache.v;
-  a.segment = mask == KVA_MASK_SEGMENT ? segment : nullptr;
+  a.segment = (mask == KVA_MASK_SEGMENT || mask == KVA_MASK_CAUSAL_SEGMENT) ? segment : nullptr;
   a.row_of_slot = row_of_slot; a.out = out;
   a.N = N; a.S = S; a.Hq = n_q_heads; a.Hkv = Hkv; a.D = D; a.capacity = cache.capacity;
   a.mask = (int)mask; a.inst_stride = cache.inst_stride;

@@ -77,6 +77,8 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
     else if (a.mask == KVA_MASK_SEGMENT) {
       lo = seg_lower(a.segment, a.S, a.segment[i0]);
       hi = seg_upper(a.segment, a.S, a.segment[i1 - 1]);
+    } else if (a.mask == KVA_MASK_CAUSAL_SEGMENT) {
+      hi = seg_upper(a.segment, a.S, a.segment[i1 - 1]);   // the last row's segment end
     }
     s_range[0] = lo; s_range[1] = hi;
   }
@@ -147,6 +149,7 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
         bool ok = (i < i1) && j >= k_lo && j < k_hi;
         if (a.mask == KVA_MASK_CAUSAL) ok = ok && j <= i;
         else if (a.mask == KVA_MASK_SEGMENT) ok = ok && a.segment[j] == qs;
+        else if (a.mask == KVA_MASK_CAUSAL_SEGMENT) ok = ok && (j <= i || a.segment[j] == qs);
         s[r][u] = ok ? s[r][u] * a.scale_log2 : -INFINITY;
         mx = fmaxf(mx, s[r][u]);
       }

@@ -142,6 +142,8 @@ __device__ __forceinline__ void tile_keys(const PrefillArgs& a, int i0, int i_la
   } else if (a.mask == KVA_MASK_SEGMENT) {
     lo = seg_lower_tc(a.segment, a.S, a.segment[i0]);
     hi = seg_upper_tc(a.segment, a.S, a.segment[i_last]);
+  } else if (a.mask == KVA_MASK_CAUSAL_SEGMENT) {
+    hi = seg_upper_tc(a.segment, a.S, a.segment[i_last]);    // the last row's segment end
   }
 }
 
@@ -340,6 +342,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       if (row_ok) {
         if (a.mask == KVA_MASK_CAUSAL) { rlo = 0; rhi = i + 1; }
         else if (a.mask == KVA_MASK_FULL) { rlo = 0; rhi = a.S; }
+        else if (a.mask == KVA_MASK_CAUSAL_SEGMENT) { rlo = 0; rhi = seg_upper_tc(a.segment, a.S, a.segment[i]); }
         else { const int sg = a.segment[i]; rlo = seg_lower_tc(a.segment, a.S, sg); rhi = seg_upper_tc(a.segment, a.S, sg); }
       }
       const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);

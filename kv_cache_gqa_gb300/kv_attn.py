@@ -20,7 +20,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkv_attn
 # enums (include/kv_attn.h)
 KVA_OK, KVA_EINVAL, KVA_ECAPACITY, KVA_EUNSUPPORTED, KVA_ECUDA, KVA_EALIGN, KVA_EWORKSPACE = range(7)
 KVA_F32, KVA_BF16 = 0, 1
-MASKS = {"causal": 0, "full": 1, "segment": 2}
+MASKS = {"causal": 0, "full": 1, "segment": 2, "causal_segment": 3}
 ROPE_KINDS = {"none": 0, "1d": 1, "sections": 2, "2d": 3}
 
 

@@ -232,6 +232,12 @@ def prefill_mask(S: int, kind: str, segment=None) -> np.ndarray:
     if kind == "segment":
         seg = np.asarray(segment)
         return seg[:, None] == seg[None, :]
+    if kind == "causal_segment":
+        # causal, plus every key of the row's own segment: an image span (one segment) is
+        # visible as a whole to its rows while text keeps the causal mask (MNN llm_demo
+        # walkthrough, section 3.3); a text token is a segment of its own
+        seg = np.asarray(segment)
+        return (j <= i) | (seg[:, None] == seg[None, :])
     raise ValueError(kind)
 
 

@@ -96,6 +96,8 @@ def test_prefill_validation(K):
     assert pf(mask=2) == K.KVA_EINVAL                                       # segment mask without ids
     assert pf(mask=2, seg=FAKE, segh=seg_bad.ctypes.data) == K.KVA_EINVAL   # not non-decreasing
     assert pf(mask=7) == K.KVA_EINVAL
+    assert pf(mask=3) == K.KVA_EINVAL                                       # causal-segment without ids
+    assert pf(mask=3, seg=FAKE, segh=seg_bad.ctypes.data) == K.KVA_EINVAL
 
 
 def test_decode_validation(K):

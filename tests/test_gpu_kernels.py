@@ -237,6 +237,36 @@ def test_prefill_d72_mha_permuted(K, dt, mask):
     _prefill_case(K, 72, 150, mask, dt, 1, seed=99, Hkv=3, perm=True)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("layout", ["image", "spans"])
+def test_prefill_causal_segment(K, dt, layout):
+    """Causal mask with image spans fully visible to their own rows."""
+    torch = T()
+    rng = np.random.default_rng(zlib.crc32(repr(("cseg", dt, layout)).encode()))
+    if layout == "image":
+        seg = WL.image_span_segments(20, 16, 16, 218)          # the 512-row image-span prompt
+    else:                                                     # several spans, ragged tail
+        seg = np.arange(300, dtype=np.int32)
+        for s0, s1 in ((5, 40), (120, 130), (131, 256), (290, 300)):
+            seg[s0:s1] = s0
+    S, N, Hkv, Hq, D = seg.size, 2, 2, 4, 128
+    q = O.store(rng.standard_normal((N, S, Hq, D)), dt)
+    kc = O.store(rng.standard_normal((N, Hkv, S + 8, D)), dt)
+    vc = O.store(rng.standard_normal((N, Hkv, S + 8, D)), dt)
+    out = T().empty((N, S, Hq, D), device="cuda")
+    tdt = _tdt(dt)
+    K.kv_attn_prefill(dev(q, tdt), K.KVCache(dev(kc, tdt), dev(vc, tdt)), out, mask="causal_segment",
+                      segment=dev(seg), segment_host=seg)
+    torch.cuda.synchronize()
+    got = host(out)
+    for n in range(N):
+        ref = O.prefill(q[n], kc[n], vc[n], S, "causal_segment", seg)
+        if dt == "f32":
+            assert_fp32_close(got[n], ref, f"causal_segment n={n}")
+        else:
+            assert_bf16_close(got[n].reshape(-1, D), ref.reshape(-1, D), f"causal_segment n={n}")
+
+
 @pytest.mark.parametrize("G", [1, 4])
 def test_prefill_group_sizes(K, G):
     _prefill_case(K, 128, 130, "causal", "bf16", G, seed=G)

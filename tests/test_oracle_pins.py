@@ -504,3 +504,35 @@ def test_lmhead_topk_top1_is_argmax_and_norm_is_scale_invariant():
     ref_ids, ref_vals = O.lmhead_topk(hn, W, V, 7)
     assert ids_n.tolist() == ref_ids.tolist()
     np.testing.assert_allclose(vals_n, ref_vals, rtol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# image span fully visible to its own rows (MNN llm_demo walkthrough, section 3.3)
+# ----------------------------------------------------------------------------
+def test_causal_segment_mask_reduces_and_spans():
+    S = 30
+    uniq = np.arange(S)
+    assert np.array_equal(O.prefill_mask(S, "causal_segment", uniq), O.prefill_mask(S, "causal"))
+    assert np.array_equal(O.prefill_mask(S, "causal_segment", np.zeros(S, int)), O.prefill_mask(S, "full"))
+    seg = WL.image_span_segments(3, 2, 4, 5)           # 3 text, begin, 2x5 grid rows, end, 5 text
+    m = O.prefill_mask(seg.size, "causal_segment", seg)
+    g0, g1 = 4, 14
+    for i in range(seg.size):
+        vis = np.nonzero(m[i])[0]
+        end = g1 if g0 <= i < g1 else i + 1            # a grid row sees the whole grid
+        assert vis.tolist() == list(range(end)), i
+    # text after the span sees the span (causally) but the begin marker does not see it
+    assert m[g1 + 1, g0:g1].all() and not m[g0 - 1, g0:g1].any()
+
+
+def test_causal_segment_prefill_equals_bidirectional_span_by_hand():
+    """Span rows attend over [0, span end): equal to attend() with that explicit key range."""
+    rng = np.random.default_rng(8)
+    seg = WL.image_span_segments(2, 2, 2, 3)
+    S, Hq, Hkv, D = seg.size, 2, 1, 4
+    q = rng.standard_normal((S, Hq, D)); ck = rng.standard_normal((Hkv, S, D)); cv = rng.standard_normal((Hkv, S, D))
+    out = O.prefill(q, ck, cv, S, "causal_segment", seg)
+    for i in range(S):
+        end = int(np.max(np.nonzero(seg == seg[i])[0])) + 1 if np.sum(seg == seg[i]) > 1 else i + 1
+        allowed = np.zeros((1, S), bool); allowed[0, :end] = True
+        np.testing.assert_allclose(out[i], O.attend(q[i:i + 1], ck, cv, allowed)[0], rtol=1e-13, atol=1e-15)

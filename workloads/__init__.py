@@ -91,6 +91,18 @@ def image_span_positions(text_before: int, grid_h: int, grid_w: int,
     return np.asarray(rows, dtype=np.int32)
 
 
+def image_span_segments(text_before: int, grid_h: int, grid_w: int, text_after: int) -> np.ndarray:
+    """Segment ids [S] for the layout of image_span_positions: every text row (the span's begin
+    and end markers included) is a segment of its own (id = its index); the h*(w+1) grid rows
+    of the span share one id (the index of the first grid row).  Non-decreasing."""
+    S = text_before + 2 + grid_h * (grid_w + 1) + text_after
+    seg = np.arange(S, dtype=np.int32)
+    g0 = text_before + 1
+    g1 = g0 + grid_h * (grid_w + 1)
+    seg[g0:g1] = g0
+    return seg
+
+
 @dataclasses.dataclass
 class VisionLayout:
     pos_rc: np.ndarray       # [S, 2] int32 (row, col) of each patch, natural row-major order
