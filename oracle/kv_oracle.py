@@ -96,6 +96,10 @@ class Rope:
                      section contains j (xdRoPE sections [16,16,16,16]).
     kind '2d':       two blocks of width D/2; block b uses position axis b
                      (dims 0..D/2-1 rows, D/2..D-1 columns).
+    kind 'interleaved': the 1D rotation after a de-interleave: the head is first reordered
+                     to [x0, x2, ..., x_{D-2}, x1, x3, ..., x_{D-1}] (view as [D/2, 2],
+                     transpose), then rotated like '1d'; the result stays in that order
+                     (rope_interleave: Youtu-VL-4B port, implementation difficulty 2).
     kind 'none':     no rotation.
     """
 
@@ -138,6 +142,11 @@ def rope_apply(x, pos, rope: Rope) -> np.ndarray:
             assert axis_of_j.shape[0] == D // 2, "sections must cover D/2 frequencies"
         ang = pos[:, axis_of_j] * inv[None, :]                # [T, D/2]
         return rotate_half_apply(x, ang[:, None, :])
+    if rope.kind == "interleaved":
+        # de-interleave (x.view(D/2, 2).transpose) then the standard rotate-half
+        xd = np.concatenate([x[..., 0::2], x[..., 1::2]], axis=-1)
+        ang = pos[:, 0:1] * inv_freq(rope.base, D)[None, :]   # [T, D/2]
+        return rotate_half_apply(xd, ang[:, None, :])
     if rope.kind == "2d":
         half = D // 2
         inv = inv_freq(rope.base, half)                       # [D/4]

@@ -536,3 +536,54 @@ def test_causal_segment_prefill_equals_bidirectional_span_by_hand():
         end = int(np.max(np.nonzero(seg == seg[i])[0])) + 1 if np.sum(seg == seg[i]) > 1 else i + 1
         allowed = np.zeros((1, S), bool); allowed[0, :end] = True
         np.testing.assert_allclose(out[i], O.attend(q[i:i + 1], ck, cv, allowed)[0], rtol=1e-13, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# interleaved RoPE (Youtu-VL-4B port, implementation difficulty 2)
+# ----------------------------------------------------------------------------
+def test_rope_interleaved_hand_example():
+    """D = 4, base 100: output [a c0 - b s0, c c1 - d s1, b c0 + a s0, d c1 + c s1] for input
+    [a, b, c, d] (pairs (a, b) and (c, d) rotated, results de-interleaved)."""
+    a, b, c, d = 0.3, -1.1, 2.0, 0.7
+    p = 5
+    t0, t1 = p * 1.0, p * 100.0 ** -0.5
+    got = O.rope_apply(np.array([[[a, b, c, d]]]), np.array([[p]]), O.Rope("interleaved", 100.0))[0, 0]
+    ref = [a * math.cos(t0) - b * math.sin(t0), c * math.cos(t1) - d * math.sin(t1),
+           b * math.cos(t0) + a * math.sin(t0), d * math.cos(t1) + c * math.sin(t1)]
+    np.testing.assert_allclose(got, ref, rtol=1e-14, atol=1e-15)
+
+
+def test_rope_interleaved_matches_the_pages_matrix_form():
+    """The page rewrites the step as two constant matrices: q_rot = (q @ P) * cos + (q @ PR) * sin
+    with P the de-interleave permutation and PR = P @ R (R the rotate-half +-1 matrix)."""
+    rng = np.random.default_rng(6)
+    D, T = 64, 9
+    P = np.zeros((D, D))
+    for j in range(D // 2):
+        P[2 * j, j] = 1.0                     # column j of the output takes x_{2j}
+        P[2 * j + 1, D // 2 + j] = 1.0        # column D/2 + j takes x_{2j+1}
+    R = np.zeros((D, D))                      # y @ R = rotate_half(y) = [-y2, y1]
+    for j in range(D // 2):
+        R[D // 2 + j, j] = -1.0
+        R[j, D // 2 + j] = 1.0
+    x = rng.standard_normal((T, 1, D))
+    pos = rng.integers(0, 3000, size=(T, 1))
+    inv = O.inv_freq(1e6, D)
+    ang = np.concatenate([pos * inv[None, :], pos * inv[None, :]], axis=1)     # [T, D]
+    ref = (x[:, 0] @ P) * np.cos(ang) + (x[:, 0] @ (P @ R)) * np.sin(ang)
+    np.testing.assert_allclose(O.rope_apply(x, pos, O.Rope("interleaved", 1e6))[:, 0], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_rope_interleaved_pairs_position_zero_and_relative_property():
+    rng = np.random.default_rng(12)
+    D = 32
+    x = rng.standard_normal((1, 1, D))
+    rope = O.Rope("interleaved", 1e6)
+    y0 = O.rope_apply(x, np.array([[0]]), rope)[0, 0]
+    np.testing.assert_array_equal(y0, np.concatenate([x[0, 0, 0::2], x[0, 0, 1::2]]))   # pure de-interleave
+    y = O.rope_apply(x, np.array([[777]]), rope)[0, 0]
+    np.testing.assert_allclose(y[:D // 2] ** 2 + y[D // 2:] ** 2, x[0, 0, 0::2] ** 2 + x[0, 0, 1::2] ** 2, rtol=1e-13)
+    q, k = rng.standard_normal((1, 1, D)), rng.standard_normal((1, 1, D))
+    d1 = np.dot(O.rope_apply(q, np.array([[50]]), rope)[0, 0], O.rope_apply(k, np.array([[20]]), rope)[0, 0])
+    d2 = np.dot(O.rope_apply(q, np.array([[1030]]), rope)[0, 0], O.rope_apply(k, np.array([[1000]]), rope)[0, 0])
+    assert abs(d1 - d2) < 1e-10
