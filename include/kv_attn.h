@@ -67,7 +67,10 @@ typedef enum {
   KVA_ROPE_NONE = 0,
   KVA_ROPE_1D = 1,       /* rotate-half over D, every frequency uses position axis 0 */
   KVA_ROPE_SECTIONS = 2, /* xdRoPE: frequency j uses the axis whose section holds j */
-  KVA_ROPE_2D = 3        /* two halves of D/2, each rotate-half; half b uses axis b */
+  KVA_ROPE_2D = 3,       /* two halves of D/2, each rotate-half; half b uses axis b */
+  KVA_ROPE_INTERLEAVED = 4  /* de-interleave x to [x0,x2,..,x1,x3,..] then 1D rotate-half; the
+                               output (q_out, cache K) stays in that order (rope_interleave:
+                               Youtu-VL-4B ncnn port, implementation difficulty 2) */
 } kva_rope_kind;
 
 /* One cache: N instances (layers and/or sequences) of K and V, each

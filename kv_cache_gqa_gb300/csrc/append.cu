@@ -221,6 +221,31 @@ append_kernel(const __grid_constant__ AppendArgs a) {
 }
 
 
+__device__ __forceinline__ void load4_smem(const float* p, float (&x)[4]) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+}
+__device__ __forceinline__ void load4_smem(const bf16_t* p, float (&x)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+}
+__device__ __forceinline__ void store4(float* p, const float (&y)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
+}
+__device__ __forceinline__ void store4(bf16_t* p, const float (&y)[4]) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+}
+
+__device__ __forceinline__ void load8_smem(const float* p, float (&x)[8]) {
+  const float4 u = reinterpret_cast<const float4*>(p)[0], w = reinterpret_cast<const float4*>(p)[1];
+  x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w; x[4] = w.x; x[5] = w.y; x[6] = w.z; x[7] = w.w;
+}
+__device__ __forceinline__ void load8_smem(const bf16_t* p, float (&x)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+  x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+}
+
 // Warp-per-token form.  tpc = tokens per CTA (1, 2, 4 or 8); the 8 / tpc warps of a token
 // take its row groups round-robin.
 template <int D, typename InT, typename QOutT, typename CacheT>
@@ -258,6 +283,9 @@ append_warp_kernel(const __grid_constant__ AppendArgs a, int tpc) {
   const int32_t slot = a.slot[(int64_t)n * a.slot_stride + t];
   const bool rotate = a.rope.kind != KVA_ROPE_NONE;
   const bool two_d = a.rope.kind == KVA_ROPE_2D;
+  // interleaved RoPE: the lane's 8 inputs are the pairs j = e0/2 .. e0/2 + 3, whose rotated
+  // values land at outputs j (x[0..3] after the rotation) and D/2 + j (x[4..7])
+  const bool inter = a.rope.kind == KVA_ROPE_INTERLEAVED;
 
   // ---- this token's angles: slot j in [0, D/2) ----
   float* cs = &s_cs[warp][0][0];
@@ -273,7 +301,15 @@ append_warp_kernel(const __grid_constant__ AppendArgs a, int tpc) {
   }
   float wq[8], wk[8];
   const bool norm = a.q_w != nullptr;
-  if (norm) {
+  if (norm && inter && a.after_rope) {            // the norm sees the outputs' order
+    const float* qwp = a.q_w + (int64_t)n * a.w_stride;
+    const float* kwp = a.k_w + (int64_t)n * a.w_stride;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      wq[i] = qwp[e0 / 2 + i]; wq[4 + i] = qwp[HALF + e0 / 2 + i];
+      wk[i] = kwp[e0 / 2 + i]; wk[4 + i] = kwp[HALF + e0 / 2 + i];
+    }
+  } else if (norm) {
     load8(a.q_w + (int64_t)n * a.w_stride + e0, wq);
     load8(a.k_w + (int64_t)n * a.w_stride + e0, wk);
   }
@@ -281,7 +317,14 @@ append_warp_kernel(const __grid_constant__ AppendArgs a, int tpc) {
   // element e0 + i uses slot j0 + i; the rotate-half partner is d +- W/2 (W = D, or D/2 per
   // half in 2D), which the sign folded into sn[] accounts for
   float c[8], sn[8];
-  if (rotate) {
+  if (inter) {                                      // angles of the lane's pairs e0/2 .. e0/2 + 3
+    const float4 c0 = *reinterpret_cast<const float4*>(&cs[e0 / 2]);
+    const float4 s0 = *reinterpret_cast<const float4*>(&cs[HALF + e0 / 2]);
+    c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+    sn[0] = s0.x; sn[1] = s0.y; sn[2] = s0.z; sn[3] = s0.w;
+#pragma unroll
+    for (int i = 4; i < 8; ++i) c[i] = sn[i] = 0.f;
+  } else if (rotate) {
     const int blk = two_d ? e0 / HALF : 0;
     const int dd = e0 - blk * HALF;
     const int wh = two_d ? QUARTER : HALF;
@@ -333,7 +376,18 @@ append_warp_kernel(const __grid_constant__ AppendArgs a, int tpc) {
         }
       };
       if (!a.after_rope) apply_norm();
-      if (rotate) {
+      if (inter) {
+        if (qk) {
+          float y[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            y[i] = fmaf(-x[u][2 * i + 1], sn[i], x[u][2 * i] * c[i]);
+            y[4 + i] = fmaf(x[u][2 * i], sn[i], x[u][2 * i + 1] * c[i]);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[u][i] = y[i];
+        }
+      } else if (rotate) {
         float y[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -346,11 +400,20 @@ append_warp_kernel(const __grid_constant__ AppendArgs a, int tpc) {
         }
       }
       if (a.after_rope) apply_norm();
+      auto put = [&](auto* dst) {                     // q/k rows of interleaved RoPE: two halves
+        if (inter && qk) {
+          float lo[4] = {x[u][0], x[u][1], x[u][2], x[u][3]}, hi[4] = {x[u][4], x[u][5], x[u][6], x[u][7]};
+          store4(dst + e0 / 2, lo);
+          store4(dst + HALF + e0 / 2, hi);
+        } else {
+          store8(dst + e0, x[u]);
+        }
+      };
       if (kind[u] == 0) {
-        store8(reinterpret_cast<QOutT*>(a.q_out) + (tok * a.Hq + head[u]) * D + e0, x[u]);
+        put(reinterpret_cast<QOutT*>(a.q_out) + (tok * a.Hq + head[u]) * D);
       } else if ((kind[u] == 1 || kind[u] == 2) && slot >= 0 && slot < a.capacity) {
         CacheT* base = reinterpret_cast<CacheT*>(kind[u] == 1 ? a.kc : a.vc);
-        store8(base + (int64_t)n * a.inst_stride + ((int64_t)head[u] * a.capacity + slot) * D + e0, x[u]);
+        put(base + (int64_t)n * a.inst_stride + ((int64_t)head[u] * a.capacity + slot) * D);
       }
     }
   }
@@ -370,21 +433,6 @@ constexpr int STREAM_CONSUMERS = 16;                      // consumer warps
 constexpr int STREAM_THREADS = (STREAM_CONSUMERS + 1) * 32;
 constexpr int STREAM_ANGLES = 512;                        // tb * D/2 per item, at most
 constexpr int STREAM_STAGE_MAX = 64 * 1024;
-
-__device__ __forceinline__ void load4_smem(const float* p, float (&x)[4]) {
-  const float4 u = *reinterpret_cast<const float4*>(p);
-  x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
-}
-__device__ __forceinline__ void load4_smem(const bf16_t* p, float (&x)[4]) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
-}
-__device__ __forceinline__ void store4(float* p, const float (&y)[4]) {
-  *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
-}
-__device__ __forceinline__ void store4(bf16_t* p, const float (&y)[4]) {
-  *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
-}
 
 // Barrier over the consumer warps (named barrier 1) that also ANDs a predicate across them.
 __device__ __forceinline__ bool consumers_all(bool v) {
@@ -462,8 +510,10 @@ append_stream_kernel(const __grid_constant__ AppendArgs a, int tb, int stage_byt
   const int gpt = (n_rows + RPW - 1) / RPW;             // row groups per token
   const bool rotate = a.rope.kind != KVA_ROPE_NONE;
   const bool two_d = a.rope.kind == KVA_ROPE_2D;
+  const bool inter = a.rope.kind == KVA_ROPE_INTERLEAVED;   // q/k inputs in (x_2j, x_2j+1) pairs
   const bool norm = a.q_w != nullptr;
-  // this lane's chunks: o1 (low half of its rotated block) and o2 = o1 + W/2; angle slot j0
+  // this lane's chunks: o1 (low half of its rotated block) and o2 = o1 + W/2; angle slot j0.
+  // With interleaved RoPE the outputs o1.. and o2.. come from the input pairs at 2 * o1 ..
   int o1, j0;
   if (two_d) {
     const int per_blk = LPR / 2, blk = rl / per_blk, ll = rl % per_blk;
@@ -534,7 +584,12 @@ append_stream_kernel(const __grid_constant__ AppendArgs a, int tb, int stage_byt
         const InT* src = kind[u] == 0 ? sq + (tt * a.Hq + head[u]) * D
                        : kind[u] == 1 ? sk + (tt * a.Hkv + head[u]) * D
                        : kind[u] == 2 ? sv + (tt * a.Hkv + head[u]) * D : nullptr;
-        if (src) {
+        if (src && inter && kind[u] <= 1) {             // evens -> low output half, odds -> high
+          float t8[8];
+          load8_smem(src + 2 * o1, t8);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) { xl[u][i] = t8[2 * i]; xh[u][i] = t8[2 * i + 1]; }
+        } else if (src) {
           load4_smem(src + o1, xl[u]);
           load4_smem(src + o2, xh[u]);
         } else {
@@ -558,8 +613,15 @@ append_stream_kernel(const __grid_constant__ AppendArgs a, int tb, int stage_byt
             const float rinv = rsqrtf(ss * (1.0f / (float)D) + a.eps);
             const float* w = kind[u] == 0 ? swq : swk;
             float wl[4], wh[4];
-            load4_smem(w + o1, wl);
-            load4_smem(w + o2, wh);
+            if (inter && !a.after_rope) {               // before RoPE the weights follow the inputs
+              float w8[8];
+              load8_smem(w + 2 * o1, w8);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) { wl[i] = w8[2 * i]; wh[i] = w8[2 * i + 1]; }
+            } else {
+              load4_smem(w + o1, wl);
+              load4_smem(w + o2, wh);
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) { xl[u][i] *= rinv * wl[i]; xh[u][i] *= rinv * wh[i]; }
           }

@@ -69,7 +69,26 @@ __device__ __forceinline__ void step_row(float (&x)[4], const float (&w)[4], boo
 #pragma unroll
     for (int i = 0; i < 4; ++i) x[i] = x[i] * r * w[i];
   }
-  if (rotate) {
+  if (rotate && st.rope.kind == KVA_ROPE_INTERLEAVED) {
+    // inputs 4 lane .. 4 lane + 3 are the pairs j = 2 lane, 2 lane + 1; their rotated values
+    // belong at outputs j and 64 + j, so after rotating, lanes exchange values until lane m
+    // holds outputs 4m .. 4m + 3 again (low outputs from lanes 2m, 2m + 1 for m < 16, high
+    // outputs from lanes 2(m - 16), 2(m - 16) + 1 otherwise)
+    float lo[2], hi[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int j = 2 * lane + t;
+      lo[t] = x[2 * t] * s_cos[j] - x[2 * t + 1] * s_sin[j];
+      hi[t] = x[2 * t + 1] * s_cos[j] + x[2 * t] * s_sin[j];
+    }
+    const int src = lane < 16 ? 2 * lane : 2 * (lane - 16);
+    const float a0 = __shfl_sync(FULL_MASK, lo[0], src), a1 = __shfl_sync(FULL_MASK, lo[1], src);
+    const float b0 = __shfl_sync(FULL_MASK, lo[0], src + 1), b1 = __shfl_sync(FULL_MASK, lo[1], src + 1);
+    const float c0 = __shfl_sync(FULL_MASK, hi[0], src), c1 = __shfl_sync(FULL_MASK, hi[1], src);
+    const float d0 = __shfl_sync(FULL_MASK, hi[0], src + 1), d1 = __shfl_sync(FULL_MASK, hi[1], src + 1);
+    if (lane < 16) { x[0] = a0; x[1] = a1; x[2] = b0; x[3] = b1; }
+    else { x[0] = c0; x[1] = c1; x[2] = d0; x[3] = d1; }
+  } else if (rotate) {
     // partner of dim d: d +- 64 (lane ^ 16) for 1D / sections, d +- 32 inside a half (lane ^ 8) for 2D
     const bool two_d = st.rope.kind == KVA_ROPE_2D;
     float y[4];

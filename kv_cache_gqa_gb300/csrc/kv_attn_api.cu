@@ -68,6 +68,7 @@ kva_status build_rope(const kva_rope& r, int D, RopeTable* t) {
   if (D / 2 > MAX_ROPE_FREQ) return fail(KVA_EUNSUPPORTED, "head_dim %d too large for RoPE", D);
   switch (r.kind) {
     case KVA_ROPE_1D:
+    case KVA_ROPE_INTERLEAVED:
       if (r.n_axes < 1) return fail(KVA_EINVAL, "1D RoPE needs n_axes >= 1");
       for (int j = 0; j < D / 2; ++j) { t->inv[j] = std::pow(r.base, -2.0 * j / D); t->axis[j] = 0; }
       return KVA_OK;
@@ -238,6 +239,8 @@ kva_status kv_cache_append_rope_qknorm(
   if (norm.q_w && (!(norm.eps >= 0.f) || norm.inst_stride < 0))
     return fail(KVA_EINVAL, "QK-Norm eps must be >= 0 and inst_stride >= 0");
   if (!append_supports_head_dim(D)) return fail(KVA_EUNSUPPORTED, "append: head_dim %d not built", D);
+  if (rope.kind == KVA_ROPE_INTERLEAVED && D % 16 != 0)
+    return fail(KVA_EUNSUPPORTED, "append: interleaved RoPE needs head_dim %% 16 == 0 (got %d)", D);
   if (N > 65535) return fail(KVA_EUNSUPPORTED, "append: N=%d > 65535", N);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out))
     return fail(KVA_EALIGN, "q/k/v/q_out must be 16-byte aligned");

@@ -21,7 +21,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkv_attn
 KVA_OK, KVA_EINVAL, KVA_ECAPACITY, KVA_EUNSUPPORTED, KVA_ECUDA, KVA_EALIGN, KVA_EWORKSPACE = range(7)
 KVA_F32, KVA_BF16 = 0, 1
 MASKS = {"causal": 0, "full": 1, "segment": 2, "causal_segment": 3}
-ROPE_KINDS = {"none": 0, "1d": 1, "sections": 2, "2d": 3}
+ROPE_KINDS = {"none": 0, "1d": 1, "sections": 2, "2d": 3, "interleaved": 4}
 
 
 class KvaError(RuntimeError):
@@ -166,14 +166,14 @@ class KVCache:
 
 @dataclasses.dataclass
 class Rope:
-    """kind: 'none' | '1d' | 'sections' | '2d'; sections for 'sections' (sum D/2)."""
+    """kind: 'none' | '1d' | 'sections' | '2d' | 'interleaved'; sections for 'sections' (sum D/2)."""
     kind: str = "1d"
     base: float = 1e6
     sections: Sequence[int] = ()
 
     @property
     def n_axes(self) -> int:
-        return {"none": 0, "1d": 1, "2d": 2}.get(self.kind, len(self.sections))
+        return {"none": 0, "1d": 1, "2d": 2, "interleaved": 1}.get(self.kind, len(self.sections))
 
     @property
     def struct(self) -> _Rope:

@@ -78,6 +78,8 @@ def test_append_validation(K):
     assert append(K, cache=_cache(FAKE, d=80)) == K.KVA_EUNSUPPORTED         # D not built
     assert append(K, rope=_rope(kind=2, secs=(16, 16, 16, 8), n_axes=4)) == K.KVA_EINVAL  # sum != D/2
     assert append(K, rope=_rope(kind=3, n_axes=1)) == K.KVA_EINVAL
+    assert append(K, rope=_rope(kind=4), cache=_cache(FAKE, d=72)) == K.KVA_EUNSUPPORTED   # interleaved, D % 16
+    assert append(K, rope=_rope(kind=5)) == K.KVA_EINVAL
     assert append(K, rope=_rope(base=-1.0)) == K.KVA_EINVAL
     assert append(K, norm=_norm(q=FAKE)) == K.KVA_EINVAL                     # q weight without k weight
     assert append(K, cache=_cache(FAKE, stride=5), N=2, slot_host=[0, 0]) == K.KVA_EINVAL

@@ -34,6 +34,8 @@ STEP_CASES = [
     ("2d", (), None, "f32", 1, None, False),
     ("none", (), "before", "bf16", 4, None, False),
     ("1d", (), None, "bf16", 1, "bf16", False),
+    ("interleaved", (), "before", "f32", 2, "bf16", False),
+    ("interleaved", (), "after", "bf16", 4, "f32", True),
 ]
 
 
@@ -45,7 +47,7 @@ def test_decode_step_parity(K, kind, secs, norm, in_dt, G, qo_dt, shared):
     Hq = Hkv * G
     lengths = np.array([1, 2, 17, 64, 65, 300, 1000, 4097, 777], np.int32)
     B, W = lengths.size, 4200
-    n_axes = {"none": 1, "1d": 1, "sections": 4, "2d": 2}[kind]
+    n_axes = {"none": 1, "1d": 1, "sections": 4, "2d": 2, "interleaved": 1}[kind]
     base = 1.11588e7 if kind == "sections" else 1e6
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16}[in_dt]
     q = O.store(rng.standard_normal((B, Hq, D)) * 3, in_dt)

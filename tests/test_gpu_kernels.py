@@ -51,6 +51,9 @@ APPEND_CASES = [
     (72, "2d", (), None, "f32", "bf16", "bf16"),
     (64, "1d", (), "after", "bf16", "bf16", "f32"),
     (72, "1d", (), "before", "f32", "f32", "f32"),
+    (128, "interleaved", (), "before", "f32", "bf16", "bf16"),
+    (128, "interleaved", (), "after", "bf16", "f32", "f32"),
+    (64, "interleaved", (), None, "f32", "f32", "bf16"),
 ]
 
 
@@ -63,7 +66,7 @@ def test_append_parity(K, D, kind, secs, norm, in_dt, qo_dt, c_dt):
     q = rng.standard_normal((N, Tt, Hq, D)).astype(np.float32) * 3
     k = rng.standard_normal((N, Tt, Hkv, D)).astype(np.float32) * 3
     v = rng.standard_normal((N, Tt, Hkv, D)).astype(np.float32)
-    n_axes = {"none": 1, "1d": 1, "sections": 4, "2d": 2}[kind]
+    n_axes = {"none": 1, "1d": 1, "sections": 4, "2d": 2, "interleaved": 1}[kind]
     pos = rng.integers(0, 40000, size=(N, Tt, n_axes)).astype(np.int32)
     slot = np.stack([rng.permutation(W)[:Tt] for _ in range(N)]).astype(np.int32)
     qw = (1 + 0.1 * rng.standard_normal((N, D))).astype(np.float32)
@@ -110,6 +113,8 @@ STREAM_CASES = [
     (128, "2d", (), None, "bf16", "bf16", "bf16"),
     (64, "1d", (), "before", "f32", "bf16", "f32"),
     (256, "1d", (), "after", "f32", "bf16", "bf16"),
+    (128, "interleaved", (), "before", "f32", "bf16", "bf16"),
+    (64, "interleaved", (), "after", "f32", "f32", "f32"),
 ]
 
 
@@ -122,7 +127,7 @@ def test_append_stream_parity(K, D, kind, secs, norm, in_dt, qo_dt, c_dt):
     q = rng.standard_normal((N, Tt, Hq, D)).astype(np.float32) * 3
     k = rng.standard_normal((N, Tt, Hkv, D)).astype(np.float32) * 3
     v = rng.standard_normal((N, Tt, Hkv, D)).astype(np.float32)
-    n_axes = {"none": 1, "1d": 1, "sections": 4, "2d": 2}[kind]
+    n_axes = {"none": 1, "1d": 1, "sections": 4, "2d": 2, "interleaved": 1}[kind]
     pos = rng.integers(0, 40000, size=(N, Tt, n_axes)).astype(np.int32)
     slot = np.stack([rng.permutation(W)[:Tt] for _ in range(N)]).astype(np.int32)
     qw = (1 + 0.1 * rng.standard_normal((N, D))).astype(np.float32)
