@@ -39,8 +39,9 @@ namespace {
 
 constexpr int BM = 128;                   // query rows per slot = TMEM lanes
 constexpr int BN = 128;                   // keys per tile
-constexpr int TMA_WARP = 8, MMA_WARP = 9;
-constexpr int THREADS = 320;
+constexpr int SOFTMAX_WARPS = 16;         // per slot: 4 lane quarters x 2 column halves
+constexpr int TMA_WARP = 16, MMA_WARP = 17;
+constexpr int THREADS = 576;
 constexpr int SUB = BM * 128;             // bytes of one [128 rows x 64 bf16] swizzled box
 constexpr int NSTAGE = 2;
 constexpr uint32_t TMEM_COLS = 512;
@@ -184,7 +185,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kv_full[i], 1); mbar_init(&kv_free[i], 1); mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1); mbar_init(&q_full[i], gather ? 4 : 1);
+      mbar_init(&p_full[i], SOFTMAX_WARPS / 2); mbar_init(&pv_done[i], 1);
+      mbar_init(&q_full[i], gather ? SOFTMAX_WARPS / 2 : 1);
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -309,8 +311,15 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int s = warp >> 2;                     // slot
-    const int t = tid & 127;                     // row within the tile = TMEM lane
+    // warp w: slot s = w / 8, column half ch = (w / 4) % 2, TMEM lane quarter w % 4.  Thread
+    // (ch, t) owns columns [64 ch, 64 ch + 64) of row t; the two threads of a row trade their
+    // partial maxima (and at the end their partial sums) through shared memory.
+    const int s = warp >> 3;
+    const int ch = (warp >> 2) & 1;
+    const int t = (warp & 3) * 32 + lane;        // row within the tile = TMEM lane
+    __shared__ float s_pmax[2][2][2][BM];        // [tile parity][slot][half][row]
+    const int pair_bar = 1 + s * 4 + (warp & 3); // named barrier of warps w and w ^ 4 (64 threads)
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" :: "r"(pair_bar) : "memory"); };
     if (s == 0 || act1) {
       const int h = sl.h[s];
       const int i = sl.qt[s] * BM + t;
@@ -318,20 +327,19 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       int row = i;
       if (row_ok && a.row_of_slot) row = a.row_of_slot[i];
       const bool row_valid = row_ok && row >= 0 && row < a.S;
-      // permuted rows: stage the Q row: chunk c (8 bf16) -> box c/8, swizzled position (c%8) ^ (t%8)
+      // permuted rows: stage the Q row (this thread's half of the 16-byte chunks): chunk c
+      // (8 bf16) -> box c/8, swizzled position (c%8) ^ (t%8)
       uint8_t* sQ = sm + LY::Q_OFF + s * NSUB * SUB;
       if (gather) {
         const uint4* src = reinterpret_cast<const uint4*>(
             reinterpret_cast<const uint16_t*>(a.q) + (((int64_t)n * a.S + row) * a.Hq + h) * D);
 #pragma unroll
-        for (int c = 0; c < DK / 8; ++c) {
+        for (int c = ch; c < DK / 8; c += 2) {
           uint4 v = make_uint4(0, 0, 0, 0);
           if (row_valid && c < D / 8) v = __ldg(src + c);
           uint8_t* dst = sQ + (c >> 3) * SUB + (t >> 3) * 1024 + (t & 7) * 128 + (((c & 7) ^ (t & 7)) << 4);
           *reinterpret_cast<uint4*>(dst) = v;
         }
-      }
-      if (gather) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_full[s]);
@@ -348,52 +356,51 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
       const uint32_t s_col = s * BN, o_col = 256 + s * 128;
       const int nk = js1[s] - js0[s];
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f;             // l: this thread's half of the row sum
       bool ok = true;
       for (int k = 0; k < nk; ++k) {
-        const int kv0 = (js0[s] + k) * BN;
+        const int kv0 = (js0[s] + k) * BN + ch * 64;     // first key of this thread's columns
         // every lane waits; the vote keeps the warp converged for the .aligned TMEM accesses
         if (!__all_sync(FULL_MASK, mbar_wait_bounded(&s_full[s], (uint32_t)(k & 1)))) { ok = false; break; }
         tc::fence_after_sync();
-        // visible columns of this tile for this row: [clo, chi) (the whole tile unless it
-        // straddles the row's key range)
+        float x[64];
+        {
+          uint32_t r0[32], r1[32];
+          tc::tmem_ld32(lane_base + s_col + ch * 64, r0);
+          tc::tmem_ld32(lane_base + s_col + ch * 64 + 32, r1);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) { x[e] = __uint_as_float(r0[e]); x[32 + e] = __uint_as_float(r1[e]); }
+        }
+        // visible columns of this thread's 64 for this row: [clo, chi)
         const int clo = rlo - kv0, chi = rhi - kv0;
-        const bool straddle = clo > 0 || chi < BN;
-        // pass 1: the row max of this tile's visible raw scores (the scale is positive, so it
-        // commutes with the max)
+        if (clo > 0 || chi < 64) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e < clo || e >= chi) x[e] = -INFINITY;
+        }
         float mr = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(lane_base + s_col + c * 32, r);
-          tc::tmem_wait_ld();
-          if (straddle) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const int col = c * 32 + e;
-              const float v0 = (col >= clo && col < chi) ? __uint_as_float(r[e]) : -INFINITY;
-              const float v1 = (col + 1 >= clo && col + 1 < chi) ? __uint_as_float(r[e + 1]) : -INFINITY;
-              mr = fmax3(mr, v0, v1);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) mr = fmax3(mr, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-          }
-        }
+        for (int e = 0; e < 64; e += 2) mr = fmax3(mr, x[e], x[e + 1]);
+        // the row max over both halves (the barrier also means both threads hold their S, so
+        // P may now overwrite it: half 1's P columns [32, 64) hold half 0's scores)
+        s_pmax[k & 1][s][ch][t] = mr;
+        pair_sync();
+        mr = fmaxf(mr, s_pmax[k & 1][s][ch ^ 1][t]);
         const float m_tile = mr == -INFINITY ? -INFINITY : mr * a.scale_log2;
         const float m_new = fmaxf(m, m_tile);
         const bool first = (m == -INFINITY);            // first visible keys: O holds nothing yet
         const bool grow = !first && m_new > m + RESCALE_LOG2;
         if (first) m = m_new;
         if (__any_sync(FULL_MASK, grow)) {
-          // some row's max grew by > 2^8: rescale those rows of O once P V of the previous
-          // tile has landed.  The whole warp takes part (TMEM accesses are warp-collective);
-          // rows that need no rescale use alpha = 1.
+          // some row's max grew by > 2^8: rescale those rows of O (this thread's 16-column
+          // chunks of it) once P V of the previous tile has landed.  The whole warp takes part
+          // (TMEM accesses are warp-collective); rows that need no rescale use alpha = 1.
           if (!__all_sync(FULL_MASK, mbar_wait_bounded(&pv_done[s], (uint32_t)((k - 1) & 1)))) { ok = false; break; }
           tc::fence_after_sync();
           const float alpha = grow ? ex2(m - m_new) : 1.0f;
 #pragma unroll
-          for (int c = 0; c < DN / 16; ++c) {
+          for (int c = ch; c < DN / 16; c += 2) {
             uint32_t r[16];
             tmem_ld16(lane_base + o_col + c * 16, r);
             tc::tmem_wait_ld();
@@ -404,32 +411,22 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           tc::tmem_wait_st();
           if (grow) { l *= alpha; m = m_new; }
         }
-        // pass 2: P = exp2(S * scale - m) as packed bf16, written over the scores already read
-        // (chunk c of 32 keys lands in columns [16 c, 16 c + 16), below the next chunk's); the
-        // row sum accumulates the fp32 values in pairs
+        // P = exp2(S * scale - m) as packed bf16 into columns [32 ch, 32 ch + 32) of the slot
         const float mref = (m == -INFINITY) ? 0.f : m;
         const uint64_t sc2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
         uint64_t lsum = f2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(lane_base + s_col + c * 32, r);
-          tc::tmem_wait_ld();
+        for (int c = 0; c < 2; ++c) {
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float x0, x1;
-            f2split(ffma2(f2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), sc2, nm2), x0, x1);
-            float p0 = ex2(x0), p1 = ex2(x1);
-            if (straddle) {
-              const int col = c * 32 + 2 * e;
-              if (!(col >= clo && col < chi)) p0 = 0.f;
-              if (!(col + 1 >= clo && col + 1 < chi)) p1 = 0.f;
-            }
+            f2split(ffma2(f2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), sc2, nm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);         // hidden keys hold -inf: exp2 -> 0
             lsum = fadd2(lsum, f2(p0, p1));
             w[e] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(lane_base + s_col + c * 16, w);
+          tmem_st16(lane_base + s_col + ch * 32 + c * 16, w);
         }
         float l0, l1;
         f2split(lsum, l0, l1);
@@ -439,17 +436,22 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[s]);
       }
+      // the row sum over both halves
+      s_pmax[nk & 1][s][ch][t] = l;
+      pair_sync();
+      const float l_row = l + s_pmax[nk & 1][s][ch ^ 1][t];
       if (!gather) {
         // epilogue: once every MMA of the CTA is done, the rings and Q tiles are free: O / l goes
         // through shared memory (per 32-column box: 128 rows of 128 bytes, 128-byte swizzled)
-        // and out with TMA stores, which also clip rows past the sequence.
+        // and out with TMA stores, which also clip rows past the sequence.  Thread half ch
+        // stages boxes ch, ch + 2, ...
         constexpr int NBOX = (D + 31) / 32;
         if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(mma_done, 0));
         tc::fence_after_sync();
-        const float inv = (ok && l > 0.f) ? 1.0f / l : NAN;
+        const float inv = (ok && l_row > 0.f) ? 1.0f / l_row : NAN;
         uint8_t* stage = sm + s * NBOX * (BM * 128);
 #pragma unroll
-        for (int b = 0; b < NBOX; ++b) {
+        for (int b = ch; b < NBOX; b += 2) {
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             uint32_t r[16];
@@ -465,21 +467,22 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           }
         }
         fence_proxy_async_smem();
-        asm volatile("bar.sync %0, 128;" :: "r"(1 + s) : "memory");        // the slot's 4 warps
-        if (t == 0) {
+        asm volatile("bar.sync %0, 256;" :: "r"(9 + s) : "memory");        // the slot's 8 warps
+        if (ch == 0 && t == 0) {
           for (int b = 0; b < NBOX; ++b) tc::tma_store_4d(&tmO, stage + b * (BM * 128), b * 32, h, sl.qt[s] * BM, n);
           tc::bulk_commit_group();
           tc::bulk_wait_read_all();
         }
       } else {
-        // epilogue, permuted rows: O / l -> token-order output row from each thread.  The TMEM
-        // loads are warp-collective, so every lane loads; only rows inside the sequence store.
+        // epilogue, permuted rows: O / l -> token-order output row from each thread (its 16-column
+        // chunks).  The TMEM loads are warp-collective, so every lane loads; only rows inside the
+        // sequence store.
         if (ok && nk > 0) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&pv_done[s], (uint32_t)((nk - 1) & 1)));
         tc::fence_after_sync();
         float* o = a.out + (((int64_t)n * a.S + (row_valid ? row : 0)) * a.Hq + h) * D;
-        const float inv = (ok && l > 0.f) ? 1.0f / l : NAN;
+        const float inv = (ok && l_row > 0.f) ? 1.0f / l_row : NAN;
 #pragma unroll
-        for (int c = 0; c < DN / 16; ++c) {
+        for (int c = ch; c < DN / 16; c += 2) {
           uint32_t r[16];
           tmem_ld16(lane_base + o_col + c * 16, r);
           tc::tmem_wait_ld();
