@@ -296,6 +296,51 @@ def verify_bench(torch, K, stream):
             "block_tokens_per_s": round(B * k / (ms / 1e3), 1)}
 
 
+def serving_bench(torch, K, stream, W, lm_ws_bytes):
+    """The batched serving step: 64 sequences with contexts uniform in [1024, 32768] (the same
+    seeded draw as the parity tests), capacity ctx + 128; one step = the fused append + decode
+    over all 64 caches and the batched lm_head argmax.  Caches are random bf16 (contents do not
+    change the work).  Timed as a graph of 8 back-to-back steps at the first step's lengths."""
+    import workloads as WL
+    ctx = WL.serving_contexts(0)
+    B, cap = ctx.size, int(ctx.max()) + 128
+    g = torch.Generator(device="cuda"); g.manual_seed(11)
+    kc = torch.randn((B, HKV, cap, D), device="cuda", generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, HKV, cap, D), device="cuda", generator=g).to(torch.bfloat16)
+    q = torch.randn((B, HQ, D), device="cuda", generator=g)
+    k = torch.randn((B, HKV, D), device="cuda", generator=g)
+    v = torch.randn((B, HKV, D), device="cuda", generator=g)
+    h = torch.randn((B, HIDDEN), device="cuda", generator=g)
+    qw = 1 + 0.1 * torch.randn((D,), device="cuda", generator=g)
+    kw = 1 + 0.1 * torch.randn((D,), device="cuda", generator=g)
+    lengths = (ctx + 1).astype(np.int32)
+    ld = torch.from_numpy(lengths).cuda()
+    pos = torch.from_numpy(ctx.reshape(B, 1).astype(np.int32)).cuda()
+    out = torch.empty((B, HQ, D), device="cuda")
+    ids = torch.empty((B,), dtype=torch.int32, device="cuda")
+    dws = torch.zeros(K.decode_workspace_bytes(B, HKV, HQ, cap, D), dtype=torch.uint8, device="cuda")
+    lws = torch.zeros(K.lmhead_workspace_bytes(B, HIDDEN), dtype=torch.uint8, device="cuda")
+    cache, rope = K.KVCache(kc, vc), K.Rope("1d", 1e6)
+    dec = lambda: K.kv_attn_decode_step(q, k, v, pos, cache, ld, lengths, out, dws, rope, q_norm_w=qw, k_norm_w=kw)
+    lmh = lambda: K.lmhead_argmax(h, W, ids, lws)
+    with torch.cuda.stream(stream):
+        dec(); lmh()                                   # configure the kernels before capture
+    torch.cuda.synchronize()
+    dec_ms = graph_avg_ms(torch, stream, dec, 8, reps=2)
+    lm_ms = graph_avg_ms(torch, stream, lmh, 8, reps=2)
+    step_ms = graph_avg_ms(torch, stream, lambda: (dec(), lmh()), 8, reps=2)
+    kv_bytes = int(lengths.sum()) * HKV * D * 2 * 2
+    dec_bytes = kv_bytes + B * ((HQ + 2 * HKV) * D * 4 + 2 * HKV * D * 2 + HQ * D * 4)
+    del kc, vc
+    return {"config": f"{B} sequences, contexts {int(ctx.min())}..{int(ctx.max())} (sum {int(ctx.sum())}), "
+                      f"{HQ}/{HKV} heads, D={D}, bf16 caches; step = fused append+decode + lm_head (B={B})",
+            "step_us": round(step_ms * 1e3, 1), "tokens_per_s": round(B / (step_ms / 1e3), 1),
+            "decode_step_us": round(dec_ms * 1e3, 1), "decode_GB/s": round(dec_bytes / (dec_ms / 1e3) / 1e9, 1),
+            "decode_algorithmic_bytes": dec_bytes,
+            "lm_head_us": round(lm_ms * 1e3, 1),
+            "lm_head_GB/s": round((VOCAB * HIDDEN * 2) / (lm_ms / 1e3) / 1e9, 1)}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import kv_cache_gqa_gb300 as K
@@ -378,6 +423,7 @@ def run_gpu(args, rank, world, local_rank):
     # speculative-decoding verify block on a cache larger than L2: 64 sequences x 2048 slots,
     # 16-token blocks (each launch streams 537 MB of K/V once for all 16 block rows)
     vb = verify_bench(torch, K, stream)
+    sv = serving_bench(torch, K, stream, job.W, None)
 
     # ---- end to end: inputs from pinned host memory, ids back to the host, every step ----
     host_in = {n: getattr(job, n).cpu().pin_memory() for n in ("q", "k", "v", "dq", "dk", "dv", "h")}
@@ -459,6 +505,8 @@ def run_gpu(args, rank, world, local_rank):
                 "lm_head": {"GB/s": round(lm_gbs, 1), "frac_hbm": round(lm_gbs / hbm, 4),
                             "avg_launch_us": round(lm_iso_ms * 1e3, 2)},
                 "verify_block": dict(vb, frac_hbm=round(vb["GB/s"] / hbm, 4)),
+                "batched_serving": dict(sv, decode_frac_hbm=round(sv["decode_GB/s"] / hbm, 4),
+                                        lm_head_frac_hbm=round(sv["lm_head_GB/s"] / hbm, 4)),
                 "lm_head_final_norm_top1_us": round(lm_norm_ms * 1e3, 2),
                 "lm_head_final_norm_top8_us": round(lm_top8_ms * 1e3, 2),
                 "time_share": {k: round(v / sum(totals.values()), 4) for k, v in totals.items()},
