@@ -101,11 +101,17 @@ class Rope:
                      transpose), then rotated like '1d'; the result stays in that order
                      (rope_interleave: Youtu-VL-4B port, implementation difficulty 2).
     kind 'none':     no rotation.
+
+    rot_offset / rot_dim: the rotation acts on dims [rot_offset, rot_offset + rot_dim) only
+    (its frequencies follow that width) and leaves the rest of the head as it is, the layout of
+    an MLA head whose last 64 of 192 dims carry the position (Youtu-VL-4B port: K = 192 with a
+    64x64 rotary permutation, implementation difficulty 2; V = 128).  rot_dim None = the head.
     """
 
-    def __init__(self, kind: str, base: float = 1e6, sections=None):
+    def __init__(self, kind: str, base: float = 1e6, sections=None, rot_offset: int = 0, rot_dim=None):
         self.kind, self.base = kind, float(base)
         self.sections = tuple(sections) if sections is not None else None
+        self.rot_offset, self.rot_dim = int(rot_offset), rot_dim
 
 
 def inv_freq(base: float, width: int) -> np.ndarray:
@@ -131,6 +137,11 @@ def rope_apply(x, pos, rope: Rope) -> np.ndarray:
     x = np.asarray(x, dtype=F64)
     if rope.kind == "none":
         return x.copy()
+    if rope.rot_dim is not None and (rope.rot_offset != 0 or rope.rot_dim != x.shape[-1]):
+        o, w = rope.rot_offset, rope.rot_dim
+        out = x.copy()
+        out[..., o:o + w] = rope_apply(x[..., o:o + w], pos, Rope(rope.kind, rope.base, rope.sections))
+        return out
     pos = np.asarray(pos, dtype=F64)
     D = x.shape[-1]
     if rope.kind in ("1d", "sections"):

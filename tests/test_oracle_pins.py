@@ -587,3 +587,100 @@ def test_rope_interleaved_pairs_position_zero_and_relative_property():
     d1 = np.dot(O.rope_apply(q, np.array([[50]]), rope)[0, 0], O.rope_apply(k, np.array([[20]]), rope)[0, 0])
     d2 = np.dot(O.rope_apply(q, np.array([[1030]]), rope)[0, 0], O.rope_apply(k, np.array([[1000]]), rope)[0, 0])
     assert abs(d1 - d2) < 1e-10
+
+
+# ----------------------------------------------------------------------------
+# asymmetric MLA-expanded cache: K = 192 (the last 64 dims rotated, interleaved), V = 128
+# (Youtu-VL-4B port, section 6 and implementation difficulty 2)
+# ----------------------------------------------------------------------------
+def _mla_rope():
+    return O.Rope("interleaved", 1e6, rot_offset=128, rot_dim=64)
+
+
+def test_rope_subrange_leaves_the_rest_and_matches_the_block_matrix():
+    """The rotation acts on dims 128..191 only, with frequencies of a 64-wide head: the whole
+    192-wide step is the block matrix diag(I_128, page form on 64) with P and PR = P @ R the
+    64x64 permutation and +-1 matrices."""
+    rng = np.random.default_rng(21)
+    T, Dk, w = 7, 192, 64
+    P = np.zeros((w, w))
+    R = np.zeros((w, w))
+    for j in range(w // 2):
+        P[2 * j, j] = 1.0
+        P[2 * j + 1, w // 2 + j] = 1.0
+        R[w // 2 + j, j] = -1.0
+        R[j, w // 2 + j] = 1.0
+    x = rng.standard_normal((T, 1, Dk))
+    pos = rng.integers(0, 5000, size=(T, 1))
+    got = O.rope_apply(x, pos, _mla_rope())[:, 0]
+    np.testing.assert_array_equal(got[:, :128], x[:, 0, :128])
+    j = np.arange(w // 2)
+    inv = 1e6 ** (-2.0 * j / w)                       # a 64-wide head, not a 192-wide one
+    ang = np.concatenate([pos * inv[None, :], pos * inv[None, :]], axis=1)
+    xr = x[:, 0, 128:]
+    ref = (xr @ P) * np.cos(ang) + (xr @ (P @ R)) * np.sin(ang)
+    np.testing.assert_allclose(got[:, 128:], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_rope_subrange_relative_property_over_the_whole_head():
+    """q.k over all 192 dims depends on the positions only through their difference, and a
+    zero-width shift of both leaves the score unchanged."""
+    rng = np.random.default_rng(22)
+    rope = _mla_rope()
+    q, k = rng.standard_normal((1, 1, 192)), rng.standard_normal((1, 1, 192))
+    s = [np.dot(O.rope_apply(q, np.array([[m]]), rope)[0, 0], O.rope_apply(k, np.array([[n]]), rope)[0, 0])
+         for m, n in ((70, 3), (1067, 1000), (40067, 40000))]
+    assert abs(s[0] - s[1]) < 1e-10 and abs(s[0] - s[2]) < 1e-9
+    nope = np.dot(q[0, 0, :128], k[0, 0, :128])
+    same = np.dot(O.rope_apply(q, np.array([[9]]), rope)[0, 0], O.rope_apply(k, np.array([[9]]), rope)[0, 0])
+    np.testing.assert_allclose(same, np.dot(q[0, 0], k[0, 0]), rtol=1e-12)
+    assert abs(nope - np.dot(q[0, 0, :128], k[0, 0, :128])) == 0.0
+
+
+def test_asymmetric_attention_two_keys_scale_follows_the_key_width():
+    """Two keys whose logits differ by d: the output is sigmoid(d / sqrt(192)) V0 + (1 - ...) V1,
+    with V 128 wide; the default scale uses the key width (192), not the value width."""
+    rng = np.random.default_rng(23)
+    q = rng.standard_normal((1, 1, 192))
+    K = rng.standard_normal((1, 2, 192))
+    V = rng.standard_normal((1, 2, 128))
+    d = float(q[0, 0] @ (K[0, 0] - K[0, 1]))
+    p0 = 1.0 / (1.0 + math.exp(-d / math.sqrt(192)))
+    got = O.attend(q, K, V, np.ones((1, 2), bool))[0, 0]
+    assert got.shape == (128,)
+    np.testing.assert_allclose(got, p0 * V[0, 0] + (1 - p0) * V[0, 1], rtol=1e-13, atol=1e-14)
+
+
+def test_asymmetric_attention_value_columns_are_independent():
+    """Splitting V [.., 128] into two 64-wide halves and attending with each gives the two halves
+    of the full result (the softmax weights see only K); the same for the decode and prefill forms."""
+    rng = np.random.default_rng(24)
+    H, W, S = 3, 40, 40
+    q = rng.standard_normal((S, H, 192))
+    K = rng.standard_normal((H, W, 192))
+    V = rng.standard_normal((H, W, 128))
+    full = O.prefill(q, K, V, S, "causal")
+    a = O.prefill(q, K, V[..., :64], S, "causal")
+    b = O.prefill(q, K, V[..., 64:], S, "causal")
+    np.testing.assert_allclose(full, np.concatenate([a, b], axis=-1), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(O.decode(q[S - 1], K, V, S), full[S - 1], rtol=1e-12, atol=1e-14)
+
+
+def test_cache_append_asymmetric_shapes():
+    """An append into K [H, W, 192] / V [H, W, 128] without QK-Norm: K gets the sub-range rotation
+    and bf16 rounding, V is stored unchanged, other slots stay untouched."""
+    rng = np.random.default_rng(25)
+    H, W, T = 4, 16, 3
+    q = rng.standard_normal((T, H, 192))
+    k = rng.standard_normal((T, H, 192))
+    v = rng.standard_normal((T, H, 128))
+    pos = np.array([[5], [6], [11]])
+    slot = np.array([2, 3, 9])
+    ck, cv = np.full((H, W, 192), 7.0), np.full((H, W, 128), 7.0)
+    qr = O.cache_append(q, k, v, pos, slot, None, None, 1e-6, _mla_rope(), False, ck, cv, "bf16")
+    np.testing.assert_array_equal(qr[..., :128], q[..., :128])
+    for t in range(T):
+        np.testing.assert_array_equal(ck[:, slot[t], :128], O.bf16_round(k[t, :, :128]))
+        np.testing.assert_array_equal(cv[:, slot[t]], O.bf16_round(v[t]))
+    rest = np.setdiff1d(np.arange(W), slot)
+    assert np.all(ck[:, rest] == 7.0) and np.all(cv[:, rest] == 7.0)
