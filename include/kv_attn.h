@@ -25,6 +25,9 @@
  *    Token-major activations: q [.., T, Hq, D], k/v [.., T, Hkv, D], as a projection
  *    emits them.  Cache instance: K [Hkv, capacity, D], V [Hkv, capacity, D]
  *    (fixed-window cache of static shape: Youtu-VL-4B ncnn port, step 7).
+ *  - Asymmetric caches: K rows of Dk = head_dim and V rows of Dv = head_dim_v elements (an
+ *    MLA layer expanded to per-head K = 192, V = 128: Youtu-VL-4B ncnn port, section 6).
+ *    Then q, k and q_out rows are Dk wide, v rows and attention outputs Dv wide.
  *  - GQA: query head h reads KV head h / (Hq / Hkv) (repeat-interleave grouping:
  *    Penguin-VL ncnn port, section 3 item 2).
  *  - Alignment: every device pointer must be 16-byte aligned, and D must be a
@@ -73,9 +76,12 @@ typedef enum {
                                Youtu-VL-4B ncnn port, implementation difficulty 2) */
 } kva_rope_kind;
 
-/* One cache: N instances (layers and/or sequences) of K and V, each
- * [n_kv_heads, capacity, head_dim] of `dtype`, instance i starting at
- * k + i * inst_stride elements (same for v).  inst_stride >= n_kv_heads*capacity*head_dim. */
+/* One cache: N instances (layers and/or sequences) of K [n_kv_heads, capacity, head_dim] and
+ * V [n_kv_heads, capacity, head_dim_v] of `dtype`, K instance i starting at
+ * k + i * inst_stride elements and V instance i at v + i * inst_stride_v elements.
+ * inst_stride >= n_kv_heads*capacity*head_dim, inst_stride_v >= n_kv_heads*capacity*head_dim_v.
+ * head_dim_v = 0 means head_dim and inst_stride_v = 0 means inst_stride (a symmetric cache,
+ * where the two strides must agree). */
 typedef struct {
   void* k;
   void* v;
@@ -84,6 +90,8 @@ typedef struct {
   int32_t head_dim;
   int32_t capacity;
   int64_t inst_stride;
+  int32_t head_dim_v;
+  int64_t inst_stride_v;
 } kva_cache;
 
 /* Rotary embedding (rotate-half pairs (j, j + W/2) inside each rotated block of width W):
@@ -92,12 +100,18 @@ typedef struct {
  *  1D (theta 1e6: Penguin-VL ncnn port, section 2.1), xdRoPE sections [16,16,16,16]
  *  with effective base 1.11588e7 (HunyuanOCR v1.0 ncnn port, section five items 1, 3),
  *  2D vision halves (Penguin-VL ncnn port, section 2.3).
- *  n_axes: position ids per token (1 for 1D, number of sections, 2 for 2D). */
+ *  n_axes: position ids per token (1 for 1D, number of sections, 2 for 2D).
+ *  rot_offset, rot_dim: the rotation covers head dims [rot_offset, rot_offset + rot_dim) and
+ *  W above is rot_dim; the other dims pass through (the rotary 64 of a 192-wide MLA head:
+ *  Youtu-VL-4B ncnn port, implementation difficulty 2).  rot_dim = 0: the whole head
+ *  (rot_offset must then be 0). */
 typedef struct {
   kva_rope_kind kind;
   int32_t n_axes;
   int32_t sections[4];
   double base;
+  int32_t rot_offset;
+  int32_t rot_dim;
 } kva_rope;
 
 /* Per-head RMSNorm y = x / sqrt(mean(x^2) + eps) * w with w [D] float32 on the device
@@ -128,8 +142,10 @@ typedef struct {
  *  slot_host  host mirror of the slot values actually read (same strides), used to reject
  *          slots outside [0, capacity) with KVA_ECAPACITY before launching
  *  q_out   [N,T,Hq,D] of q_out_dtype (device), token order
- *  Errors: KVA_EINVAL (N,T < 0, Hq % Hkv, sections not summing to D/2, D/2 odd for 2D),
- *          KVA_ECAPACITY, KVA_EALIGN, KVA_EUNSUPPORTED (D > 256), KVA_ECUDA.
+ *  Asymmetric caches take q, k [.., Dk] and v [.., Dv]; QK-Norm weights are Dk wide.
+ *  Errors: KVA_EINVAL (N,T < 0, Hq % Hkv, sections not summing to W/2, W/2 odd for 2D, a
+ *          rotary range outside the head), KVA_ECAPACITY, KVA_EALIGN,
+ *          KVA_EUNSUPPORTED (Dk or Dv > 256), KVA_ECUDA.
  *  N == 0 or T == 0 is a no-op returning KVA_OK. */
 kva_status kv_cache_append_rope_qknorm(
     const void* q, const void* k, const void* v, kva_dtype in_dtype,
@@ -154,8 +170,8 @@ kva_status kv_cache_append_rope_qknorm(
  *  segment [S] int32 (device), non-decreasing segment id per slot, for KVA_MASK_SEGMENT
  *          and KVA_MASK_CAUSAL_SEGMENT (else NULL); segment_host: its host mirror
  *          (validated: non-decreasing).
- *  scale   softmax scale; <= 0 selects 1/sqrt(D).
- *  out     [N,S,Hq,D] float32 (device).
+ *  scale   softmax scale; <= 0 selects 1/sqrt(Dk).
+ *  out     [N,S,Hq,Dv] float32 (device).
  *  Errors: KVA_EINVAL, KVA_ECAPACITY (S > capacity), KVA_EALIGN, KVA_EUNSUPPORTED
  *          (D > 256), KVA_ECUDA.  q_dtype must equal cache.dtype. */
 kva_status kv_attn_prefill(
@@ -180,8 +196,10 @@ kva_status kv_attn_prefill(
  *             first kva_decode_workspace_zero_bytes(B, Hkv) bytes are zero before the first
  *             call; every call leaves them zero again.  Calls sharing one workspace must
  *             not overlap on the GPU.
+ *  Built for (Dk, Dv) = (128, 128) and the asymmetric (192, 128); q is [B,Hq,Dk], out
+ *  [B,Hq,Dv]; kva_decode_workspace_size takes Dv as its head_dim.
  *  Errors: KVA_EINVAL, KVA_ECAPACITY, KVA_EALIGN, KVA_EWORKSPACE,
- *          KVA_EUNSUPPORTED (D != 128), KVA_ECUDA.  B == 0 is a no-op. */
+ *          KVA_EUNSUPPORTED (other head dims), KVA_ECUDA.  B == 0 is a no-op. */
 kva_status kv_attn_decode(
     const void* q, kva_dtype q_dtype, kva_cache cache,
     const int32_t* lengths, const int32_t* lengths_host, int32_t B, int32_t n_q_heads,
@@ -202,8 +220,9 @@ kva_status kv_attn_decode(
  *  lengths  [B] valid slots including the new token (device) + lengths_host (host mirror)
  *  q_out    nullable [B,Hq,D] of q_out_dtype: the transformed queries, if wanted
  *  out      [B,Hq,D] float32;  workspace as for kv_attn_decode
- *  Requires a bf16 cache with head_dim 128 and Hq/Hkv in {1, 2, 4} (else KVA_EUNSUPPORTED:
- *  call the two entry points).  Errors as the two calls it replaces. */
+ *  Requires a symmetric bf16 cache with head_dim 128, RoPE over the whole head and Hq/Hkv in
+ *  {1, 2, 4} (else KVA_EUNSUPPORTED: call the two entry points).  Errors as the two calls it
+ *  replaces. */
 kva_status kv_attn_decode_step(
     const void* q, const void* k, const void* v, kva_dtype in_dtype,
     const int32_t* pos, int64_t pos_inst_stride,
@@ -223,7 +242,7 @@ kva_status kv_attn_decode_step(
  *           upper bound of it (used for validation and work planning; L >= k required)
  *  out      [B,k,Hq,D] float32
  *  workspace as for kv_attn_decode, sized by kva_verify_workspace_size; merge counters are
- *  left at zero.  Requires a bf16 cache with head_dim 128 (else KVA_EUNSUPPORTED) and
+ *  left at zero.  Requires a symmetric bf16 cache with head_dim 128 (else KVA_EUNSUPPORTED) and
  *  1 <= k <= KVA_VERIFY_MAX_BLOCK. */
 #define KVA_VERIFY_MAX_BLOCK 64
 kva_status kv_attn_verify(
@@ -258,7 +277,7 @@ size_t kva_decode_workspace_zero_bytes(int32_t B, int32_t n_kv_heads);
  *   fixed 4 MiB array inside this library's device image; every GPU that loads the
  *   library holds it until the process exits.  The reference pages have no counterpart
  *   of this call.
- *  Arguments and errors: as kv_attn_decode.  A batch whose partials cannot fit the fixed
+ *  Arguments and errors: as kv_attn_decode, for symmetric caches.  A batch whose partials cannot fit the fixed
  *   scratch even as one chunk per instance (B * n_q_heads * (head_dim + 2) * 4 bytes plus
  *   the counters above 4 MiB) returns KVA_EWORKSPACE; otherwise larger chunks are chosen
  *   until the partials fit.

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkv_attn.so")
-SOURCES = ["kv_attn_api.cu", "append.cu", "decode.cu", "decode_mma.cu", "decode_static.cu", "lmhead.cu", "lmhead_tc.cu", "lmhead_topk.cu",
+SOURCES = ["kv_attn_api.cu", "append.cu", "append_general.cu", "decode.cu", "decode_mma.cu", "decode_static.cu", "lmhead.cu", "lmhead_tc.cu", "lmhead_topk.cu",
            "prefill_simt.cu", "prefill_tc.cu", "verify_mma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

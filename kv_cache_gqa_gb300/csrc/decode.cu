@@ -8,7 +8,9 @@
 // byte is read from HBM once per step.  Scores stay in fp32 (log2 domain) with an
 // online softmax across stages; the partial (max, sum, acc) of every chunk goes to the
 // workspace and the last CTA to finish a (b, g) merges them - no CTA ever waits on
-// another.
+// another.  The K rows may be wider than the V rows: an asymmetric cache with Dk = 192,
+// Dv = 128 (an MLA layer expanded to per-head K and V, Youtu-VL-4B ncnn port, section 6)
+// takes the same kernel with wider K tiles.
 //
 // Method: one query against the valid prefix of the cache window (Youtu-VL-4B ncnn port,
 // step 8: each new token attends to the whole cache behind the mask), GQA by
@@ -24,7 +26,7 @@ namespace kva {
 
 namespace {
 
-constexpr int D = DECODE_HEAD_DIM;
+constexpr int D = DECODE_HEAD_DIM;    // V row width (and the output's)
 constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
 constexpr int NSTAGE = 3;
@@ -50,23 +52,27 @@ template <> __device__ __forceinline__ void chunk_to_f32<float, 4>(uint4 w, floa
   x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
 }
 
-template <typename CacheT, int G>
-__global__ void __launch_bounds__(THREADS, 2)
+template <typename CacheT, int G, int DK>
+__global__ void __launch_bounds__(THREADS, DK > D ? 1 : 2)   // wide K tiles: one CTA per SM by smem
 decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
   constexpr int ES = ElemSize<CacheT>::value;
   constexpr int KT = DecodeTile<CacheT>::KT;   // keys per stage
-  constexpr int ROWB = D * ES;                 // bytes per cache row
-  constexpr int TILEB = KT * ROWB;             // bytes per K (or V) stage
+  constexpr int ROWK = DK * ES;                // bytes per K row
+  constexpr int ROWB = D * ES;                 // bytes per V row
+  constexpr int TILEK = KT * ROWK;             // bytes per K stage
+  constexpr int TILEB = KT * ROWB;             // bytes per V stage
   constexpr int CH = 16 / ES;                  // elements per 16-byte chunk
-  constexpr int NCH = 16 / CH;                 // chunks per lane in the QK phase (16 dims)
+  constexpr int QPL = DK / 8;                  // query dims per lane in the QK phase
+  constexpr int NCH = QPL / CH;                // 16-byte chunks per lane in the QK phase
+  static_assert(DK % (8 * CH) == 0, "K rows split into whole 16-byte chunks over 8 lanes");
   constexpr int KPW = KT / WARPS;              // keys per warp per stage
   constexpr int QK_PASSES = KPW / 4;           // 4 keys per warp pass (8 lanes per key)
   constexpr int SPL = KT / 32;                 // scores per lane in the softmax phase
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* sK = smem;
-  unsigned char* sV = smem + NSTAGE * TILEB;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * NSTAGE * TILEB);  // [NSTAGE]
+  unsigned char* sV = smem + NSTAGE * TILEK;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSTAGE * (TILEK + TILEB));  // [NSTAGE]
   float* sS = reinterpret_cast<float*>(full + NSTAGE);               // [G][KT]
   float* sP = sS + G * KT;                                           // [KT][G]
   float* sAlpha = sP + KT * G;                                       // [G]
@@ -83,9 +89,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
   const int n_sub = (k1 - k0 + KT - 1) / KT;
 
   const unsigned char* Kg = reinterpret_cast<const unsigned char*>(a.kc) +
-      ((int64_t)b * a.inst_stride + (int64_t)g * a.capacity * D) * ES;
+      ((int64_t)b * a.inst_stride + (int64_t)g * a.capacity * DK) * ES;
   const unsigned char* Vg = reinterpret_cast<const unsigned char*>(a.vc) +
-      ((int64_t)b * a.inst_stride + (int64_t)g * a.capacity * D) * ES;
+      ((int64_t)b * a.inst_stride_v + (int64_t)g * a.capacity * D) * ES;
 
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(&full[s], 1);
@@ -96,20 +102,20 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
   if (tid == 0) {
     for (int s = 0; s < NSTAGE && s < n_sub; ++s) {
       const int ks = k0 + s * KT;
-      const uint32_t bytes = (uint32_t)(min(KT, k1 - ks) * ROWB);
-      mbar_arrive_expect_tx(&full[s], 2 * bytes);
-      bulk_g2s(sK + s * TILEB, Kg + (int64_t)ks * ROWB, bytes, &full[s]);
-      bulk_g2s(sV + s * TILEB, Vg + (int64_t)ks * ROWB, bytes, &full[s]);
+      const int nr = min(KT, k1 - ks);
+      mbar_arrive_expect_tx(&full[s], (uint32_t)(nr * (ROWK + ROWB)));
+      bulk_g2s(sK + s * TILEK, Kg + (int64_t)ks * ROWK, (uint32_t)(nr * ROWK), &full[s]);
+      bulk_g2s(sV + s * TILEB, Vg + (int64_t)ks * ROWB, (uint32_t)(nr * ROWB), &full[s]);
     }
   }
 
-  // Query registers for the QK phase: lane owns 16 dims, NCH chunks of CH elements at
+  // Query registers for the QK phase: lane owns DK/8 dims, NCH chunks of CH elements at
   // element offsets CH*(lane&7) + 8*CH*i.  Pre-scaled so dots are log2-domain logits.
   const int l8 = lane & 7;
-  float qv[G][16];
+  float qv[G][QPL];
 #pragma unroll
   for (int hh = 0; hh < G; ++hh) {
-    const int64_t qbase = ((int64_t)b * a.Hq + g * G + hh) * D;
+    const int64_t qbase = ((int64_t)b * a.Hq + g * G + hh) * DK;
 #pragma unroll
     for (int i = 0; i < NCH; ++i)
 #pragma unroll
@@ -132,7 +138,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
     __syncthreads();
     if (s_flag) { timed_out = true; break; }
     const int nk = min(KT, k1 - (k0 + it * KT));
-    const unsigned char* tK = sK + stage * TILEB;
+    const unsigned char* tK = sK + stage * TILEK;
     const unsigned char* tV = sV + stage * TILEB;
 
     // ---- S = q K^T (8 lanes per key, 4 keys per warp pass) ----
@@ -145,7 +151,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
       if (j < nk) {
 #pragma unroll
         for (int i = 0; i < NCH; ++i) {
-          const uint4 w = *reinterpret_cast<const uint4*>(tK + j * ROWB + 16 * l8 + 128 * i);
+          const uint4 w = *reinterpret_cast<const uint4*>(tK + j * ROWK + 16 * l8 + 128 * i);
           float x[CH];
           chunk_to_f32<CacheT, CH>(w, x);
 #pragma unroll
@@ -218,10 +224,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
 
     if (tid == 0 && it + NSTAGE < n_sub) {
       const int ks = k0 + (it + NSTAGE) * KT;
-      const uint32_t bytes = (uint32_t)(min(KT, k1 - ks) * ROWB);
-      mbar_arrive_expect_tx(&full[stage], 2 * bytes);
-      bulk_g2s(sK + stage * TILEB, Kg + (int64_t)ks * ROWB, bytes, &full[stage]);
-      bulk_g2s(sV + stage * TILEB, Vg + (int64_t)ks * ROWB, bytes, &full[stage]);
+      const int nr = min(KT, k1 - ks);
+      mbar_arrive_expect_tx(&full[stage], (uint32_t)(nr * (ROWK + ROWB)));
+      bulk_g2s(sK + stage * TILEK, Kg + (int64_t)ks * ROWK, (uint32_t)(nr * ROWK), &full[stage]);
+      bulk_g2s(sV + stage * TILEB, Vg + (int64_t)ks * ROWB, (uint32_t)(nr * ROWB), &full[stage]);
     }
   }
 
@@ -286,35 +292,35 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
   if (tid == 0) a.counters[b * a.Hkv + g] = 0u;   // ready for the next call
 }
 
-template <typename CacheT, int G>
+template <typename CacheT, int G, int DK>
 size_t decode_smem_bytes() {
   constexpr int ES = ElemSize<CacheT>::value;
   constexpr int KT = DecodeTile<CacheT>::KT;
-  return (size_t)2 * NSTAGE * KT * D * ES + sizeof(uint64_t) * NSTAGE +
+  return (size_t)NSTAGE * KT * (DK + D) * ES + sizeof(uint64_t) * NSTAGE +
          sizeof(float) * (2 * G * KT + 3 * G) + 16;
 }
 
-template <typename CacheT, int G>
+template <typename CacheT, int G, int DK>
 cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
-  const size_t smem = decode_smem_bytes<CacheT, G>();
+  const size_t smem = decode_smem_bytes<CacheT, G, DK>();
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<CacheT, G>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<CacheT, G, DK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   dim3 grid(a.max_chunks, a.Hkv, a.B);
-  decode_kernel<CacheT, G><<<grid, THREADS, smem, s>>>(a, q_dtype);
+  decode_kernel<CacheT, G, DK><<<grid, THREADS, smem, s>>>(a, q_dtype);
   return cudaGetLastError();
 }
 
-template <typename CacheT>
+template <typename CacheT, int DK>
 cudaError_t launch_t(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
   switch (a.Hq / a.Hkv) {
-    case 1: return launch_g<CacheT, 1>(a, q_dtype, s);
-    case 2: return launch_g<CacheT, 2>(a, q_dtype, s);
-    case 4: return launch_g<CacheT, 4>(a, q_dtype, s);
+    case 1: return launch_g<CacheT, 1, DK>(a, q_dtype, s);
+    case 2: return launch_g<CacheT, 2, DK>(a, q_dtype, s);
+    case 4: return launch_g<CacheT, 4, DK>(a, q_dtype, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -343,8 +349,17 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, kva_dtype q_dtype, cudaStream
 cudaError_t launch_decode(const DecodeArgs& a, kva_dtype q_dtype, kva_dtype cache_dtype,
                           cudaStream_t s) {
   if (cache_dtype == KVA_BF16 && decode_mma_supported()) return launch_decode_mma(a, q_dtype, s);
-  if (cache_dtype == KVA_BF16) return launch_t<bf16_t>(a, q_dtype, s);
-  return launch_t<float>(a, q_dtype, s);
+  if (cache_dtype == KVA_BF16) return launch_t<bf16_t, D>(a, q_dtype, s);
+  return launch_t<float, D>(a, q_dtype, s);
+}
+
+bool decode_asym_supported(int Dk, int Dv) { return Dk == 192 && Dv == D; }
+
+cudaError_t launch_decode_asym(const DecodeArgs& a, int Dk, int Dv, kva_dtype q_dtype, kva_dtype cache_dtype,
+                               cudaStream_t s) {
+  if (!decode_asym_supported(Dk, Dv)) return cudaErrorInvalidValue;
+  if (cache_dtype == KVA_BF16) return launch_t<bf16_t, 192>(a, q_dtype, s);
+  return launch_t<float, 192>(a, q_dtype, s);
 }
 
 }  // namespace kva

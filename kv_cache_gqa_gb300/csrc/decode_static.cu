@@ -78,6 +78,8 @@ kva_status kv_attn_decode_static(
   const int64_t inst = (int64_t)Hkv * cache.capacity * D;
   if (B > 1 && cache.inst_stride < inst) return static_fail(KVA_EINVAL, "cache inst_stride too small");
   if (D != DECODE_HEAD_DIM) return static_fail(KVA_EUNSUPPORTED, "decode is built for head_dim 128");
+  if ((cache.head_dim_v != 0 && cache.head_dim_v != D) || (cache.inst_stride_v != 0 && cache.inst_stride_v != cache.inst_stride))
+    return static_fail(KVA_EUNSUPPORTED, "the static decode takes symmetric caches only");
   const int G = n_q_heads / Hkv;
   if (G != 1 && G != 2 && G != 4) return static_fail(KVA_EUNSUPPORTED, "decode group size must be 1, 2 or 4");
   const int es = cache.dtype == KVA_BF16 ? 2 : 4;
@@ -120,6 +122,7 @@ kva_status kv_attn_decode_static(
   a.q = q; a.kc = cache.k; a.vc = cache.v; a.lengths = lengths; a.out = out;
   a.B = B; a.Hq = n_q_heads; a.Hkv = Hkv; a.capacity = cache.capacity;
   a.chunk = (int)chunk; a.max_chunks = max_chunks; a.inst_stride = cache.inst_stride;
+  a.inst_stride_v = cache.inst_stride;
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   a.scale_log2 = sc * 1.4426950408889634f;
   e = launch_decode(a, q_dtype, cache.dtype, (cudaStream_t)stream);

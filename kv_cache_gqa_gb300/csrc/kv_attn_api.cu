@@ -16,7 +16,7 @@ static std::atomic<unsigned long long> g_launches{0};
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int lmhead_max_hidden();
-bool prefill_simt_supports_head_dim(int D);
+bool prefill_simt_supports(int Dk, int Dv);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, kva_dtype dt, cudaStream_t s);
 bool prefill_tc_supports(int D, kva_dtype dt);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
@@ -42,23 +42,53 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int elem_size(kva_dtype d) { return d == KVA_BF16 ? 2 : 4; }
 bool valid_dtype(kva_dtype d) { return d == KVA_F32 || d == KVA_BF16; }
 
-kva_status check_cache(const kva_cache& c, int n_instances) {
+// Checks the cache and resolves its defaults in place (head_dim_v, inst_stride_v).
+kva_status check_cache(kva_cache& c, int n_instances) {
   if (!valid_dtype(c.dtype)) return fail(KVA_EINVAL, "cache dtype %d unknown", (int)c.dtype);
   if (!c.k || !c.v) return fail(KVA_EINVAL, "cache k/v pointer is NULL");
+  if (c.head_dim_v < 0 || c.inst_stride_v < 0) return fail(KVA_EINVAL, "negative head_dim_v or inst_stride_v");
+  if (c.head_dim_v == 0) c.head_dim_v = c.head_dim;
+  if (c.inst_stride_v == 0) c.inst_stride_v = c.inst_stride;
   if (c.n_kv_heads <= 0 || c.head_dim <= 0 || c.capacity <= 0)
     return fail(KVA_EINVAL, "cache shape must be positive (Hkv=%d D=%d capacity=%d)",
                 c.n_kv_heads, c.head_dim, c.capacity);
+  if (c.head_dim_v == c.head_dim && c.inst_stride_v != c.inst_stride)
+    return fail(KVA_EINVAL, "a symmetric cache has one instance stride (inst_stride_v %lld != %lld)",
+                (long long)c.inst_stride_v, (long long)c.inst_stride);
   const int64_t inst = (int64_t)c.n_kv_heads * c.capacity * c.head_dim;
+  const int64_t inst_v = (int64_t)c.n_kv_heads * c.capacity * c.head_dim_v;
   if (n_instances > 1 && c.inst_stride < inst)
     return fail(KVA_EINVAL, "cache inst_stride %lld < Hkv*capacity*D = %lld",
                 (long long)c.inst_stride, (long long)inst);
-  if (c.head_dim % 8 != 0) return fail(KVA_EALIGN, "head_dim %d is not a multiple of 8", c.head_dim);
+  if (n_instances > 1 && c.inst_stride_v < inst_v)
+    return fail(KVA_EINVAL, "cache inst_stride_v %lld < Hkv*capacity*Dv = %lld",
+                (long long)c.inst_stride_v, (long long)inst_v);
+  if (c.head_dim % 8 != 0 || c.head_dim_v % 8 != 0)
+    return fail(KVA_EALIGN, "head_dim %d / head_dim_v %d not a multiple of 8", c.head_dim, c.head_dim_v);
   if (!aligned16(c.k) || !aligned16(c.v)) return fail(KVA_EALIGN, "cache k/v not 16-byte aligned");
-  if ((c.inst_stride * elem_size(c.dtype)) % 16 != 0)
-    return fail(KVA_EALIGN, "cache inst_stride is not a multiple of 16 bytes");
+  if ((c.inst_stride * elem_size(c.dtype)) % 16 != 0 || (c.inst_stride_v * elem_size(c.dtype)) % 16 != 0)
+    return fail(KVA_EALIGN, "cache instance strides are not multiples of 16 bytes");
   return KVA_OK;
 }
 
+bool asymmetric(const kva_cache& c) { return c.head_dim_v != c.head_dim; }
+
+// Resolves the rotated range of a head of width Dk: [*off, *off + *width).
+kva_status rope_range(const kva_rope& r, int Dk, int* off, int* width) {
+  if (r.rot_dim == 0) {
+    if (r.rot_offset != 0) return fail(KVA_EINVAL, "rot_offset %d needs a rot_dim", r.rot_offset);
+    *off = 0; *width = Dk;
+    return KVA_OK;
+  }
+  if (r.rot_offset < 0 || r.rot_dim < 0 || (int64_t)r.rot_offset + r.rot_dim > Dk)
+    return fail(KVA_EINVAL, "rotary range [%d, %d + %d) outside the head of %d dims", r.rot_offset,
+                r.rot_offset, r.rot_dim, Dk);
+  if (r.rot_dim % 2 != 0) return fail(KVA_EINVAL, "rot_dim %d must be even", r.rot_dim);
+  *off = r.rot_offset; *width = r.rot_dim;
+  return KVA_OK;
+}
+
+// Table of a rotated block of width D (the head, or the rotary sub-range of it).
 kva_status build_rope(const kva_rope& r, int D, RopeTable* t) {
   std::memset(t, 0, sizeof(*t));
   t->kind = (int)r.kind;
@@ -88,7 +118,7 @@ kva_status build_rope(const kva_rope& r, int D, RopeTable* t) {
     }
     case KVA_ROPE_2D: {
       if (r.n_axes != 2) return fail(KVA_EINVAL, "2D RoPE needs n_axes == 2");
-      if (D % 4 != 0) return fail(KVA_EINVAL, "2D RoPE needs head_dim %% 4 == 0");
+      if (D % 4 != 0) return fail(KVA_EINVAL, "2D RoPE needs a rotated width %% 4 == 0");
       const int Q = D / 4;
       for (int b = 0; b < 2; ++b)
         for (int j = 0; j < Q; ++j) {
@@ -140,10 +170,10 @@ void set_last_error(const char* msg) { std::snprintf(g_msg, sizeof(g_msg), "%s",
 // (fixed cost = a CTA's first DRAM round trip and its merge)
 // Short contexts thus get one wave of whole-instance CTAs (no partials to merge); long, ragged
 // contexts get a few waves of equal chunks so that no CTA runs long past the others.
-int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len) {
+int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len, double row_bytes) {
   constexpr double T_FIX_US = 3.0;           // per-wave fixed cost
   constexpr double BW = 6.5e6;               // bytes per microsecond (HBM)
-  constexpr double ROW = 512.0;              // bytes per key and KV head (bf16 K + V, D = 128)
+  const double ROW = row_bytes;              // bytes per key and KV head (512: bf16 K + V, D = 128)
   const double slots = 2.0 * decode_num_sms();
   long long total = 0;
   for (int b = 0; b < B; ++b) total += lengths[b];
@@ -238,9 +268,17 @@ kva_status kv_cache_append_rope_qknorm(
     return fail(KVA_EINVAL, "q and k norm weights must both be given or both be NULL");
   if (norm.q_w && (!(norm.eps >= 0.f) || norm.inst_stride < 0))
     return fail(KVA_EINVAL, "QK-Norm eps must be >= 0 and inst_stride >= 0");
-  if (!append_supports_head_dim(D)) return fail(KVA_EUNSUPPORTED, "append: head_dim %d not built", D);
-  if (rope.kind == KVA_ROPE_INTERLEAVED && D % 16 != 0)
-    return fail(KVA_EUNSUPPORTED, "append: interleaved RoPE needs head_dim %% 16 == 0 (got %d)", D);
+  int rot_off = 0, rot_w = D;
+  if (rope.kind != KVA_ROPE_NONE) {
+    st = rope_range(rope, D, &rot_off, &rot_w);
+    if (st != KVA_OK) return st;
+  }
+  // the fast forms take symmetric heads they tile, with RoPE over the whole head
+  const bool fast = !asymmetric(cache) && rot_off == 0 && rot_w == D && append_supports_head_dim(D) &&
+                    !(rope.kind == KVA_ROPE_INTERLEAVED && D % 16 != 0);
+  if (!fast && !append_general_supports(D, cache.head_dim_v))
+    return fail(KVA_EUNSUPPORTED, "append: head dims %d/%d not built (multiples of 8 up to 256)", D,
+                cache.head_dim_v);
   if (N > 65535) return fail(KVA_EUNSUPPORTED, "append: N=%d > 65535", N);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out))
     return fail(KVA_EALIGN, "q/k/v/q_out must be 16-byte aligned");
@@ -248,7 +286,7 @@ kva_status kv_cache_append_rope_qknorm(
     return fail(KVA_EALIGN, "norm weights must be 16-byte aligned with a 16-byte instance stride");
 
   AppendArgs a{};
-  st = build_rope_table(rope, D, &a.rope);
+  st = build_rope_table(rope, rot_w, &a.rope);
   if (st != KVA_OK) return st;
   for (int n = 0; n < N; ++n)
     for (int t = 0; t < T; ++t) {
@@ -263,7 +301,10 @@ kva_status kv_cache_append_rope_qknorm(
   a.after_rope = norm.after_rope ? 1 : 0;
   a.N = N; a.T = T; a.Hq = n_q_heads; a.Hkv = Hkv; a.D = D; a.capacity = cache.capacity;
   a.inst_stride = cache.inst_stride;
-  cudaError_t e = launch_append(a, in_dtype, q_out_dtype, cache.dtype, (cudaStream_t)stream);
+  a.Dv = cache.head_dim_v; a.inst_stride_v = cache.inst_stride_v;
+  a.rot_offset = rot_off; a.rot_dim = rot_w;
+  cudaError_t e = fast ? launch_append(a, in_dtype, q_out_dtype, cache.dtype, (cudaStream_t)stream)
+                       : launch_append_general(a, in_dtype, q_out_dtype, cache.dtype, (cudaStream_t)stream);
   if (e == cudaSuccess) count_launches(1);
   return cuda_status(e, "append launch");
 }
@@ -300,15 +341,16 @@ kva_status kv_attn_prefill(
   a.row_of_slot = row_of_slot; a.out = out;
   a.N = N; a.S = S; a.Hq = n_q_heads; a.Hkv = Hkv; a.D = D; a.capacity = cache.capacity;
   a.mask = (int)mask; a.inst_stride = cache.inst_stride;
+  a.Dv = cache.head_dim_v; a.inst_stride_v = cache.inst_stride_v;
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   a.scale_log2 = sc * 1.4426950408889634f;
   cudaError_t e;
-  if (prefill_tc_supports(D, cache.dtype)) {
+  if (!asymmetric(cache) && prefill_tc_supports(D, cache.dtype)) {
     e = launch_prefill_tc(a, (cudaStream_t)stream);
-  } else if (prefill_simt_supports_head_dim(D)) {
+  } else if (prefill_simt_supports(D, cache.head_dim_v)) {
     e = launch_prefill_simt(a, cache.dtype, (cudaStream_t)stream);
   } else {
-    return fail(KVA_EUNSUPPORTED, "prefill: head_dim %d not built", D);
+    return fail(KVA_EUNSUPPORTED, "prefill: head dims %d/%d not built", D, cache.head_dim_v);
   }
   if (e == cudaSuccess) count_launches(1);
   return cuda_status(e, "prefill launch");
@@ -326,7 +368,10 @@ kva_status kv_attn_decode(
   const int D = cache.head_dim, Hkv = cache.n_kv_heads;
   if (n_q_heads <= 0 || n_q_heads % Hkv != 0)
     return fail(KVA_EINVAL, "n_q_heads %d must be a positive multiple of n_kv_heads %d", n_q_heads, Hkv);
-  if (D != DECODE_HEAD_DIM) return fail(KVA_EUNSUPPORTED, "decode: head_dim %d (built: 128)", D);
+  const int Dv = cache.head_dim_v;
+  const bool asym = asymmetric(cache);
+  if (asym ? !decode_asym_supported(D, Dv) : D != DECODE_HEAD_DIM)
+    return fail(KVA_EUNSUPPORTED, "decode: head dims %d/%d (built: 128/128, 192/128)", D, Dv);
   const int G = n_q_heads / Hkv;
   if (G != 1 && G != 2 && G != 4) return fail(KVA_EUNSUPPORTED, "decode: group size %d", G);
   if (!q || !out || !lengths || !lengths_host) return fail(KVA_EINVAL, "NULL q/out/lengths");
@@ -340,9 +385,9 @@ kva_status kv_attn_decode(
       return fail(KVA_ECAPACITY, "length %d of instance %d outside [1, %d]", L, b, cache.capacity);
     max_len = std::max(max_len, L);
   }
-  const int chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len);
+  const int chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len, (double)(D + Dv) * elem_size(cache.dtype));
   const int max_chunks = (max_len + chunk - 1) / chunk;
-  const size_t need = decode_ws_bytes(B, Hkv, n_q_heads, max_chunks, D);
+  const size_t need = decode_ws_bytes(B, Hkv, n_q_heads, max_chunks, Dv);
   if (workspace_bytes < need)
     return fail(KVA_EWORKSPACE, "decode workspace %zu bytes < %zu needed", workspace_bytes, need);
 
@@ -355,9 +400,11 @@ kva_status kv_attn_decode(
   a.q = q; a.kc = cache.k; a.vc = cache.v; a.lengths = lengths; a.out = out;
   a.B = B; a.Hq = n_q_heads; a.Hkv = Hkv; a.capacity = cache.capacity;
   a.chunk = chunk; a.max_chunks = max_chunks; a.inst_stride = cache.inst_stride;
+  a.inst_stride_v = cache.inst_stride_v;
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   a.scale_log2 = sc * 1.4426950408889634f;
-  cudaError_t e = launch_decode(a, q_dtype, cache.dtype, (cudaStream_t)stream);
+  cudaError_t e = asym ? launch_decode_asym(a, D, Dv, q_dtype, cache.dtype, (cudaStream_t)stream)
+                       : launch_decode(a, q_dtype, cache.dtype, (cudaStream_t)stream);
   if (e == cudaSuccess) count_launches(1);
   return cuda_status(e, "decode launch");
 }
@@ -384,8 +431,10 @@ kva_status kv_attn_decode_step(
     return fail(KVA_EINVAL, "q and k norm weights must both be given or both be NULL");
   if (norm.q_w && (!(norm.eps >= 0.f) || norm.inst_stride < 0)) return fail(KVA_EINVAL, "bad QK-Norm eps/stride");
   const int G = n_q_heads / Hkv;
-  if (cache.dtype != KVA_BF16 || D != DECODE_HEAD_DIM || !decode_step_supported(G))
-    return fail(KVA_EUNSUPPORTED, "fused step needs a bf16 cache, head_dim 128, Hq/Hkv in {1,2,4}");
+  if (cache.dtype != KVA_BF16 || D != DECODE_HEAD_DIM || asymmetric(cache) || !decode_step_supported(G))
+    return fail(KVA_EUNSUPPORTED, "fused step needs a symmetric bf16 cache, head_dim 128, Hq/Hkv in {1,2,4}");
+  if (rope.kind != KVA_ROPE_NONE && (rope.rot_offset != 0 || (rope.rot_dim != 0 && rope.rot_dim != D)))
+    return fail(KVA_EUNSUPPORTED, "fused step rotates the whole head (no rotary sub-range)");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (q_out && !aligned16(q_out)))
     return fail(KVA_EALIGN, "q/k/v/out/q_out must be 16-byte aligned");
   if (norm.q_w && (!aligned16(norm.q_w) || !aligned16(norm.k_w) || (norm.inst_stride * 4) % 16 != 0))
@@ -417,6 +466,7 @@ kva_status kv_attn_decode_step(
   a.q = nullptr; a.kc = cache.k; a.vc = cache.v; a.lengths = lengths; a.out = out;
   a.B = B; a.Hq = n_q_heads; a.Hkv = Hkv; a.capacity = cache.capacity;
   a.chunk = chunk; a.max_chunks = max_chunks; a.inst_stride = cache.inst_stride;
+  a.inst_stride_v = cache.inst_stride_v;
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   a.scale_log2 = sc * 1.4426950408889634f;
   sa.q = q; sa.k = k; sa.v = v; sa.in_dtype = (int)in_dtype;
@@ -454,8 +504,8 @@ kva_status kv_attn_verify(
   if (n_q_heads <= 0 || n_q_heads % Hkv != 0)
     return fail(KVA_EINVAL, "n_q_heads %d must be a positive multiple of n_kv_heads %d", n_q_heads, Hkv);
   if (!q || !out || !lengths || !lengths_host) return fail(KVA_EINVAL, "NULL q/out/lengths");
-  if (cache.dtype != KVA_BF16 || D != DECODE_HEAD_DIM)
-    return fail(KVA_EUNSUPPORTED, "verify: needs a bf16 cache with head_dim 128");
+  if (cache.dtype != KVA_BF16 || D != DECODE_HEAD_DIM || asymmetric(cache))
+    return fail(KVA_EUNSUPPORTED, "verify: needs a symmetric bf16 cache with head_dim 128");
   if (!workspace) return fail(KVA_EWORKSPACE, "verify: workspace is NULL");
   if (!aligned16(workspace)) return fail(KVA_EALIGN, "workspace must be 16-byte aligned");
   const int G = n_q_heads / Hkv, RT = verify_row_tiles(G, k);

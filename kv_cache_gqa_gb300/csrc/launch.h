@@ -40,10 +40,17 @@ struct AppendArgs {
   int after_rope;
   int N, T, Hq, Hkv, D, capacity;
   int64_t inst_stride;
+  int Dv;                  // V row width (= D unless the cache is asymmetric)
+  int64_t inst_stride_v;   // elements between V instances
+  int rot_offset, rot_dim; // rotated dims [rot_offset, rot_offset + rot_dim); the table is rot_dim wide
   RopeTable rope;
 };
 
 bool append_supports_head_dim(int D);
+// Any layout the fast forms do not take: an asymmetric cache, a rotary sub-range, other head dims.
+bool append_general_supports(int Dk, int Dv);
+cudaError_t launch_append_general(const AppendArgs& a, kva_dtype in_dtype, kva_dtype q_out_dtype,
+                                  kva_dtype cache_dtype, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, kva_dtype in_dtype, kva_dtype q_out_dtype,
                           kva_dtype cache_dtype, cudaStream_t s);
 
@@ -59,6 +66,7 @@ struct DecodeArgs {
   float* part_ml;         // [B, Hq, max_chunks, 2]
   int B, Hq, Hkv, capacity, chunk, max_chunks;
   int64_t inst_stride;
+  int64_t inst_stride_v;  // V instances (= inst_stride for symmetric caches)
   float scale_log2;       // softmax scale * log2(e)
 };
 
@@ -108,9 +116,14 @@ int decode_subtile(kva_dtype cache_dtype);   // keys per pipeline stage
 int decode_num_sms();
 // Split-KV plan: `chunk` = target keys per CTA (instance b is cut into ceil(L_b / chunk)
 // nearly equal chunks), a multiple of 64, with at most 64 chunks per instance.
-int decode_plan_chunk(const int32_t* lengths_host, int B, int Hkv, int max_len);
+// row_bytes: K plus V bytes per key and KV head.
+int decode_plan_chunk(const int32_t* lengths_host, int B, int Hkv, int max_len, double row_bytes = 512.0);
 cudaError_t launch_decode(const DecodeArgs& a, kva_dtype q_dtype, kva_dtype cache_dtype,
                           cudaStream_t s);
+// CUDA-core decode for (Dk, Dv) = (192, 128) caches (G in {1, 2, 4}).
+bool decode_asym_supported(int Dk, int Dv);
+cudaError_t launch_decode_asym(const DecodeArgs& a, int Dk, int Dv, kva_dtype q_dtype, kva_dtype cache_dtype,
+                               cudaStream_t s);
 // Fused append + decode (bf16 cache, D = 128, G in {1, 2, 4}); false if this build cannot.
 bool decode_step_supported(int G);
 cudaError_t launch_decode_step(const DecodeArgs& a, const StepArgs& st, cudaStream_t s);
@@ -149,9 +162,11 @@ struct PrefillArgs {
   const void* vc;
   const int32_t* segment;     // [S] or null
   const int32_t* row_of_slot; // [S] or null
-  float* out;                 // [N, S, Hq, D]
+  float* out;                 // [N, S, Hq, Dv]
   int N, S, Hq, Hkv, D, capacity, mask;
   int64_t inst_stride;
+  int Dv;                     // V row width (= D unless asymmetric)
+  int64_t inst_stride_v;
   float scale_log2;
 };
 int lmhead_max_hidden();

@@ -2,7 +2,9 @@
 //
 // This is the path for fp32 caches (where the contract asks for 1e-5 relative error, which
 // bf16 tensor-core operands cannot give) and for head dims the tensor-core kernel does not
-// tile.  One CTA per (64-query tile, query head, instance): Q, K and V tiles are widened
+// tile, including asymmetric caches (K rows Dk = 192 wide, V rows Dv = 128: an MLA layer
+// expanded per head, Youtu-VL-4B ncnn port, section 6).  One CTA per (64-query tile, query
+// head, instance): Q, K and V tiles are widened
 // to fp32 in shared memory; each warp owns 8 query rows, computes their 8x64 score block
 // as a register tile, applies the mask, runs the online softmax (max -> subtract -> exp
 // -> sum, final divide) and accumulates P.V with each lane owning head-dim columns.
@@ -46,16 +48,16 @@ __device__ int seg_upper(const int32_t* seg, int S, int key) {
   return lo;
 }
 
-template <int D, typename T>
-__global__ void __launch_bounds__(THREADS, 2)
+template <int D, int DV, typename T>
+__global__ void __launch_bounds__(THREADS, (D + DV > 256) ? 1 : 2)   // wide heads: one CTA per SM by smem
 prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
   constexpr int DP = D + 4;                          // padded K row (conflict-free float4)
-  constexpr int DPL = (D + 31) / 32;                 // output columns per lane
+  constexpr int DPL = (DV + 31) / 32;                // output columns per lane
   extern __shared__ __align__(16) float sm[];
   float* sQ = sm;                                    // [BQ][D]
   float* sK = sQ + BQ * D;                           // [BK][DP]
-  float* sV = sK + BK * DP;                          // [BK][D]
-  float* sP = sV + BK * D;                           // [WARPS][BK][RPW]
+  float* sV = sK + BK * DP;                          // [BK][DV]
+  float* sP = sV + BK * DV;                          // [WARPS][BK][RPW]
   __shared__ int s_range[2];
   __shared__ int s_qseg[BQ];
 
@@ -67,7 +69,7 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
   const int i1 = min(a.S, i0 + BQ);
 
   const T* Kc = reinterpret_cast<const T*>(a.kc) + (int64_t)n * a.inst_stride + (int64_t)g * a.capacity * D;
-  const T* Vc = reinterpret_cast<const T*>(a.vc) + (int64_t)n * a.inst_stride + (int64_t)g * a.capacity * D;
+  const T* Vc = reinterpret_cast<const T*>(a.vc) + (int64_t)n * a.inst_stride_v + (int64_t)g * a.capacity * DV;
   const T* Qn = reinterpret_cast<const T*>(a.q) + (int64_t)n * a.S * a.Hq * D;
 
   // ---- key range visible to this tile ----
@@ -113,9 +115,10 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
       const int j = kt + r;
       if (j < k_hi && j >= 0) {
         load_row_f32(Kc + (int64_t)j * D, sK + r * DP, D, lane, 32);
-        load_row_f32(Vc + (int64_t)j * D, sV + r * D, D, lane, 32);
+        load_row_f32(Vc + (int64_t)j * DV, sV + r * DV, DV, lane, 32);
       } else {
-        for (int e = lane; e < D; e += 32) { sK[r * DP + e] = 0.f; sV[r * D + e] = 0.f; }
+        for (int e = lane; e < D; e += 32) sK[r * DP + e] = 0.f;
+        for (int e = lane; e < DV; e += 32) sV[r * DV + e] = 0.f;
       }
     }
     __syncthreads();
@@ -186,7 +189,7 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
 #pragma unroll
       for (int c = 0; c < DPL; ++c) {
         const int d = lane + 32 * c;
-        const float v = (d < D) ? sV[j * D + d] : 0.f;
+        const float v = (d < DV) ? sV[j * DV + d] : 0.f;
 #pragma unroll
         for (int r = 0; r < RPW; ++r) acc[r][c] = fmaf(p[r], v, acc[r][c]);
       }
@@ -201,49 +204,53 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
     if (i >= i1) continue;
     const int row = a.row_of_slot ? a.row_of_slot[i] : i;
     if (row < 0 || row >= a.S) continue;
-    float* o = a.out + (((int64_t)n * a.S + row) * a.Hq + h) * D;
+    float* o = a.out + (((int64_t)n * a.S + row) * a.Hq + h) * DV;
     const float inv = 1.0f / l_run[r];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) {
       const int d = lane + 32 * c;
-      if (d < D) o[d] = acc[r][c] * inv;
+      if (d < DV) o[d] = acc[r][c] * inv;
     }
   }
 }
 
-template <int D>
-size_t simt_smem() { return sizeof(float) * ((size_t)BQ * D + BK * (D + 4) + BK * D + WARPS * BK * RPW); }
+template <int D, int DV>
+size_t simt_smem() { return sizeof(float) * ((size_t)BQ * D + BK * (D + 4) + BK * DV + WARPS * BK * RPW); }
 
-template <int D, typename T>
+template <int D, int DV, typename T>
 cudaError_t launch_dt(const PrefillArgs& a, cudaStream_t s) {
-  const size_t smem = simt_smem<D>();
+  const size_t smem = simt_smem<D, DV>();
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<D, T>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<D, DV, T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   dim3 grid((a.S + BQ - 1) / BQ, a.Hq, a.N);
-  prefill_simt_kernel<D, T><<<grid, THREADS, smem, s>>>(a);
+  prefill_simt_kernel<D, DV, T><<<grid, THREADS, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, int DV>
 cudaError_t launch_d(const PrefillArgs& a, kva_dtype dt, cudaStream_t s) {
-  if (dt == KVA_BF16) return launch_dt<D, bf16_t>(a, s);
-  return launch_dt<D, float>(a, s);
+  if (dt == KVA_BF16) return launch_dt<D, DV, bf16_t>(a, s);
+  return launch_dt<D, DV, float>(a, s);
 }
 
 }  // namespace
 
-bool prefill_simt_supports_head_dim(int D) { return D == 64 || D == 72 || D == 128; }
+bool prefill_simt_supports(int Dk, int Dv) {
+  return (Dk == Dv && (Dk == 64 || Dk == 72 || Dk == 128)) || (Dk == 192 && Dv == 128);
+}
 
 cudaError_t launch_prefill_simt(const PrefillArgs& a, kva_dtype dt, cudaStream_t s) {
+  if (a.D == 192 && a.Dv == 128) return launch_d<192, 128>(a, dt, s);
+  if (a.D != a.Dv) return cudaErrorInvalidValue;
   switch (a.D) {
-    case 64: return launch_d<64>(a, dt, s);
-    case 72: return launch_d<72>(a, dt, s);
-    case 128: return launch_d<128>(a, dt, s);
+    case 64: return launch_d<64, 64>(a, dt, s);
+    case 72: return launch_d<72, 72>(a, dt, s);
+    case 128: return launch_d<128, 128>(a, dt, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -33,12 +33,12 @@ class KvaError(RuntimeError):
 class _Cache(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("dtype", C.c_int),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("capacity", C.c_int32),
-                ("inst_stride", C.c_int64)]
+                ("inst_stride", C.c_int64), ("head_dim_v", C.c_int32), ("inst_stride_v", C.c_int64)]
 
 
 class _Rope(C.Structure):
     _fields_ = [("kind", C.c_int), ("n_axes", C.c_int32), ("sections", C.c_int32 * 4),
-                ("base", C.c_double)]
+                ("base", C.c_double), ("rot_offset", C.c_int32), ("rot_dim", C.c_int32)]
 
 
 class _Norm(C.Structure):
@@ -137,19 +137,21 @@ def _stream(stream) -> Optional[int]:
 
 @dataclasses.dataclass
 class KVCache:
-    """N cache instances: k, v torch CUDA tensors [N, Hkv, capacity, D] (f32 or bf16)."""
+    """N cache instances: k [N, Hkv, capacity, Dk] and v [N, Hkv, capacity, Dv] torch CUDA
+    tensors (f32 or bf16); Dv differs from Dk for an asymmetric (MLA-expanded) cache."""
     k: object
     v: object
 
     @property
     def struct(self) -> _Cache:
-        k = self.k
-        if k.dim() != 4 or self.v.shape != k.shape or self.v.dtype != k.dtype:
-            raise KvaError(KVA_EINVAL, "cache k/v must be matching [N, Hkv, W, D] tensors")
-        if not (k.is_contiguous() and self.v.is_contiguous()):
+        k, v = self.k, self.v
+        if k.dim() != 4 or v.dim() != 4 or v.shape[:3] != k.shape[:3] or v.dtype != k.dtype:
+            raise KvaError(KVA_EINVAL, "cache k/v must be [N, Hkv, W, Dk] / [N, Hkv, W, Dv] tensors of one dtype")
+        if not (k.is_contiguous() and v.is_contiguous()):
             raise KvaError(KVA_EINVAL, "cache tensors must be contiguous")
         N, Hkv, W, D = k.shape
-        return _Cache(k.data_ptr(), self.v.data_ptr(), _dtype_code(k), Hkv, D, W, Hkv * W * D)
+        Dv = v.shape[3]
+        return _Cache(k.data_ptr(), v.data_ptr(), _dtype_code(k), Hkv, D, W, Hkv * W * D, Dv, Hkv * W * Dv)
 
     @property
     def n_kv_heads(self):
@@ -160,16 +162,24 @@ class KVCache:
         return self.k.shape[3]
 
     @property
+    def head_dim_v(self):
+        return self.v.shape[3]
+
+    @property
     def capacity(self):
         return self.k.shape[2]
 
 
 @dataclasses.dataclass
 class Rope:
-    """kind: 'none' | '1d' | 'sections' | '2d' | 'interleaved'; sections for 'sections' (sum D/2)."""
+    """kind: 'none' | '1d' | 'sections' | '2d' | 'interleaved'; sections for 'sections' (sum W/2).
+    rot_offset / rot_dim: rotate head dims [rot_offset, rot_offset + rot_dim) only (W = rot_dim);
+    rot_dim 0 = the whole head."""
     kind: str = "1d"
     base: float = 1e6
     sections: Sequence[int] = ()
+    rot_offset: int = 0
+    rot_dim: int = 0
 
     @property
     def n_axes(self) -> int:
@@ -178,7 +188,8 @@ class Rope:
     @property
     def struct(self) -> _Rope:
         secs = (C.c_int32 * 4)(*(list(self.sections) + [0] * (4 - len(self.sections))))
-        return _Rope(ROPE_KINDS[self.kind], self.n_axes, secs, float(self.base))
+        return _Rope(ROPE_KINDS[self.kind], self.n_axes, secs, float(self.base), int(self.rot_offset),
+                     int(self.rot_dim))
 
 
 def kv_cache_append_rope_qknorm(q, k, v, pos, slot, slot_host, cache: KVCache, q_out, rope: Rope,

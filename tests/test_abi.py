@@ -13,6 +13,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def K():
+    try:
+        import torch
+        if torch.cuda.is_available():
+            # the calls below pass dummy device addresses; a validation gap must never reach a GPU
+            pytest.skip("ABI validation tests run on hosts without a GPU")
+    except ImportError:
+        pass
     from kv_cache_gqa_gb300 import build
     build.build_library(verbose=False)
     import kv_cache_gqa_gb300.kv_attn as K
@@ -42,14 +49,14 @@ def test_strerror_and_version(K):
     assert L.kva_launch_count() >= 0
 
 
-def _cache(ptr=16, dtype=1, hkv=8, d=128, cap=1024, stride=None):
+def _cache(ptr=16, dtype=1, hkv=8, d=128, cap=1024, stride=None, dv=0, stride_v=0):
     import kv_cache_gqa_gb300.kv_attn as K
-    return K._Cache(ptr, ptr, dtype, hkv, d, cap, stride if stride is not None else hkv * cap * d)
+    return K._Cache(ptr, ptr, dtype, hkv, d, cap, stride if stride is not None else hkv * cap * d, dv, stride_v)
 
 
-def _rope(kind=1, base=1e6, secs=(0, 0, 0, 0), n_axes=1):
+def _rope(kind=1, base=1e6, secs=(0, 0, 0, 0), n_axes=1, rot_offset=0, rot_dim=0):
     import kv_cache_gqa_gb300.kv_attn as K
-    return K._Rope(kind, n_axes, (C.c_int32 * 4)(*secs), base)
+    return K._Rope(kind, n_axes, (C.c_int32 * 4)(*secs), base, rot_offset, rot_dim)
 
 
 def _norm(q=0, k=0, eps=1e-6):
@@ -75,15 +82,45 @@ def test_append_validation(K):
     assert append(K, slot_host=[-1]) == K.KVA_ECAPACITY
     assert append(K, q=FAKE + 4) == K.KVA_EALIGN
     assert append(K, cache=_cache(FAKE, d=100)) == K.KVA_EALIGN              # D % 8
-    assert append(K, cache=_cache(FAKE, d=80)) == K.KVA_EUNSUPPORTED         # D not built
+    assert append(K, cache=_cache(FAKE, d=264)) == K.KVA_EUNSUPPORTED        # D above 256
     assert append(K, rope=_rope(kind=2, secs=(16, 16, 16, 8), n_axes=4)) == K.KVA_EINVAL  # sum != D/2
     assert append(K, rope=_rope(kind=3, n_axes=1)) == K.KVA_EINVAL
-    assert append(K, rope=_rope(kind=4), cache=_cache(FAKE, d=72)) == K.KVA_EUNSUPPORTED   # interleaved, D % 16
     assert append(K, rope=_rope(kind=5)) == K.KVA_EINVAL
     assert append(K, rope=_rope(base=-1.0)) == K.KVA_EINVAL
     assert append(K, norm=_norm(q=FAKE)) == K.KVA_EINVAL                     # q weight without k weight
     assert append(K, cache=_cache(FAKE, stride=5), N=2, slot_host=[0, 0]) == K.KVA_EINVAL
     assert b"stride" in K.lib().kva_last_error()
+
+
+def test_asymmetric_cache_and_rotary_range_validation(K):
+    """K rows 192 wide, V rows 128 (MLA-expanded cache) and RoPE over a sub-range of the head."""
+    asym = dict(hkv=32, d=192, dv=128, cap=512)
+    assert append(K, rope=_rope(kind=4, rot_offset=128, rot_dim=63), Hq=32, cache=_cache(FAKE, **asym)) == K.KVA_EINVAL
+    assert append(K, rope=_rope(kind=4, rot_offset=160, rot_dim=64), Hq=32, cache=_cache(FAKE, **asym)) == K.KVA_EINVAL
+    assert append(K, rope=_rope(kind=1, rot_offset=8), cache=_cache(FAKE)) == K.KVA_EINVAL   # offset without width
+    assert append(K, rope=_rope(kind=3, n_axes=2, rot_offset=0, rot_dim=62)) == K.KVA_EINVAL  # 2D needs W % 4
+    assert append(K, rope=_rope(kind=2, secs=(16, 8, 0, 0), n_axes=2, rot_dim=64)) == K.KVA_EINVAL  # sum != W/2
+    assert append(K, Hq=32, cache=_cache(FAKE, hkv=32, d=192, dv=264, cap=512)) == K.KVA_EUNSUPPORTED
+    assert append(K, Hq=32, cache=_cache(FAKE, **asym, stride_v=-16)) == K.KVA_EINVAL
+    two = dict(N=2, slot_host=[0, 0], Hq=32)
+    assert append(K, cache=_cache(FAKE, hkv=32, d=192, dv=128, cap=512, stride_v=32 * 512 * 128 - 8), **two) == K.KVA_EINVAL
+    assert b"inst_stride_v" in K.lib().kva_last_error()
+    assert append(K, cache=_cache(FAKE, stride_v=8 * 1024 * 128 + 64), N=2, slot_host=[0, 0]) == K.KVA_EINVAL  # symmetric
+    assert append(K, Hq=32, cache=_cache(FAKE, hkv=32, d=192, dv=100, cap=512)) == K.KVA_EALIGN
+    L = K.lib()
+    lh = np.array([3], np.int32)
+    ac = _cache(FAKE, hkv=32, d=192, dv=64, cap=64)
+    assert L.kv_attn_decode(FAKE, 1, ac, FAKE, lh.ctypes.data, 1, 32, 0.0, FAKE, FAKE, 1 << 30, None) == K.KVA_EUNSUPPORTED
+    ac = _cache(FAKE, hkv=32, d=192, dv=128, cap=64)
+    assert L.kv_attn_decode_step(FAKE, FAKE, FAKE, 0, FAKE, 0, _norm(), _rope(), ac, FAKE, lh.ctypes.data, 1, 32,
+                                 0.0, None, 0, FAKE, FAKE, 1 << 30, None) == K.KVA_EUNSUPPORTED
+    sc = _cache(FAKE, cap=64)
+    assert L.kv_attn_decode_step(FAKE, FAKE, FAKE, 0, FAKE, 0, _norm(), _rope(rot_offset=64, rot_dim=64), sc, FAKE,
+                                 lh.ctypes.data, 1, 16, 0.0, None, 0, FAKE, FAKE, 1 << 30, None) == K.KVA_EUNSUPPORTED
+    assert L.kv_attn_verify(FAKE, 1, ac, FAKE, lh.ctypes.data, 1, 2, 32, 0.0, FAKE, FAKE, 1 << 30, None) == K.KVA_EUNSUPPORTED
+    assert L.kv_attn_decode_static(FAKE, 1, ac, FAKE, lh.ctypes.data, 1, 32, 0.0, FAKE, None) == K.KVA_EUNSUPPORTED
+    pc = _cache(FAKE, hkv=32, d=160, dv=128, cap=64)
+    assert L.kv_attn_prefill(FAKE, 1, pc, 1, 3, 32, 0, None, None, None, 0.0, FAKE, None) == K.KVA_EUNSUPPORTED
 
 
 def test_prefill_validation(K):
