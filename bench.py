@@ -341,6 +341,81 @@ def serving_bench(torch, K, stream, W, lm_ws_bytes):
             "lm_head_GB/s": round((VOCAB * HIDDEN * 2) / (lm_ms / 1e3) / 1e9, 1)}
 
 
+MLA_LAYERS, MLA_H, MLA_W, MLA_DK, MLA_DV = 40, 32, 512, 192, 128
+
+
+def mla_bench(torch, K, stream):
+    """The asymmetric MLA-expanded cache of a 40-layer model (K rows 192 wide, V rows 128, 32 heads,
+    a 512-slot window, interleaved RoPE on the last 64 K dims): the prompt phase (per layer: append
+    512 bf16 tokens, causal prefill over them) and one decode token (per layer: append, decode over
+    the full 512-slot window), each as a graph of all 40 layers back to back; plus the decode kernel
+    alone on 16 sequences x 32 heads x 4096 slots, a cache larger than L2, for its bandwidth."""
+    Lr, H, W, DKm, DVm = MLA_LAYERS, MLA_H, MLA_W, MLA_DK, MLA_DV
+    g = torch.Generator(device="cuda"); g.manual_seed(13)
+    bf = torch.bfloat16
+    kc = torch.zeros((Lr, H, W, DKm), device="cuda", dtype=bf)
+    vc = torch.zeros((Lr, H, W, DVm), device="cuda", dtype=bf)
+    caches = [K.KVCache(kc[l:l + 1], vc[l:l + 1]) for l in range(Lr)]
+    rope = K.Rope("interleaved", 1e6, rot_offset=128, rot_dim=64)
+    q = torch.randn((1, W, H, DKm), device="cuda", generator=g).to(bf)
+    k = torch.randn((1, W, H, DKm), device="cuda", generator=g).to(bf)
+    v = torch.randn((1, W, H, DVm), device="cuda", generator=g).to(bf)
+    pos = torch.arange(W, dtype=torch.int32, device="cuda").view(1, W, 1)
+    slot_h = np.arange(W, dtype=np.int32).reshape(1, W)
+    slot = torch.from_numpy(slot_h).cuda()
+    q_out = torch.empty((1, W, H, DKm), device="cuda", dtype=bf)
+    out = torch.empty((1, W, H, DVm), device="cuda")
+
+    def prompt():
+        for c in caches:
+            K.kv_cache_append_rope_qknorm(q, k, v, pos, slot, slot_h, c, q_out, rope)
+            K.kv_attn_prefill(q_out, c, out, mask="causal")
+
+    qn, kn, vn = q[:, :1].contiguous(), k[:, :1].contiguous(), v[:, :1].contiguous()
+    pn = torch.full((1, 1, 1), W - 1, dtype=torch.int32, device="cuda")
+    sn_h = np.full((1, 1), W - 1, np.int32)
+    sn = torch.from_numpy(sn_h).cuda()
+    lens_h = np.array([W], np.int32)
+    lens = torch.from_numpy(lens_h).cuda()
+    qo = torch.empty((1, 1, H, DKm), device="cuda", dtype=bf)
+    o = torch.empty((1, H, DVm), device="cuda")
+    ws = torch.zeros(K.decode_workspace_bytes(1, H, H, W, DVm), dtype=torch.uint8, device="cuda")
+
+    def token():
+        for c in caches:
+            K.kv_cache_append_rope_qknorm(qn, kn, vn, pn, sn, sn_h, c, qo, rope)
+            K.kv_attn_decode(qo[:, 0], c, lens, lens_h, o, ws)
+
+    B2, L2 = 16, 4096
+    kb = torch.randn((B2, H, L2, DKm), device="cuda", generator=g).to(bf)
+    vb = torch.randn((B2, H, L2, DVm), device="cuda", generator=g).to(bf)
+    qb = torch.randn((B2, H, DKm), device="cuda", generator=g).to(bf)
+    ob = torch.empty((B2, H, DVm), device="cuda")
+    lb_h = np.full(B2, L2, np.int32)
+    lb = torch.from_numpy(lb_h).cuda()
+    wsb = torch.zeros(K.decode_workspace_bytes(B2, H, H, L2, DVm), dtype=torch.uint8, device="cuda")
+    cb = K.KVCache(kb, vb)
+    big = lambda: K.kv_attn_decode(qb, cb, lb, lb_h, ob, wsb)
+    with torch.cuda.stream(stream):
+        prompt(); token(); big()                       # configure the kernels before capture
+    torch.cuda.synchronize()
+    prompt_ms = graph_avg_ms(torch, stream, prompt, 1, reps=4)
+    token_ms = graph_avg_ms(torch, stream, token, 2, reps=4)
+    big_ms = graph_avg_ms(torch, stream, big, 8, reps=2)
+    big_bytes = B2 * H * L2 * (DKm + DVm) * 2 + B2 * H * (DKm * 2 + DVm * 4)
+    tok_bytes = Lr * H * W * (DKm + DVm) * 2
+    del kb, vb, kc, vc
+    return {"config": f"{Lr} layers, {H}/{H} heads, K {DKm} / V {DVm}, {W}-slot bf16 window, interleaved RoPE "
+                      f"on dims 128..191; prompt = {W} tokens (append + causal prefill per layer), token = one "
+                      f"decode step at the full window (append + decode per layer)",
+            "prompt_ms": round(prompt_ms, 3), "prompt_tokens_per_s": round(W / (prompt_ms / 1e3), 1),
+            "token_us": round(token_ms * 1e3, 1), "token_per_layer_us": round(token_ms * 1e3 / Lr, 2),
+            "token_cache_GB/s": round(tok_bytes / (token_ms / 1e3) / 1e9, 1),
+            "decode_16x4096_us": round(big_ms * 1e3, 1),
+            "decode_16x4096_GB/s": round(big_bytes / (big_ms / 1e3) / 1e9, 1),
+            "decode_16x4096_algorithmic_bytes": big_bytes}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import kv_cache_gqa_gb300 as K
@@ -424,6 +499,7 @@ def run_gpu(args, rank, world, local_rank):
     # 16-token blocks (each launch streams 537 MB of K/V once for all 16 block rows)
     vb = verify_bench(torch, K, stream)
     sv = serving_bench(torch, K, stream, job.W, None)
+    mla = mla_bench(torch, K, stream)
 
     # ---- end to end: inputs from pinned host memory, ids back to the host, every step ----
     host_in = {n: getattr(job, n).cpu().pin_memory() for n in ("q", "k", "v", "dq", "dk", "dv", "h")}
@@ -507,6 +583,7 @@ def run_gpu(args, rank, world, local_rank):
                 "verify_block": dict(vb, frac_hbm=round(vb["GB/s"] / hbm, 4)),
                 "batched_serving": dict(sv, decode_frac_hbm=round(sv["decode_GB/s"] / hbm, 4),
                                         lm_head_frac_hbm=round(sv["lm_head_GB/s"] / hbm, 4)),
+                "mla_asymmetric_cache": dict(mla, decode_16x4096_frac_hbm=round(mla["decode_16x4096_GB/s"] / hbm, 4)),
                 "lm_head_final_norm_top1_us": round(lm_norm_ms * 1e3, 2),
                 "lm_head_final_norm_top8_us": round(lm_top8_ms * 1e3, 2),
                 "time_share": {k: round(v / sum(totals.values()), 4) for k, v in totals.items()},

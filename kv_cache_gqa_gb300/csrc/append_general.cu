@@ -9,8 +9,9 @@
 //    interleaved: implementation difficulty 2); the rest passes through.
 //  - Any head width that is a multiple of 8 up to 256.
 //
-// One CTA per (token t, instance n), one warp per row.  The token's rot_dim/2 angles are
-// evaluated once into shared memory.  A lane holds 8 consecutive elements of its row in
+// One CTA per (token t, instance n, row group), one warp per row; short appends (a decode
+// token) split a token's rows over several CTAs so that its row loads run in parallel.  Each
+// CTA evaluates the token's rot_dim/2 angles once into shared memory.  A lane holds 8 consecutive elements of its row in
 // registers (a 16- or 32-byte access); the row is mirrored into a per-warp shared buffer so
 // that each element can read its rotation partner wherever it sits (rotate-half partner,
 // 2D-halves partner, or the interleaved pair).  The norm's sum of squares is a warp
@@ -20,6 +21,8 @@
 // in 1D, xdRoPE-section, 2D-halves or de-interleaved form (Youtu-VL-4B ncnn port,
 // implementation difficulty 2; HunyuanOCR v1.0 ncnn port, section five; Penguin-VL ncnn
 // port, section 2.3); k/v written into the token's cache slot (Youtu-VL-4B ncnn port, step 6).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -65,7 +68,7 @@ append_general_kernel(const __grid_constant__ AppendArgs a) {
 
   float* rowbuf = s_row[warp];
   const int e0 = lane * 8;
-  for (int r = warp; r < n_rows; r += GEN_WARPS) {
+  for (int r = blockIdx.z * GEN_WARPS + warp; r < n_rows; r += GEN_WARPS * gridDim.z) {
     const int kind = r < a.Hq ? 0 : (r < a.Hq + a.Hkv ? 1 : 2);     // q, k, v (warp-uniform)
     const int head = kind == 0 ? r : (kind == 1 ? r - a.Hq : r - a.Hq - a.Hkv);
     const int width = kind == 2 ? Dv : Dk;
@@ -148,9 +151,24 @@ append_general_kernel(const __grid_constant__ AppendArgs a) {
   }
 }
 
+int gen_num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 148;
+  }
+  return n;
+}
+
 template <typename InT, typename QOutT>
 cudaError_t launch_c(const AppendArgs& a, kva_dtype cache_dtype, cudaStream_t s) {
-  dim3 grid(a.T, a.N);
+  // row groups per token: enough CTAs for about two per SM, at most one warp per row
+  const int64_t tokens = (int64_t)a.T * a.N;
+  const int n_rows = a.Hq + 2 * a.Hkv;
+  const int max_groups = (n_rows + GEN_WARPS - 1) / GEN_WARPS;
+  const int groups = (int)std::max<int64_t>(1, std::min<int64_t>(max_groups, 2 * gen_num_sms() / std::max<int64_t>(1, tokens)));
+  dim3 grid(a.T, a.N, std::min(groups, 65535));
   if (cache_dtype == KVA_BF16) append_general_kernel<InT, QOutT, bf16_t><<<grid, GEN_THREADS, 0, s>>>(a);
   else append_general_kernel<InT, QOutT, float><<<grid, GEN_THREADS, 0, s>>>(a);
   return cudaGetLastError();

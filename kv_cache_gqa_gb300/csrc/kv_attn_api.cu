@@ -167,14 +167,16 @@ void set_last_error(const char* msg) { std::snprintf(g_msg, sizeof(g_msg), "%s",
 // simple cost model and the cheapest wins:
 //   one wave:   fixed cost + max(all bytes / HBM bandwidth, one chunk / one CTA's share)
 //   more waves: waves x fixed cost + all bytes / HBM bandwidth + one chunk / share (the tail)
-// (fixed cost = a CTA's first DRAM round trip and its merge)
+// (fixed cost = a CTA's first DRAM round trip and its merge; a CTA's share of the bandwidth is
+// at most what its ~100 KB of copies in flight sustain, so a small batch still spreads its keys)
 // Short contexts thus get one wave of whole-instance CTAs (no partials to merge); long, ragged
 // contexts get a few waves of equal chunks so that no CTA runs long past the others.
-int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len, double row_bytes) {
+int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len, double row_bytes, int ctas_per_sm) {
   constexpr double T_FIX_US = 3.0;           // per-wave fixed cost
   constexpr double BW = 6.5e6;               // bytes per microsecond (HBM)
+  constexpr double CTA_BW = 1.0e5;           // bytes per microsecond one CTA sustains
   const double ROW = row_bytes;              // bytes per key and KV head (512: bf16 K + V, D = 128)
-  const double slots = 2.0 * decode_num_sms();
+  const double slots = (double)ctas_per_sm * decode_num_sms();
   long long total = 0;
   for (int b = 0; b < B; ++b) total += lengths[b];
   const double total_bytes = (double)total * Hkv * ROW;
@@ -191,7 +193,7 @@ int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len, doubl
     for (int b = 0; b < B; ++b) ctas += (lengths[b] + chunk - 1) / chunk;
     ctas *= Hkv;
     const double waves = std::ceil((double)ctas / slots);
-    const double share = BW / std::min((double)ctas, slots);
+    const double share = std::min(CTA_BW, BW / std::min((double)ctas, slots));
     const double chunk_t = (double)chunk * ROW / share;  // one CTA's chunk at its bandwidth share
     const double t = waves <= 1.0 ? T_FIX_US + std::max(total_bytes / BW, chunk_t)
                                   : waves * T_FIX_US + total_bytes / BW + chunk_t;   // + tail of the last wave
@@ -385,7 +387,8 @@ kva_status kv_attn_decode(
       return fail(KVA_ECAPACITY, "length %d of instance %d outside [1, %d]", L, b, cache.capacity);
     max_len = std::max(max_len, L);
   }
-  const int chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len, (double)(D + Dv) * elem_size(cache.dtype));
+  const int chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len, (double)(D + Dv) * elem_size(cache.dtype),
+                                      asym ? 1 : 2);
   const int max_chunks = (max_len + chunk - 1) / chunk;
   const size_t need = decode_ws_bytes(B, Hkv, n_q_heads, max_chunks, Dv);
   if (workspace_bytes < need)

@@ -116,8 +116,9 @@ int decode_subtile(kva_dtype cache_dtype);   // keys per pipeline stage
 int decode_num_sms();
 // Split-KV plan: `chunk` = target keys per CTA (instance b is cut into ceil(L_b / chunk)
 // nearly equal chunks), a multiple of 64, with at most 64 chunks per instance.
-// row_bytes: K plus V bytes per key and KV head.
-int decode_plan_chunk(const int32_t* lengths_host, int B, int Hkv, int max_len, double row_bytes = 512.0);
+// row_bytes: K plus V bytes per key and KV head; ctas_per_sm: resident decode CTAs per SM.
+int decode_plan_chunk(const int32_t* lengths_host, int B, int Hkv, int max_len, double row_bytes = 512.0,
+                      int ctas_per_sm = 2);
 cudaError_t launch_decode(const DecodeArgs& a, kva_dtype q_dtype, kva_dtype cache_dtype,
                           cudaStream_t s);
 // CUDA-core decode for (Dk, Dv) = (192, 128) caches (G in {1, 2, 4}).
