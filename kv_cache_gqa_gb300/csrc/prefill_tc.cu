@@ -1,27 +1,36 @@
 // Kernel (b), tensor-core form: flash-style prefill attention on tcgen05 (bf16 operands,
-// fp32 accumulation in tensor memory).
+// fp32 accumulation in tensor memory), persistent.
 //
-// One CTA serves two 128-row query tiles ("slots") that read the same KV head: the two query
+// Work unit: two 128-row query tiles ("slots") that read the same KV head: the two query
 // heads of a GQA group at the same rows when the group size is even (each K/V tile is loaded
 // once for both), otherwise two row tiles of one head paired so that causal work is balanced
-// (tiles t and n-1-t).  Ten warps with fixed roles:
+// (tiles t and n-1-t).  Units are numbered heaviest first; one CTA per SM walks units
+// b, 2P-1-b, 2P+b, ... (a snake over the P CTAs, which evens out the causal cost), so a
+// unit's epilogue overlaps the next unit's Q load and first Q K^T.
+//
+// Twelve warps (three warpgroups) with fixed roles:
 //   warps 0-3, 4-7  softmax of slot 0 and slot 1: thread t of a group owns row t = TMEM lane
-//              t.  It stages its Q row in shared memory (128-byte swizzled, K-major), then per
-//              key tile reads the 128 fp32 scores from TMEM, applies the row's visible-key
-//              range (causal, window segment or full), keeps the running max and sum, writes
-//              P = exp2(S - m) back into the same TMEM columns as packed bf16 pairs, and at
-//              the end divides O by the row sum.  O is rescaled only when the row max grows
-//              by more than 2^8 (the stale max keeps every P <= 256).
-//   warp 8     TMA producer: K and V tiles (64-column, 128-byte swizzled boxes) into a
-//              2-stage ring; rows past the valid keys read as zeros.
+//              t.  Per key tile it reads the row's 128 fp32 scores from TMEM, applies the
+//              row's visible-key range (causal, window segment or full), keeps the running
+//              max and sum, and writes P = exp2(S - m) back over the same columns as packed
+//              bf16 pairs.  O is rescaled only when the row max grows by more than 2^8 (the
+//              stale max keeps every P <= 256).  At the end of a unit it copies O out of
+//              TMEM (which frees it for the next unit's P V), divides by the row sum and
+//              writes the rows through a double-buffered 32 x 16 staging tile per warp with
+//              TMA stores.
+//   warp 8     TMA producer: per unit the slots' Q tiles (once the previous unit's last
+//              Q K^T has read its Q), then K and V tiles (64-column, 128-byte swizzled boxes)
+//              into a 2-stage ring that runs on across units; rows past the valid keys read
+//              as zeros.
 //   warp 9     MMA issuer (one thread).  TMEM: S of slot s at columns [128 s, 128 s + 128),
 //              O of slot s at [256 + 128 s, ...).  Per key tile j it issues, for s = 0, 1:
 //              O_s += P_s(j) V_j once slot s's softmax has written P_s(j), then
 //              S_s(j+1) = Q_s K_{j+1}^T into the same columns (tensor-core operations of one
-//              thread run in issue order, so the P V read precedes the overwrite).  While
-//              one slot's warps run the softmax of tile j, the tensor core works on the
-//              other slot's P V and next S: the two slots ping-pong.
-// Every mbarrier wait is bounded; a timeout marks the output rows NaN instead of hanging.
+//              thread run in issue order, so the P V read precedes the overwrite).  While one
+//              slot's warps run the softmax of tile j, the tensor core works on the other
+//              slot's P V and next S: the two slots ping-pong.
+// Every mbarrier wait is bounded; a timeout stops the CTA and marks its remaining output rows
+// NaN instead of hanging.
 //
 // Method: QK^T*scale + mask, softmax, times V (Youtu-VL-4B ncnn port, implementation
 // difficulty 3; parallel causal prefill, step 7; block-diagonal window mask, step 3) fused
@@ -39,11 +48,18 @@ namespace {
 
 constexpr int BM = 128;                   // query rows per slot = TMEM lanes
 constexpr int BN = 128;                   // keys per tile
-constexpr int SOFTMAX_WARPS = 16;         // per slot: 4 lane quarters x 2 column halves
-constexpr int TMA_WARP = 16, MMA_WARP = 17;
-constexpr int THREADS = 576;
+constexpr int SOFTMAX_WARPS = 8;          // 4 per slot, one row per thread
+constexpr int TMA_WARP = 8, MMA_WARP = 9;  // warps 10, 11 complete their warpgroup and idle
+constexpr int THREADS = 384;
+// Registers per thread: 168 at launch (65536 / 384, rounded down to a multiple of 8); the
+// producer/MMA warpgroup gives up 64 per thread, which the two softmax warpgroups take:
+// 128 * (200 + 200 + 104) = 384 * 168, so the increase never waits on registers nobody frees.
+constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 200, REGS_CONTROL = 104;
+static_assert(2 * REGS_SOFTMAX + REGS_CONTROL <= 3 * REGS_LAUNCH, "register split exceeds the launch total");
+static_assert(REGS_LAUNCH * THREADS <= 65536, "launch registers");
 constexpr int SUB = BM * 128;             // bytes of one [128 rows x 64 bf16] swizzled box
 constexpr int NSTAGE = 2;
+constexpr int ST_BYTES = 32 * 64;         // one staging tile: 32 rows x 16 fp32 (64-byte swizzle)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
 
@@ -53,7 +69,8 @@ struct Layout {
   static constexpr int Q_OFF = 0;                            // [2 slots][NSUB boxes]
   static constexpr int K_OFF = Q_OFF + 2 * NSUB * SUB;       // [NSTAGE][NSUB]
   static constexpr int V_OFF = K_OFF + NSTAGE * NSUB * SUB;  // [NSTAGE][NSUB]
-  static constexpr int BAR_OFF = V_OFF + NSTAGE * NSUB * SUB;
+  static constexpr int ST_OFF = V_OFF + NSTAGE * NSUB * SUB; // [softmax warp][2]
+  static constexpr int BAR_OFF = ST_OFF + SOFTMAX_WARPS * 2 * ST_BYTES;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;          // + slack to align the base to 1024
 };
 
@@ -85,6 +102,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+// 16 consecutive TMEM columns of this thread's lane, into x[0..16) as floats.
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float* x) {
+  uint32_t r[16];
+  tmem_ld16(taddr, r);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(r[e]);
+}
 // Paired fp32 arithmetic (two lanes of a 64-bit register pair per instruction) and a
 // three-input max.
 __device__ __forceinline__ uint64_t f2(float a, float b) {
@@ -115,21 +139,48 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ void bulk_wait_read(int pending) {   // pending: 0 or 1 (immediate)
+  if (pending == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  else asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// The two slots of a CTA: (query head, row tile) each, or an empty slot (qt < 0).
-struct Slots {
-  int h[2], qt[2];
+// Unit geometry: units are numbered x fastest (KV-head pair or head), then instance, then
+// the row-tile index z, with z = 0 the heaviest causal tiles.
+struct Units {
+  int X, Z, total;
 };
-__device__ __forceinline__ Slots cta_slots(const PrefillArgs& a, int nq) {
+__device__ __forceinline__ Units unit_geometry(const PrefillArgs& a) {
+  const int nq = (a.S + BM - 1) / BM;
+  const bool pair_heads = (a.Hq / a.Hkv) % 2 == 0;
+  Units g;
+  g.X = pair_heads ? a.Hq / 2 : a.Hq;
+  g.Z = pair_heads ? nq : (nq + 1) / 2;
+  g.total = g.X * a.N * g.Z;
+  return g;
+}
+// The r-th unit of CTA b out of P (snake order), or -1 past the end.
+__device__ __forceinline__ int unit_of(int r, int b, int P, int total) {
+  const int u = r * P + ((r & 1) ? (P - 1 - b) : b);
+  return u < total ? u : -1;
+}
+
+// The two slots of a unit: (query head, row tile) each, or an empty slot (qt < 0).
+struct Slots {
+  int h[2], qt[2], n;
+};
+__device__ __forceinline__ Slots unit_slots(const PrefillArgs& a, const Units& g, int u) {
   Slots sl;
-  const int G = a.Hq / a.Hkv;
-  if (G % 2 == 0) {            // grid (Hq/2, N, nq): the two heads of a pair, heaviest row tiles first
-    sl.h[0] = 2 * blockIdx.x; sl.h[1] = 2 * blockIdx.x + 1;
-    sl.qt[0] = sl.qt[1] = nq - 1 - (int)blockIdx.z;
-  } else {                     // grid (Hq, N, ceil(nq/2)): row tiles t and nq-1-t of one head
-    sl.h[0] = sl.h[1] = blockIdx.x;
-    sl.qt[0] = blockIdx.z;
-    sl.qt[1] = nq - 1 - (int)blockIdx.z;
+  const int nq = (a.S + BM - 1) / BM;
+  const int x = u % g.X, n = (u / g.X) % a.N, z = u / (g.X * a.N);
+  sl.n = n;
+  if ((a.Hq / a.Hkv) % 2 == 0) {   // the two heads of a pair, heaviest row tiles first
+    sl.h[0] = 2 * x; sl.h[1] = 2 * x + 1;
+    sl.qt[0] = sl.qt[1] = nq - 1 - z;
+  } else {                         // row tiles z and nq-1-z of one head
+    sl.h[0] = sl.h[1] = x;
+    sl.qt[0] = z;
+    sl.qt[1] = nq - 1 - z;
     if (sl.qt[1] == sl.qt[0]) sl.qt[1] = -1;
   }
   return sl;
@@ -148,6 +199,39 @@ __device__ __forceinline__ void tile_keys(const PrefillArgs& a, int i0, int i_la
   }
 }
 
+// Key tiles of each slot of a unit, [js0, js1), their union [j0, j1) and the tile walk.
+struct TileRanges {
+  int js0[2], js1[2], j0, j1;
+  bool act1;
+  __device__ __forceinline__ bool active(int s, int j) const {
+    return (s == 0 || act1) && j >= js0[s] && j < js1[s];
+  }
+  // Key tiles the CTA loads: those some slot needs, in increasing order (the two slots' ranges
+  // may be disjoint under a window mask).  Producer and MMA walk the same list; its entries
+  // number the ring stages and barrier phases.
+  __device__ __forceinline__ int next_tile(int j) const {
+    ++j;
+    while (j < j1 && !active(0, j) && !active(1, j)) ++j;
+    return j;
+  }
+  __device__ __forceinline__ int ntiles(int s) const { return (s == 0 || act1) ? js1[s] - js0[s] : 0; }
+};
+__device__ __forceinline__ TileRanges tile_ranges(const PrefillArgs& a, const Slots& sl) {
+  TileRanges tr;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    if (sl.qt[s] < 0) { tr.js0[s] = tr.js1[s] = 0; continue; }
+    const int i0 = sl.qt[s] * BM, i_last = min(a.S, i0 + BM) - 1;
+    int lo, hi;
+    tile_keys(a, i0, i_last, lo, hi);
+    tr.js0[s] = lo / BN; tr.js1[s] = (hi + BN - 1) / BN;
+  }
+  tr.act1 = sl.qt[1] >= 0;
+  tr.j0 = tr.act1 ? min(tr.js0[0], tr.js0[1]) : tr.js0[0];
+  tr.j1 = tr.act1 ? max(tr.js1[0], tr.js1[1]) : tr.js1[0];
+  return tr;
+}
+
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmK,
@@ -158,6 +242,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   constexpr int DN = DK;                      // MMA N extent of P V
   constexpr int KSTEPS = DK / 16;
   constexpr int NSUB = LY::NSUB;
+  constexpr int NCH = (D + 15) / 16;          // 16-column output chunks
   constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0, 0);
   constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, DN, 0, 1);
   static_assert(DN % 16 == 0 && DN <= 128, "N extent");
@@ -171,15 +256,16 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   uint64_t* p_full = bars + 6;     // [slot] P written to TMEM by the slot's 4 warps
   uint64_t* pv_done = bars + 8;    // [slot] P V of the slot's tile finished
   uint64_t* q_full = bars + 10;    // [slot] Q tile landed (TMA) or staged by the slot's 4 warps
-  uint64_t* mma_done = bars + 12;  // every MMA of the CTA completed
-  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* o_full = bars + 12;    // [slot] the unit's last P V done: O final in TMEM
+  uint64_t* o_free = bars + 14;    // [slot] O copied out of TMEM by the slot's 4 warps
+  uint64_t* q_free = bars + 16;    // the unit's last Q K^T done: both Q tiles may be replaced
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(bars + 17);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 18);
   const bool gather = a.row_of_slot != nullptr;   // permuted rows: threads stage Q and store O
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = blockIdx.y;
-  const int nq = (a.S + BM - 1) / BM;
-  const Slots sl = cta_slots(a, nq);
-  const int g = sl.h[0] / (a.Hq / a.Hkv);
+  const Units ug = unit_geometry(a);
+  const int P = gridDim.x, b = blockIdx.x;
 
   if (warp == MMA_WARP) tc::tmem_alloc(s_taddr, TMEM_COLS);
   if (tid == 0) {
@@ -187,8 +273,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       mbar_init(&kv_full[i], 1); mbar_init(&kv_free[i], 1); mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], SOFTMAX_WARPS / 2); mbar_init(&pv_done[i], 1);
       mbar_init(&q_full[i], gather ? SOFTMAX_WARPS / 2 : 1);
+      mbar_init(&o_full[i], 1); mbar_init(&o_free[i], SOFTMAX_WARPS / 2);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(q_free, 1);
+    *s_abort = 0;
     fence_mbar_init();
   }
   if (warp == TMA_WARP && lane == 0) {
@@ -198,143 +286,165 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_taddr;
-  griddep_wait();                              // inputs of this launch are complete from here on
-  griddep_launch_dependents();
-
-  // key tiles of each slot, [js0, js1), and their union [j0, j1)
-  int js0[2], js1[2];
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    if (sl.qt[s] < 0) { js0[s] = js1[s] = 0; continue; }
-    const int i0 = sl.qt[s] * BM, i_last = min(a.S, i0 + BM) - 1;
-    int lo, hi;
-    tile_keys(a, i0, i_last, lo, hi);
-    js0[s] = lo / BN; js1[s] = (hi + BN - 1) / BN;
-  }
-  const bool act1 = sl.qt[1] >= 0;
-  const int j0 = act1 ? min(js0[0], js0[1]) : js0[0];
-  const int j1 = act1 ? max(js1[0], js1[1]) : js1[0];
-  auto active = [&](int s, int j) { return (s == 0 || act1) && j >= js0[s] && j < js1[s]; };
-  // Key tiles the CTA loads: those some slot needs, in increasing order (the two slots' ranges
-  // may be disjoint under a window mask).  Producer and MMA walk the same list, numbering its
-  // entries it = 0, 1, ... for the ring stage and barrier phases.
-  auto next_tile = [&](int j) {
-    ++j;
-    while (j < j1 && !active(0, j) && !active(1, j)) ++j;
-    return j;
-  };
-
-
+  // Registers move from the control warpgroup to the softmax warpgroups (warpgroup-wide; each
+  // role's code follows its own setmaxnreg so the compiler budgets it with that count).
+  if (warp >= SOFTMAX_WARPS) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(REGS_CONTROL));
+    griddep_wait();                            // inputs of this launch are complete from here on
+    griddep_launch_dependents();
   if (warp == TMA_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      if (!gather) {
-        for (int s = 0; s < 2; ++s) {
-          if (s == 1 && !act1) break;
-          mbar_arrive_expect_tx(&q_full[s], NSUB * SUB);
-          for (int b = 0; b < NSUB; ++b)
-            tc::tma_load_4d(sm + LY::Q_OFF + (s * NSUB + b) * SUB, &tmQ, b * 64, sl.h[s], sl.qt[s] * BM, n, &q_full[s]);
+      bool ok = true;
+      int it = 0;                               // ring entries issued so far (all units)
+      int nu = 0;                               // units begun so far
+      for (int r = 0; ok; ++r, ++nu) {
+        const int u = unit_of(r, b, P, ug.total);
+        if (u < 0) break;
+        const Slots sl = unit_slots(a, ug, u);
+        const TileRanges tr = tile_ranges(a, sl);
+        if (!gather) {
+          // the previous unit's last Q K^T has read both Q tiles
+          if (nu > 0 && !mbar_wait_bounded(q_free, (uint32_t)((nu - 1) & 1))) { ok = false; break; }
+          for (int s = 0; s < 2; ++s) {
+            if (s == 1 && !tr.act1) break;
+            mbar_arrive_expect_tx(&q_full[s], NSUB * SUB);
+            for (int c = 0; c < NSUB; ++c)
+              tc::tma_load_4d(sm + LY::Q_OFF + (s * NSUB + c) * SUB, &tmQ, c * 64, sl.h[s], sl.qt[s] * BM, sl.n,
+                              &q_full[s]);
+          }
         }
-      }
-      int issued = 0;
-      for (int j = j0, it = 0; j < j1; j = next_tile(j), ++it) {
-        const int st = it % NSTAGE;
-        if (it >= NSTAGE && !mbar_wait_bounded(&kv_free[st], (uint32_t)((it / NSTAGE - 1) & 1))) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * NSUB * SUB);
-        const int key0 = j * BN;
-        for (int b = 0; b < NSUB; ++b) {
-          tc::tma_load_4d(sm + LY::K_OFF + (st * NSUB + b) * SUB, &tmK, b * 64, key0, g, n, &kv_full[st]);
-          tc::tma_load_4d(sm + LY::V_OFF + (st * NSUB + b) * SUB, &tmV, b * 64, key0, g, n, &kv_full[st]);
+        const int g = sl.h[0] / (a.Hq / a.Hkv);
+        for (int j = tr.j0; j < tr.j1; j = tr.next_tile(j), ++it) {
+          const int st = it % NSTAGE;
+          if (it >= NSTAGE && !mbar_wait_bounded(&kv_free[st], (uint32_t)((it / NSTAGE - 1) & 1))) { ok = false; break; }
+          mbar_arrive_expect_tx(&kv_full[st], 2 * NSUB * SUB);
+          const int key0 = j * BN;
+          for (int c = 0; c < NSUB; ++c) {
+            tc::tma_load_4d(sm + LY::K_OFF + (st * NSUB + c) * SUB, &tmK, c * 64, key0, g, sl.n, &kv_full[st]);
+            tc::tma_load_4d(sm + LY::V_OFF + (st * NSUB + c) * SUB, &tmV, c * 64, key0, g, sl.n, &kv_full[st]);
+          }
         }
-        issued = it + 1;
+        if (*s_abort) ok = false;
       }
+      if (!ok) *s_abort = 1;
       // the copies this CTA issued have normally landed long ago; never leave one in flight
-      for (int it = max(0, issued - NSTAGE); it < issued; ++it)
-        mbar_wait_bounded(&kv_full[it % NSTAGE], (uint32_t)((it / NSTAGE) & 1));
-      if (!gather) {
-        mbar_wait_bounded(&q_full[0], 0);
-        if (act1) mbar_wait_bounded(&q_full[1], 0);
-      }
+      for (int e = max(0, it - NSTAGE); e < it; ++e)
+        mbar_wait_bounded(&kv_full[e % NSTAGE], (uint32_t)((e / NSTAGE) & 1));
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = mbar_wait_bounded(&q_full[0], 0) && (!act1 || mbar_wait_bounded(&q_full[1], 0));
-      tc::fence_after_sync();
-      auto issue_s = [&](int s, int it) {
-        const int st = it % NSTAGE;
-        const uint32_t q_addr = smem_u32(sm + LY::Q_OFF + s * NSUB * SUB);
-        const uint32_t k_addr = smem_u32(sm + LY::K_OFF + st * NSUB * SUB);
-#pragma unroll
-        for (int k = 0; k < KSTEPS; ++k) {
-          const uint32_t off = (k >> 2) * SUB + (k & 3) * 32;
-          tc::mma_ss(tmem + s * BN, tc::desc_at(DESC_KMAJ, q_addr + off), tc::desc_at(DESC_KMAJ, k_addr + off),
-                     IDESC_S, k > 0);
-        }
-        tc::mma_commit(&s_full[s]);
-      };
-      if (ok) {
-        ok = mbar_wait_bounded(&kv_full[0], 0);
+      bool ok = true;
+      int it = 0;                               // ring entries consumed so far
+      int ks[2] = {0, 0};                       // key tiles of each slot so far
+      int nus[2] = {0, 0};                      // units in which each slot was active so far
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of(r, b, P, ug.total);
+        if (u < 0) break;
+        const Slots sl = unit_slots(a, ug, u);
+        const TileRanges tr = tile_ranges(a, sl);
+        const int s_total = tr.ntiles(0) + tr.ntiles(1);
+        int s_issued = 0;
+        ok = mbar_wait_bounded(&q_full[0], (uint32_t)(nus[0] & 1)) &&
+             (!tr.act1 || mbar_wait_bounded(&q_full[1], (uint32_t)(nus[1] & 1)));
         tc::fence_after_sync();
-        for (int s = 0; ok && s < 2; ++s)
-          if (active(s, j0)) issue_s(s, 0);
-      }
-      for (int j = j0, it = 0; ok && j < j1; ++it) {
-        const int st = it % NSTAGE;
-        const int jn = next_tile(j);                  // the tile loaded after j (entry it + 1)
-        bool next_landed = false;
-        for (int s = 0; ok && s < 2; ++s) {
-          if (active(s, j)) {
-            const int k = j - js0[s];
-            if (!mbar_wait_bounded(&p_full[s], (uint32_t)(k & 1))) { ok = false; break; }
-            tc::fence_after_sync();
-            const uint32_t v_addr = smem_u32(sm + LY::V_OFF + st * NSUB * SUB);
+        auto issue_s = [&](int s, int e) {
+          const int st = e % NSTAGE;
+          const uint32_t q_addr = smem_u32(sm + LY::Q_OFF + s * NSUB * SUB);
+          const uint32_t k_addr = smem_u32(sm + LY::K_OFF + st * NSUB * SUB);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              tc::mma_ts(tmem + 256 + s * 128, tmem + s * BN + kk * 8, tc::desc_at(DESC_VMN, v_addr + kk * 2048),
-                         IDESC_PV, (k > 0 || kk > 0));
-            tc::mma_commit(&pv_done[s]);
+          for (int k = 0; k < KSTEPS; ++k) {
+            const uint32_t off = (k >> 2) * SUB + (k & 3) * 32;
+            tc::mma_ss(tmem + s * BN, tc::desc_at(DESC_KMAJ, q_addr + off), tc::desc_at(DESC_KMAJ, k_addr + off),
+                       IDESC_S, k > 0);
           }
-          if (jn < j1 && active(s, jn)) {
-            if (!next_landed) {
-              if (!mbar_wait_bounded(&kv_full[(it + 1) % NSTAGE], (uint32_t)(((it + 1) / NSTAGE) & 1))) { ok = false; break; }
-              tc::fence_after_sync();
-              next_landed = true;
-            }
-            issue_s(s, it + 1);
-          }
+          tc::mma_commit(&s_full[s]);
+          if (++s_issued == s_total) tc::mma_commit(q_free);   // the unit's last Q K^T
+        };
+        if (ok) {
+          ok = mbar_wait_bounded(&kv_full[it % NSTAGE], (uint32_t)((it / NSTAGE) & 1));
+          tc::fence_after_sync();
+#pragma unroll
+          for (int s = 0; s < 2; ++s)
+            if (ok && tr.active(s, tr.j0)) issue_s(s, it);
         }
-        tc::mma_commit(&kv_free[st]);             // the stage is free once this tile's MMAs are done
-        j = jn;
+        for (int j = tr.j0; ok && j < tr.j1; ++it) {
+          const int st = it % NSTAGE;
+          const int jn = tr.next_tile(j);              // the tile loaded after j (entry it + 1)
+          bool next_landed = false;
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            if (!ok) continue;
+            if (tr.active(s, j)) {
+              const int k = j - tr.js0[s];
+              if (!mbar_wait_bounded(&p_full[s], (uint32_t)((ks[s] + k) & 1))) { ok = false; continue; }
+              // the first P V of a unit overwrites O: the previous unit's O must have been read
+              if (k == 0 && nus[s] > 0 && !mbar_wait_bounded(&o_free[s], (uint32_t)((nus[s] - 1) & 1))) { ok = false; continue; }
+              tc::fence_after_sync();
+              const uint32_t v_addr = smem_u32(sm + LY::V_OFF + st * NSUB * SUB);
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk)
+                tc::mma_ts(tmem + 256 + s * 128, tmem + s * BN + kk * 8, tc::desc_at(DESC_VMN, v_addr + kk * 2048),
+                           IDESC_PV, (k > 0 || kk > 0));
+              tc::mma_commit(&pv_done[s]);
+              if (j == tr.js1[s] - 1) tc::mma_commit(&o_full[s]);
+            }
+            if (jn < tr.j1 && tr.active(s, jn)) {
+              if (!next_landed) {
+                if (!mbar_wait_bounded(&kv_full[(it + 1) % NSTAGE], (uint32_t)(((it + 1) / NSTAGE) & 1))) { ok = false; continue; }
+                tc::fence_after_sync();
+                next_landed = true;
+              }
+              issue_s(s, it + 1);
+            }
+          }
+          tc::mma_commit(&kv_free[st]);             // the stage is free once this tile's MMAs are done
+          j = jn;
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          if (s == 0 || tr.act1) { ks[s] += tr.ntiles(s); ++nus[s]; }
+        if (*s_abort) ok = false;
       }
-      tc::mma_commit(mma_done);
+      if (!ok) *s_abort = 1;
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(REGS_SOFTMAX));
+    griddep_wait();
+    griddep_launch_dependents();
     // ------------------------------------------------------------ softmax warps
-    // warp w: slot s = w / 8, column half ch = (w / 4) % 2, TMEM lane quarter w % 4.  Thread
-    // (ch, t) owns columns [64 ch, 64 ch + 64) of row t; the two threads of a row trade their
-    // partial maxima (and at the end their partial sums) through shared memory.
-    const int s = warp >> 3;
-    const int ch = (warp >> 2) & 1;
-    const int t = (warp & 3) * 32 + lane;        // row within the tile = TMEM lane
-    __shared__ float s_pmax[2][2][2][BM];        // [tile parity][slot][half][row]
-    const int pair_bar = 1 + s * 4 + (warp & 3); // named barrier of warps w and w ^ 4 (64 threads)
-    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" :: "r"(pair_bar) : "memory"); };
-    if (s == 0 || act1) {
-      const int h = sl.h[s];
+    const int s = warp >> 2;                    // slot
+    const int quarter = warp & 3;               // TMEM lane quarter of this warp
+    const int t = quarter * 32 + lane;          // row within the tile = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_col = s * BN, o_col = 256 + s * 128;
+    uint8_t* stage = sm + LY::ST_OFF + warp * 2 * ST_BYTES;
+    uint8_t* sQ = sm + LY::Q_OFF + s * NSUB * SUB;
+    bool ok = true;
+    int ks = 0, nus = 0, nu = 0;                // tiles and active units of this slot, units begun
+    int r = 0;
+    for (; ok; ++r, ++nu) {
+      const int u = unit_of(r, b, P, ug.total);
+      if (u < 0) break;
+      const Slots sl = unit_slots(a, ug, u);
+      const TileRanges tr = tile_ranges(a, sl);
+      if (s == 1 && !tr.act1) continue;         // the slot is empty in this unit
+      const int h = sl.h[s], n = sl.n;
       const int i = sl.qt[s] * BM + t;
       const bool row_ok = i < a.S;
       int row = i;
-      if (row_ok && a.row_of_slot) row = a.row_of_slot[i];
+      if (row_ok && gather) row = a.row_of_slot[i];
       const bool row_valid = row_ok && row >= 0 && row < a.S;
-      // permuted rows: stage the Q row (this thread's half of the 16-byte chunks): chunk c
-      // (8 bf16) -> box c/8, swizzled position (c%8) ^ (t%8)
-      uint8_t* sQ = sm + LY::Q_OFF + s * NSUB * SUB;
       if (gather) {
+        // permuted rows: stage this thread's Q row once the previous unit's last Q K^T is done.
+        // Chunk c (8 bf16) -> box c/8, swizzled position (c%8) ^ (t%8)
+        if (nu > 0 && !__all_sync(FULL_MASK, mbar_wait_bounded(q_free, (uint32_t)((nu - 1) & 1)))) { ok = false; break; }
         const uint4* src = reinterpret_cast<const uint4*>(
             reinterpret_cast<const uint16_t*>(a.q) + (((int64_t)n * a.S + row) * a.Hq + h) * D);
 #pragma unroll
-        for (int c = ch; c < DK / 8; c += 2) {
+        for (int c = 0; c < DK / 8; ++c) {
           uint4 v = make_uint4(0, 0, 0, 0);
           if (row_valid && c < D / 8) v = __ldg(src + c);
           uint8_t* dst = sQ + (c >> 3) * SUB + (t >> 3) * 1024 + (t & 7) * 128 + (((c & 7) ^ (t & 7)) << 4);
@@ -353,70 +463,68 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         else if (a.mask == KVA_MASK_CAUSAL_SEGMENT) { rlo = 0; rhi = seg_upper_tc(a.segment, a.S, a.segment[i]); }
         else { const int sg = a.segment[i]; rlo = seg_lower_tc(a.segment, a.S, sg); rhi = seg_upper_tc(a.segment, a.S, sg); }
       }
-      const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      const uint32_t s_col = s * BN, o_col = 256 + s * 128;
-      const int nk = js1[s] - js0[s];
-      float m = -INFINITY, l = 0.f;             // l: this thread's half of the row sum
-      bool ok = true;
+      const int nk = tr.ntiles(s);
+      float m = -INFINITY, l = 0.f;
+      float x[128];
       for (int k = 0; k < nk; ++k) {
-        const int kv0 = (js0[s] + k) * BN + ch * 64;     // first key of this thread's columns
+        const int kk = ks + k;
+        const int kv0 = (tr.js0[s] + k) * BN;          // first key of the tile
         // every lane waits; the vote keeps the warp converged for the .aligned TMEM accesses
-        if (!__all_sync(FULL_MASK, mbar_wait_bounded(&s_full[s], (uint32_t)(k & 1)))) { ok = false; break; }
+        if (!__all_sync(FULL_MASK, mbar_wait_bounded(&s_full[s], (uint32_t)(kk & 1)))) { ok = false; break; }
         tc::fence_after_sync();
-        float x[64];
         {
-          uint32_t r0[32], r1[32];
-          tc::tmem_ld32(lane_base + s_col + ch * 64, r0);
-          tc::tmem_ld32(lane_base + s_col + ch * 64 + 32, r1);
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tc::tmem_ld32(lane_base + s_col, r0);
+          tc::tmem_ld32(lane_base + s_col + 32, r1);
+          tc::tmem_ld32(lane_base + s_col + 64, r2);
+          tc::tmem_ld32(lane_base + s_col + 96, r3);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) { x[e] = __uint_as_float(r0[e]); x[32 + e] = __uint_as_float(r1[e]); }
+          for (int e = 0; e < 32; ++e) {
+            x[e] = __uint_as_float(r0[e]); x[32 + e] = __uint_as_float(r1[e]);
+            x[64 + e] = __uint_as_float(r2[e]); x[96 + e] = __uint_as_float(r3[e]);
+          }
         }
-        // visible columns of this thread's 64 for this row: [clo, chi)
+        // visible columns of this row in the tile: [clo, chi)
         const int clo = rlo - kv0, chi = rhi - kv0;
-        if (clo > 0 || chi < 64) {
+        if (clo > 0 || chi < BN) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
+          for (int e = 0; e < BN; ++e)
             if (e < clo || e >= chi) x[e] = -INFINITY;
         }
         float mr = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) mr = fmax3(mr, x[e], x[e + 1]);
-        // the row max over both halves (the barrier also means both threads hold their S, so
-        // P may now overwrite it: half 1's P columns [32, 64) hold half 0's scores)
-        s_pmax[k & 1][s][ch][t] = mr;
-        pair_sync();
-        mr = fmaxf(mr, s_pmax[k & 1][s][ch ^ 1][t]);
+        for (int e = 0; e < BN; e += 2) mr = fmax3(mr, x[e], x[e + 1]);
         const float m_tile = mr == -INFINITY ? -INFINITY : mr * a.scale_log2;
         const float m_new = fmaxf(m, m_tile);
         const bool first = (m == -INFINITY);            // first visible keys: O holds nothing yet
         const bool grow = !first && m_new > m + RESCALE_LOG2;
         if (first) m = m_new;
         if (__any_sync(FULL_MASK, grow)) {
-          // some row's max grew by > 2^8: rescale those rows of O (this thread's 16-column
-          // chunks of it) once P V of the previous tile has landed.  The whole warp takes part
-          // (TMEM accesses are warp-collective); rows that need no rescale use alpha = 1.
-          if (!__all_sync(FULL_MASK, mbar_wait_bounded(&pv_done[s], (uint32_t)((k - 1) & 1)))) { ok = false; break; }
+          // some row's max grew by > 2^8: rescale those rows of O once P V of the previous tile
+          // has landed.  The whole warp takes part (TMEM accesses are warp-collective); rows
+          // that need no rescale use alpha = 1.
+          if (!__all_sync(FULL_MASK, mbar_wait_bounded(&pv_done[s], (uint32_t)((kk - 1) & 1)))) { ok = false; break; }
           tc::fence_after_sync();
           const float alpha = grow ? ex2(m - m_new) : 1.0f;
 #pragma unroll
-          for (int c = ch; c < DN / 16; c += 2) {
-            uint32_t r[16];
-            tmem_ld16(lane_base + o_col + c * 16, r);
+          for (int c = 0; c < DN / 16; ++c) {
+            uint32_t rr[16];
+            tmem_ld16(lane_base + o_col + c * 16, rr);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st16(lane_base + o_col + c * 16, r);
+            for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+            tmem_st16(lane_base + o_col + c * 16, rr);
           }
           tc::tmem_wait_st();
           if (grow) { l *= alpha; m = m_new; }
         }
-        // P = exp2(S * scale - m) as packed bf16 into columns [32 ch, 32 ch + 32) of the slot
+        // P = exp2(S * scale - m) as packed bf16 into columns [0, 64) of the slot
         const float mref = (m == -INFINITY) ? 0.f : m;
         const uint64_t sc2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
         uint64_t lsum = f2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -426,7 +534,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
             lsum = fadd2(lsum, f2(p0, p1));
             w[e] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(lane_base + s_col + ch * 32 + c * 16, w);
+          tmem_st16(lane_base + s_col + c * 16, w);
         }
         float l0, l1;
         f2split(lsum, l0, l1);
@@ -436,68 +544,71 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[s]);
       }
-      // the row sum over both halves
-      s_pmax[nk & 1][s][ch][t] = l;
-      pair_sync();
-      const float l_row = l + s_pmax[nk & 1][s][ch ^ 1][t];
+      if (!ok) break;
+      // epilogue: copy O out of TMEM (freeing it for the next unit's first P V), then O / l
+      if (!__all_sync(FULL_MASK, mbar_wait_bounded(&o_full[s], (uint32_t)(nus & 1)))) { ok = false; break; }
+      tc::fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < DN / 16; ++c) tmem_ld16f(lane_base + o_col + c * 16, x + 16 * c);
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[s]);
+      const float inv = l > 0.f ? 1.0f / l : NAN;
       if (!gather) {
-        // epilogue: once every MMA of the CTA is done, the rings and Q tiles are free: O / l goes
-        // through shared memory (per 32-column box: 128 rows of 128 bytes, 128-byte swizzled)
-        // and out with TMA stores, which also clip rows past the sequence.  Thread half ch
-        // stages boxes ch, ch + 2, ...
-        constexpr int NBOX = (D + 31) / 32;
-        if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(mma_done, 0));
-        tc::fence_after_sync();
-        const float inv = (ok && l_row > 0.f) ? 1.0f / l_row : NAN;
-        uint8_t* stage = sm + s * NBOX * (BM * 128);
+        // 16-column chunks through this warp's two staging tiles (32 rows x 64 bytes, 64-byte
+        // swizzle: 16-byte chunk k of row r sits at position k ^ ((r >> 1) & 3)); TMA stores
+        // clip rows past the sequence.
+        const int row0 = sl.qt[s] * BM + quarter * 32;
 #pragma unroll
-        for (int b = ch; b < NBOX; b += 2) {
+        for (int c = 0; c < NCH; ++c) {
+          uint8_t* buf = stage + (c & 1) * ST_BYTES;
+          // this buffer's previous store has read it (c = 0: every store of the previous unit)
+          if (lane == 0 && c != 1) bulk_wait_read(c == 0 ? 0 : 1);
+          __syncwarp();
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t r[16];
-            tmem_ld16(lane_base + o_col + b * 32 + hf * 16, r);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int chunk = hf * 4 + q4;
-              *reinterpret_cast<float4*>(stage + b * (BM * 128) + t * 128 + ((chunk ^ (t & 7)) << 4)) =
-                  make_float4(__uint_as_float(r[4 * q4]) * inv, __uint_as_float(r[4 * q4 + 1]) * inv,
-                              __uint_as_float(r[4 * q4 + 2]) * inv, __uint_as_float(r[4 * q4 + 3]) * inv);
-            }
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float* xs = x + 16 * c + 4 * k4;
+            *reinterpret_cast<float4*>(buf + lane * 64 + ((k4 ^ ((lane >> 1) & 3)) << 4)) =
+                make_float4(xs[0] * inv, xs[1] * inv, xs[2] * inv, xs[3] * inv);
           }
-        }
-        fence_proxy_async_smem();
-        asm volatile("bar.sync %0, 256;" :: "r"(9 + s) : "memory");        // the slot's 8 warps
-        if (ch == 0 && t == 0) {
-          for (int b = 0; b < NBOX; ++b) tc::tma_store_4d(&tmO, stage + b * (BM * 128), b * 32, h, sl.qt[s] * BM, n);
-          tc::bulk_commit_group();
-          tc::bulk_wait_read_all();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < a.S) {
+            tc::tma_store_4d(&tmO, buf, c * 16, h, row0, n);
+            tc::bulk_commit_group();
+          }
         }
       } else {
-        // epilogue, permuted rows: O / l -> token-order output row from each thread (its 16-column
-        // chunks).  The TMEM loads are warp-collective, so every lane loads; only rows inside the
-        // sequence store.
-        if (ok && nk > 0) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&pv_done[s], (uint32_t)((nk - 1) & 1)));
-        tc::fence_after_sync();
-        float* o = a.out + (((int64_t)n * a.S + (row_valid ? row : 0)) * a.Hq + h) * D;
-        const float inv = (ok && l_row > 0.f) ? 1.0f / l_row : NAN;
+        // permuted rows: O / l -> the token-order output row, written by each thread
+        if (row_valid) {
+          float* o = a.out + (((int64_t)n * a.S + row) * a.Hq + h) * D;
 #pragma unroll
-        for (int c = ch; c < DN / 16; c += 2) {
-          uint32_t r[16];
-          tmem_ld16(lane_base + o_col + c * 16, r);
-          tc::tmem_wait_ld();
-          if (row_valid) {
-#pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-              const int d = c * 16 + e;
-              if (d < D)
-                *reinterpret_cast<float4*>(o + d) = make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
-                                                                __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
-            }
-          }
+          for (int d = 0; d < DN; d += 4)
+            if (d < D) *reinterpret_cast<float4*>(o + d) = make_float4(x[d] * inv, x[d + 1] * inv, x[d + 2] * inv, x[d + 3] * inv);
         }
       }
+      ks += nk;
+      ++nus;
+      if (*s_abort) { ok = false; break; }
     }
+    if (!ok) {
+      *s_abort = 1;
+      // a wait gave up: this CTA's unfinished rows of this slot become NaN (plain stores)
+      for (;; ++r) {
+        const int u = unit_of(r, b, P, ug.total);
+        if (u < 0) break;
+        const Slots sl = unit_slots(a, ug, u);
+        if (sl.qt[s] < 0) continue;
+        const int i = sl.qt[s] * BM + t;
+        if (i >= a.S) continue;
+        const int row = gather ? a.row_of_slot[i] : i;
+        if (row < 0 || row >= a.S) continue;
+        float* o = a.out + (((int64_t)sl.n * a.S + row) * a.Hq + sl.h[s]) * D;
+        for (int d = 0; d < D; ++d) o[d] = NAN;
+      }
+    }
+    if (lane == 0) bulk_wait_all();             // every TMA store of this warp has completed
   }
 
   tc::fence_before_sync();
@@ -540,16 +651,16 @@ cudaError_t make_q_map(CUtensorMap* map, const PrefillArgs& a) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// out [N, S, Hq, D] fp32 as (D, Hq, S, N): stores of [128 rows x 32 columns] boxes.
+// out [N, S, Hq, D] fp32 as (D, Hq, S, N): stores of [32 rows x 16 columns] boxes (64-byte swizzle).
 cudaError_t make_out_map(CUtensorMap* map, const PrefillArgs& a) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[4] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq, (cuuint64_t)a.S, (cuuint64_t)a.N};
   const cuuint64_t strides[3] = {(cuuint64_t)a.D * 4, (cuuint64_t)a.Hq * a.D * 4, (cuuint64_t)a.S * a.Hq * a.D * 4};
-  const cuuint32_t box[4] = {32, 1, BM, 1};
+  const cuuint32_t box[4] = {16, 1, 32, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.out, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -568,13 +679,31 @@ cudaError_t make_cache_map(CUtensorMap* map, const void* base, const PrefillArgs
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+int prefill_num_sms() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (n[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    n[dev] = v;
+  }
+  return n[dev];
+}
+
 template <int D>
 cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   constexpr int SMEM = Layout<D>::SMEM;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
+    // the register split assumes the launch holds exactly REGS_LAUNCH per thread: with fewer,
+    // the softmax warpgroups' setmaxnreg.inc could never be satisfied
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>)) != cudaSuccess) return e;
+    if (fa.numRegs != REGS_LAUNCH) return cudaErrorInvalidDeviceFunction;
     configured = true;
   }
   CUtensorMap mk, mv, mq, mo;
@@ -583,11 +712,14 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   if ((e = make_cache_map(&mv, a.vc, a)) != cudaSuccess) return e;
   if ((e = make_q_map(&mq, a)) != cudaSuccess) return e;
   if ((e = make_out_map(&mo, a)) != cudaSuccess) return e;
+  // units: the two heads of a GQA pair at one row tile, else two row tiles of one head
   const int nq = (a.S + BM - 1) / BM;
   const int G = a.Hq / a.Hkv;
-  // slots: the two heads of a GQA pair (heaviest row tiles launched first), else two row tiles
-  const dim3 grid = (G % 2 == 0) ? dim3(a.Hq / 2, a.N, nq) : dim3(a.Hq, a.N, (nq + 1) / 2);
-  return launch_pdl(prefill_tc_kernel<D>, grid, dim3(THREADS), (size_t)SMEM, s, a, mk, mv, mq, mo);
+  const long long units = (G % 2 == 0) ? (long long)(a.Hq / 2) * a.N * nq : (long long)a.Hq * a.N * ((nq + 1) / 2);
+  if (units <= 0) return cudaSuccess;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int grid = (int)std::min<long long>(units, prefill_num_sms());
+  return launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, a, mk, mv, mq, mo);
 }
 
 }  // namespace
