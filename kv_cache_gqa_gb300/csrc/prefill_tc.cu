@@ -16,11 +16,12 @@
 //              bf16 pairs.  O is rescaled only when the row max grows by more than 2^8 (the
 //              stale max keeps every P <= 256).  At the end of a unit it copies O out of
 //              TMEM (which frees it for the next unit's P V), divides by the row sum and
-//              writes the rows through a double-buffered 32 x 16 staging tile per warp with
-//              TMA stores.
+//              writes the rows in 16-column chunks transposed through a 32 x 16 staging tile
+//              per warp, so each store instruction covers 8 rows x 64 contiguous bytes.
 //   warp 8     TMA producer: per unit the slots' Q tiles (once the previous unit's last
 //              Q K^T has read its Q), then K and V tiles (64-column, 128-byte swizzled boxes)
-//              into a 2-stage ring that runs on across units; rows past the valid keys read
+//              into 2-stage K and V rings that run on across units (a K stage frees as soon
+//              as its Q K^T is done, a V stage after its P V); rows past the valid keys read
 //              as zeros.
 //   warp 9     MMA issuer (one thread).  TMEM: S of slot s at columns [128 s, 128 s + 128),
 //              O of slot s at [256 + 128 s, ...).  Per key tile j it issues, for s = 0, 1:
@@ -52,9 +53,9 @@ constexpr int SOFTMAX_WARPS = 8;          // 4 per slot, one row per thread
 constexpr int TMA_WARP = 8, MMA_WARP = 9;  // warps 10, 11 complete their warpgroup and idle
 constexpr int THREADS = 384;
 // Registers per thread: 168 at launch (65536 / 384, rounded down to a multiple of 8); the
-// producer/MMA warpgroup gives up 64 per thread, which the two softmax warpgroups take:
-// 128 * (200 + 200 + 104) = 384 * 168, so the increase never waits on registers nobody frees.
-constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 200, REGS_CONTROL = 104;
+// producer/MMA warpgroup gives up 48 per thread, which the two softmax warpgroups take:
+// 128 * (192 + 192 + 120) = 384 * 168, so the increase never waits on registers nobody frees.
+constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 192, REGS_CONTROL = 120;
 static_assert(2 * REGS_SOFTMAX + REGS_CONTROL <= 3 * REGS_LAUNCH, "register split exceeds the launch total");
 static_assert(REGS_LAUNCH * THREADS <= 65536, "launch registers");
 constexpr int SUB = BM * 128;             // bytes of one [128 rows x 64 bf16] swizzled box
@@ -134,17 +135,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// Two floats to packed bf16 (round to nearest even) in one instruction: lo in bits 0..15.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ void bulk_wait_read(int pending) {   // pending: 0 or 1 (immediate)
-  if (pending == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-  else asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Unit geometry: units are numbered x fastest (KV-head pair or head), then instance, then
 // the row-tile index z, with z = 0 the heaviest causal tiles.
 struct Units {
@@ -235,8 +236,7 @@ __device__ __forceinline__ TileRanges tile_ranges(const PrefillArgs& a, const Sl
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ,
-                  const __grid_constant__ CUtensorMap tmO) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ) {
   using LY = Layout<D>;
   constexpr int DK = (D + 15) / 16 * 16;      // MMA K extent of Q K^T (zero padded)
   constexpr int DN = DK;                      // MMA N extent of P V
@@ -250,17 +250,19 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::BAR_OFF);
-  uint64_t* kv_full = bars + 0;    // [NSTAGE] K, V tile landed
-  uint64_t* kv_free = bars + 2;    // [NSTAGE] both slots' P V of the tile done: stage free
-  uint64_t* s_full = bars + 4;     // [slot] S ready in TMEM
-  uint64_t* p_full = bars + 6;     // [slot] P written to TMEM by the slot's 4 warps
-  uint64_t* pv_done = bars + 8;    // [slot] P V of the slot's tile finished
-  uint64_t* q_full = bars + 10;    // [slot] Q tile landed (TMA) or staged by the slot's 4 warps
-  uint64_t* o_full = bars + 12;    // [slot] the unit's last P V done: O final in TMEM
-  uint64_t* o_free = bars + 14;    // [slot] O copied out of TMEM by the slot's 4 warps
-  uint64_t* q_free = bars + 16;    // the unit's last Q K^T done: both Q tiles may be replaced
-  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(bars + 17);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 18);
+  uint64_t* k_full = bars + 0;     // [NSTAGE] K tile landed
+  uint64_t* k_free = bars + 2;     // [NSTAGE] both slots' Q K^T of the tile done: K stage free
+  uint64_t* v_full = bars + 4;     // [NSTAGE] V tile landed
+  uint64_t* v_free = bars + 6;     // [NSTAGE] both slots' P V of the tile done: V stage free
+  uint64_t* s_full = bars + 8;     // [slot] S ready in TMEM
+  uint64_t* p_full = bars + 10;    // [slot] P written to TMEM by the slot's 4 warps
+  uint64_t* pv_done = bars + 12;   // [slot] P V of the slot's tile finished
+  uint64_t* q_full = bars + 14;    // [slot] Q tile landed (TMA) or staged by the slot's 4 warps
+  uint64_t* o_full = bars + 16;    // [slot] the unit's last P V done: O final in TMEM
+  uint64_t* o_free = bars + 18;    // [slot] O copied out of TMEM by the slot's 4 warps
+  uint64_t* q_free = bars + 20;    // the unit's last Q K^T done: both Q tiles may be replaced
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(bars + 21);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 22);
   const bool gather = a.row_of_slot != nullptr;   // permuted rows: threads stage Q and store O
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -270,7 +272,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   if (warp == MMA_WARP) tc::tmem_alloc(s_taddr, TMEM_COLS);
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1); mbar_init(&kv_free[i], 1); mbar_init(&s_full[i], 1);
+      mbar_init(&k_full[i], 1); mbar_init(&k_free[i], 1); mbar_init(&v_full[i], 1); mbar_init(&v_free[i], 1);
+      mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], SOFTMAX_WARPS / 2); mbar_init(&pv_done[i], 1);
       mbar_init(&q_full[i], gather ? SOFTMAX_WARPS / 2 : 1);
       mbar_init(&o_full[i], 1); mbar_init(&o_free[i], SOFTMAX_WARPS / 2);
@@ -280,7 +283,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     fence_mbar_init();
   }
   if (warp == TMA_WARP && lane == 0) {
-    tc::tma_prefetch_desc(&tmK); tc::tma_prefetch_desc(&tmV); tc::tma_prefetch_desc(&tmQ); tc::tma_prefetch_desc(&tmO);
+    tc::tma_prefetch_desc(&tmK); tc::tma_prefetch_desc(&tmV); tc::tma_prefetch_desc(&tmQ);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -303,6 +306,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         if (u < 0) break;
         const Slots sl = unit_slots(a, ug, u);
         const TileRanges tr = tile_ranges(a, sl);
+        const int g = sl.h[0] / (a.Hq / a.Hkv);
         if (!gather) {
           // the previous unit's last Q K^T has read both Q tiles
           if (nu > 0 && !mbar_wait_bounded(q_free, (uint32_t)((nu - 1) & 1))) { ok = false; break; }
@@ -314,28 +318,41 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
                               &q_full[s]);
           }
         }
-        const int g = sl.h[0] / (a.Hq / a.Hkv);
         for (int j = tr.j0; j < tr.j1; j = tr.next_tile(j), ++it) {
+          // K and V of a tile use separate stages: K is free again once both slots' Q K^T have
+          // run (early in the tile), V only after both P V
           const int st = it % NSTAGE;
-          if (it >= NSTAGE && !mbar_wait_bounded(&kv_free[st], (uint32_t)((it / NSTAGE - 1) & 1))) { ok = false; break; }
-          mbar_arrive_expect_tx(&kv_full[st], 2 * NSUB * SUB);
+          const uint32_t ph = (uint32_t)((it / NSTAGE - 1) & 1);
           const int key0 = j * BN;
-          for (int c = 0; c < NSUB; ++c) {
-            tc::tma_load_4d(sm + LY::K_OFF + (st * NSUB + c) * SUB, &tmK, c * 64, key0, g, sl.n, &kv_full[st]);
-            tc::tma_load_4d(sm + LY::V_OFF + (st * NSUB + c) * SUB, &tmV, c * 64, key0, g, sl.n, &kv_full[st]);
-          }
+          if (it >= NSTAGE && !mbar_wait_bounded(&k_free[st], ph)) { ok = false; break; }
+          mbar_arrive_expect_tx(&k_full[st], NSUB * SUB);
+          for (int c = 0; c < NSUB; ++c)
+            tc::tma_load_4d(sm + LY::K_OFF + (st * NSUB + c) * SUB, &tmK, c * 64, key0, g, sl.n, &k_full[st]);
+          if (it >= NSTAGE && !mbar_wait_bounded(&v_free[st], ph)) { ok = false; break; }
+          mbar_arrive_expect_tx(&v_full[st], NSUB * SUB);
+          for (int c = 0; c < NSUB; ++c)
+            tc::tma_load_4d(sm + LY::V_OFF + (st * NSUB + c) * SUB, &tmV, c * 64, key0, g, sl.n, &v_full[st]);
         }
         if (*s_abort) ok = false;
       }
       if (!ok) *s_abort = 1;
       // the copies this CTA issued have normally landed long ago; never leave one in flight
-      for (int e = max(0, it - NSTAGE); e < it; ++e)
-        mbar_wait_bounded(&kv_full[e % NSTAGE], (uint32_t)((e / NSTAGE) & 1));
+      for (int e = max(0, it - NSTAGE); e < it; ++e) {
+        mbar_wait_bounded(&k_full[e % NSTAGE], (uint32_t)((e / NSTAGE) & 1));
+        mbar_wait_bounded(&v_full[e % NSTAGE], (uint32_t)((e / NSTAGE) & 1));
+      }
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
+      static_assert(NSTAGE == 2, "descriptor selection assumes two stages");
+      const uint64_t q_desc0 = tc::desc_at(DESC_KMAJ, smem_u32(sm + LY::Q_OFF));
+      const uint64_t q_desc1 = tc::desc_at(DESC_KMAJ, smem_u32(sm + LY::Q_OFF + NSUB * SUB));
+      const uint64_t k_desc0 = tc::desc_at(DESC_KMAJ, smem_u32(sm + LY::K_OFF));
+      const uint64_t k_desc1 = tc::desc_at(DESC_KMAJ, smem_u32(sm + LY::K_OFF + NSUB * SUB));
+      const uint64_t v_desc0 = tc::desc_at(DESC_VMN, smem_u32(sm + LY::V_OFF));
+      const uint64_t v_desc1 = tc::desc_at(DESC_VMN, smem_u32(sm + LY::V_OFF + NSUB * SUB));
       int it = 0;                               // ring entries consumed so far
       int ks[2] = {0, 0};                       // key tiles of each slot so far
       int nus[2] = {0, 0};                      // units in which each slot was active so far
@@ -350,56 +367,62 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
              (!tr.act1 || mbar_wait_bounded(&q_full[1], (uint32_t)(nus[1] & 1)));
         tc::fence_after_sync();
         auto issue_s = [&](int s, int e) {
-          const int st = e % NSTAGE;
-          const uint32_t q_addr = smem_u32(sm + LY::Q_OFF + s * NSUB * SUB);
-          const uint32_t k_addr = smem_u32(sm + LY::K_OFF + st * NSUB * SUB);
+          const uint64_t qd = s ? q_desc1 : q_desc0;
+          const uint64_t kd = (e & 1) ? k_desc1 : k_desc0;
 #pragma unroll
           for (int k = 0; k < KSTEPS; ++k) {
-            const uint32_t off = (k >> 2) * SUB + (k & 3) * 32;
-            tc::mma_ss(tmem + s * BN, tc::desc_at(DESC_KMAJ, q_addr + off), tc::desc_at(DESC_KMAJ, k_addr + off),
-                       IDESC_S, k > 0);
+            // descriptor start addresses advance by constant offsets (addresses stay below 2^18)
+            const uint64_t off = (uint64_t)((((k >> 2) * SUB) + (k & 3) * 32) >> 4);
+            tc::mma_ss(tmem + s * BN, qd + off, kd + off, IDESC_S, k > 0);
           }
           tc::mma_commit(&s_full[s]);
           if (++s_issued == s_total) tc::mma_commit(q_free);   // the unit's last Q K^T
         };
         if (ok) {
-          ok = mbar_wait_bounded(&kv_full[it % NSTAGE], (uint32_t)((it / NSTAGE) & 1));
+          ok = mbar_wait_bounded(&k_full[it % NSTAGE], (uint32_t)((it / NSTAGE) & 1));
           tc::fence_after_sync();
 #pragma unroll
           for (int s = 0; s < 2; ++s)
             if (ok && tr.active(s, tr.j0)) issue_s(s, it);
+          tc::mma_commit(&k_free[it % NSTAGE]);         // this K stage is free once those finish
         }
         for (int j = tr.j0; ok && j < tr.j1; ++it) {
           const int st = it % NSTAGE;
           const int jn = tr.next_tile(j);              // the tile loaded after j (entry it + 1)
-          bool next_landed = false;
+          bool next_landed = false, v_landed = false;
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             if (!ok) continue;
             if (tr.active(s, j)) {
               const int k = j - tr.js0[s];
               if (!mbar_wait_bounded(&p_full[s], (uint32_t)((ks[s] + k) & 1))) { ok = false; continue; }
+              if (!v_landed) {
+                if (!mbar_wait_bounded(&v_full[st], (uint32_t)((it / NSTAGE) & 1))) { ok = false; continue; }
+                v_landed = true;
+              }
               // the first P V of a unit overwrites O: the previous unit's O must have been read
               if (k == 0 && nus[s] > 0 && !mbar_wait_bounded(&o_free[s], (uint32_t)((nus[s] - 1) & 1))) { ok = false; continue; }
               tc::fence_after_sync();
-              const uint32_t v_addr = smem_u32(sm + LY::V_OFF + st * NSUB * SUB);
+              const uint64_t vd = st ? v_desc1 : v_desc0;
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk)
-                tc::mma_ts(tmem + 256 + s * 128, tmem + s * BN + kk * 8, tc::desc_at(DESC_VMN, v_addr + kk * 2048),
+                tc::mma_ts(tmem + 256 + s * 128, tmem + s * BN + kk * 8, vd + (uint64_t)(kk * 2048 >> 4),
                            IDESC_PV, (k > 0 || kk > 0));
               tc::mma_commit(&pv_done[s]);
               if (j == tr.js1[s] - 1) tc::mma_commit(&o_full[s]);
             }
             if (jn < tr.j1 && tr.active(s, jn)) {
               if (!next_landed) {
-                if (!mbar_wait_bounded(&kv_full[(it + 1) % NSTAGE], (uint32_t)(((it + 1) / NSTAGE) & 1))) { ok = false; continue; }
+                if (!mbar_wait_bounded(&k_full[(it + 1) % NSTAGE], (uint32_t)(((it + 1) / NSTAGE) & 1))) { ok = false; continue; }
                 tc::fence_after_sync();
                 next_landed = true;
               }
               issue_s(s, it + 1);
             }
           }
-          tc::mma_commit(&kv_free[st]);             // the stage is free once this tile's MMAs are done
+          if (!ok) break;
+          tc::mma_commit(&v_free[st]);              // V of this tile: free once both P V are done
+          if (jn < tr.j1) tc::mma_commit(&k_free[(it + 1) % NSTAGE]);   // K of the next: after its Q K^T
           j = jn;
         }
 #pragma unroll
@@ -492,9 +515,15 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           for (int e = 0; e < BN; ++e)
             if (e < clo || e >= chi) x[e] = -INFINITY;
         }
-        float mr = -INFINITY;
+        // row max: four independent chains, then combined (a single chain would serialise 64
+        // dependent max instructions)
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int e = 0; e < BN; e += 2) mr = fmax3(mr, x[e], x[e + 1]);
+        for (int e = 0; e < BN; e += 8) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mq[c] = fmax3(mq[c], x[e + 2 * c], x[e + 2 * c + 1]);
+        }
+        const float mr = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
         const float m_tile = mr == -INFINITY ? -INFINITY : mr * a.scale_log2;
         const float m_new = fmaxf(m, m_tile);
         const bool first = (m == -INFINITY);            // first visible keys: O holds nothing yet
@@ -532,7 +561,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
             f2split(ffma2(f2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), sc2, nm2), x0, x1);
             const float p0 = ex2(x0), p1 = ex2(x1);         // hidden keys hold -inf: exp2 -> 0
             lsum = fadd2(lsum, f2(p0, p1));
-            w[e] = pack_bf16x2(p0, p1);
+            w[e] = cvt_bf16x2(p0, p1);
           }
           tmem_st16(lane_base + s_col + c * 16, w);
         }
@@ -555,37 +584,35 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[s]);
       const float inv = l > 0.f ? 1.0f / l : NAN;
-      if (!gather) {
-        // 16-column chunks through this warp's two staging tiles (32 rows x 64 bytes, 64-byte
-        // swizzle: 16-byte chunk k of row r sits at position k ^ ((r >> 1) & 3)); TMA stores
-        // clip rows past the sequence.
-        const int row0 = sl.qt[s] * BM + quarter * 32;
+      // O / l goes out in 16-column chunks, transposed through this warp's staging tile so that
+      // every store instruction writes 8 rows x 64 contiguous bytes: lane r writes its row's
+      // chunk (16-byte piece k at position k ^ ((r >> 1) & 3), conflict-free), then lane
+      // 4 j + q stores piece q of rows j, j + 8, j + 16, j + 24.  Rows outside the sequence
+      // (and, for permuted rows, their token-order destination) are resolved per row.
+      {
+        const int my_row = row_valid ? row : -1;
+        float* orow[4];
+#pragma unroll
+        for (int p4 = 0; p4 < 4; ++p4) {
+          const int rr = __shfl_sync(FULL_MASK, my_row, (lane >> 2) + 8 * p4);
+          orow[p4] = rr < 0 ? nullptr : a.out + (((int64_t)n * a.S + rr) * a.Hq + h) * D + (lane & 3) * 4;
+        }
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
           uint8_t* buf = stage + (c & 1) * ST_BYTES;
-          // this buffer's previous store has read it (c = 0: every store of the previous unit)
-          if (lane == 0 && c != 1) bulk_wait_read(c == 0 ? 0 : 1);
-          __syncwarp();
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const float* xs = x + 16 * c + 4 * k4;
             *reinterpret_cast<float4*>(buf + lane * 64 + ((k4 ^ ((lane >> 1) & 3)) << 4)) =
                 make_float4(xs[0] * inv, xs[1] * inv, xs[2] * inv, xs[3] * inv);
           }
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && row0 < a.S) {
-            tc::tma_store_4d(&tmO, buf, c * 16, h, row0, n);
-            tc::bulk_commit_group();
-          }
-        }
-      } else {
-        // permuted rows: O / l -> the token-order output row, written by each thread
-        if (row_valid) {
-          float* o = a.out + (((int64_t)n * a.S + row) * a.Hq + h) * D;
 #pragma unroll
-          for (int d = 0; d < DN; d += 4)
-            if (d < D) *reinterpret_cast<float4*>(o + d) = make_float4(x[d] * inv, x[d + 1] * inv, x[d + 2] * inv, x[d + 3] * inv);
+          for (int p4 = 0; p4 < 4; ++p4) {
+            const int rr = (lane >> 2) + 8 * p4, q = lane & 3;
+            const float4 v = *reinterpret_cast<const float4*>(buf + rr * 64 + ((q ^ ((rr >> 1) & 3)) << 4));
+            if (orow[p4] != nullptr && c * 16 + q * 4 < D) *reinterpret_cast<float4*>(orow[p4] + c * 16) = v;
+          }
         }
       }
       ks += nk;
@@ -608,7 +635,6 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         for (int d = 0; d < D; ++d) o[d] = NAN;
       }
     }
-    if (lane == 0) bulk_wait_all();             // every TMA store of this warp has completed
   }
 
   tc::fence_before_sync();
@@ -647,20 +673,6 @@ cudaError_t make_q_map(CUtensorMap* map, const PrefillArgs& a) {
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.q), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-// out [N, S, Hq, D] fp32 as (D, Hq, S, N): stores of [32 rows x 16 columns] boxes (64-byte swizzle).
-cudaError_t make_out_map(CUtensorMap* map, const PrefillArgs& a) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[4] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq, (cuuint64_t)a.S, (cuuint64_t)a.N};
-  const cuuint64_t strides[3] = {(cuuint64_t)a.D * 4, (cuuint64_t)a.Hq * a.D * 4, (cuuint64_t)a.S * a.Hq * a.D * 4};
-  const cuuint32_t box[4] = {16, 1, 32, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.out, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -706,12 +718,11 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
     if (fa.numRegs != REGS_LAUNCH) return cudaErrorInvalidDeviceFunction;
     configured = true;
   }
-  CUtensorMap mk, mv, mq, mo;
+  CUtensorMap mk, mv, mq;
   cudaError_t e = make_cache_map(&mk, a.kc, a);
   if (e != cudaSuccess) return e;
   if ((e = make_cache_map(&mv, a.vc, a)) != cudaSuccess) return e;
   if ((e = make_q_map(&mq, a)) != cudaSuccess) return e;
-  if ((e = make_out_map(&mo, a)) != cudaSuccess) return e;
   // units: the two heads of a GQA pair at one row tile, else two row tiles of one head
   const int nq = (a.S + BM - 1) / BM;
   const int G = a.Hq / a.Hkv;
@@ -719,7 +730,7 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   if (units <= 0) return cudaSuccess;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)std::min<long long>(units, prefill_num_sms());
-  return launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, a, mk, mv, mq, mo);
+  return launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, a, mk, mv, mq);
 }
 
 }  // namespace
