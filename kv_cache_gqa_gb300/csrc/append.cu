@@ -660,6 +660,208 @@ append_stream_kernel(const __grid_constant__ AppendArgs a, int tb, int stage_byt
   }
 }
 
+// Lean streaming form for the common prefill layout: head_dim 128, float32 inputs, rotate-half
+// RoPE over the whole head (1D or xdRoPE sections, or none) and QK-Norm before, after or
+// absent, all fixed at compile time.  The producer and the per-item angle table are those of the
+// general streaming form.  The consumer work is cut to what the method needs: a token's rows are
+// taken in pairs (both q, both k or both v, since Hq and Hkv are even), half a warp per row and
+// 8 elements per lane (lane chunk at o and o + 64, so the rotate-half partner is in the same
+// lane), norm weights held in registers for the item, and no per-row mode branches.
+template <int NORM, bool ROT, typename QOutT, typename CacheT>
+__global__ void __launch_bounds__(STREAM_THREADS, 1)
+append_lean_kernel(const __grid_constant__ AppendArgs a, int tb, int stage_bytes) {
+  constexpr int D = 128, HALF = 64;
+  constexpr int NC = STREAM_CONSUMERS;
+  constexpr int APT = (STREAM_ANGLES + NC * 32 - 1) / (NC * 32);
+  static_assert((NC * 32) % HALF == 0, "a thread keeps one angle slot across its angles");
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ __align__(8) uint64_t full[STREAM_STAGES], empty[STREAM_STAGES];
+  __shared__ __align__(16) float s_cs[STREAM_STAGES][2][STREAM_ANGLES];
+  __shared__ int32_t s_slot[STREAM_STAGES][STREAM_ANGLES / 32];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tb = (a.T + tb - 1) / tb;
+  const int items = a.N * n_tb;
+  const int64_t tok_q = (int64_t)a.Hq * D, tok_kv = (int64_t)a.Hkv * D;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < STREAM_STAGES; ++st) { mbar_init(&full[st], 1); mbar_init(&empty[st], NC); }
+    fence_mbar_init();
+  }
+  const int ct = threadIdx.x;
+  const int my_j = ct % HALF;
+  const float my_ih = a.rope.inv_hi[my_j], my_il = a.rope.inv_lo[my_j];
+  const double my_inv = a.rope.inv[my_j];
+  const int my_axis = a.rope.axis[my_j];
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+
+  if (warp == NC) {                                     // ---- producer (as the general form) ----
+    if (lane == 0) {
+      int k = 0;
+      for (int it = blockIdx.x; it < items; it += gridDim.x, ++k) {
+        const int st = k % STREAM_STAGES;
+        if (k >= STREAM_STAGES && !mbar_wait_bounded(&empty[st], (uint32_t)((k / STREAM_STAGES - 1) & 1))) break;
+        const int n = it / n_tb, t0 = (it % n_tb) * tb, nt = min(tb, a.T - t0);
+        const int64_t tok = (int64_t)n * a.T + t0;
+        const uint32_t bq = (uint32_t)(nt * tok_q * 4), bkv = (uint32_t)(nt * tok_kv * 4);
+        const uint32_t bw = NORM ? 2u * D * 4u : 0u;
+        unsigned char* dst = ring + (size_t)st * stage_bytes;
+        mbar_arrive_expect_tx(&full[st], bq + 2 * bkv + bw);
+        bulk_g2s(dst, reinterpret_cast<const float*>(a.q) + tok * tok_q, bq, &full[st]);
+        bulk_g2s(dst + (size_t)tb * tok_q * 4, reinterpret_cast<const float*>(a.k) + tok * tok_kv, bkv, &full[st]);
+        bulk_g2s(dst + (size_t)tb * (tok_q + tok_kv) * 4, reinterpret_cast<const float*>(a.v) + tok * tok_kv, bkv,
+                 &full[st]);
+        if (NORM) {
+          unsigned char* wdst = dst + (size_t)tb * (tok_q + 2 * tok_kv) * 4;
+          bulk_g2s(wdst, a.q_w + (int64_t)n * a.w_stride, D * 4, &full[st]);
+          bulk_g2s(wdst + D * 4, a.k_w + (int64_t)n * a.w_stride, D * 4, &full[st]);
+        }
+      }
+      for (int j = max(0, k - STREAM_STAGES); j < k; ++j)
+        mbar_wait_bounded(&full[j % STREAM_STAGES], (uint32_t)((j / STREAM_STAGES) & 1));
+    }
+    return;
+  }
+
+  // ---- consumers ----
+  const int hw = lane >> 4;                             // row of the pair
+  const int o1 = 4 * (lane & 15), o2 = o1 + HALF;
+  const int pq = a.Hq / 2, pk = a.Hkv / 2, ppt = pq + 2 * pk;   // row pairs per token
+  auto load_meta = [&](int it, int32_t (&p)[APT], int32_t& slot) {
+    if (it >= items) return;
+    const int n = it / n_tb, t0 = (it % n_tb) * tb, nt = min(tb, a.T - t0);
+    if (ct < nt) slot = a.slot[(int64_t)n * a.slot_stride + t0 + ct];
+    if constexpr (ROT) {
+#pragma unroll
+      for (int i = 0; i < APT; ++i) {
+        const int tt = (ct + i * NC * 32) / HALF;
+        if (tt < nt) p[i] = a.pos[(int64_t)n * a.pos_stride + (int64_t)(t0 + tt) * a.rope.n_axes + my_axis];
+      }
+    }
+  };
+  int32_t p_next[APT], slot_next = 0;
+#pragma unroll
+  for (int i = 0; i < APT; ++i) p_next[i] = 0;
+  load_meta(blockIdx.x, p_next, slot_next);
+  int k = 0;
+  for (int it = blockIdx.x; it < items; it += gridDim.x, ++k) {
+    const int st = k % STREAM_STAGES;
+    const int n = it / n_tb, t0 = (it % n_tb) * tb, nt = min(tb, a.T - t0);
+    int32_t p_cur[APT];
+#pragma unroll
+    for (int i = 0; i < APT; ++i) p_cur[i] = p_next[i];
+    if (ct < nt) s_slot[st][ct] = slot_next;
+    load_meta(it + gridDim.x, p_next, slot_next);
+    if constexpr (ROT) {
+#pragma unroll
+      for (int i = 0; i < APT; ++i) {
+        const int idx = ct + i * NC * 32;
+        if (idx / HALF < nt) rope_cos_sin(p_cur[i], my_ih, my_il, my_inv, &s_cs[st][0][idx], &s_cs[st][1][idx]);
+      }
+    }
+    const bool landed = mbar_wait_bounded(&full[st], (uint32_t)((k / STREAM_STAGES) & 1));
+    if (!consumers_all(landed)) break;
+    const float* sq = reinterpret_cast<const float*>(ring + (size_t)st * stage_bytes);
+    const float* sk = sq + (size_t)tb * tok_q;
+    const float* sv = sk + (size_t)tb * tok_kv;
+    float4 wql = make_float4(1.f, 1.f, 1.f, 1.f), wqh = wql, wkl = wql, wkh = wql;
+    if (NORM) {
+      const float* swq = sv + (size_t)tb * tok_kv;
+      wql = *reinterpret_cast<const float4*>(swq + o1); wqh = *reinterpret_cast<const float4*>(swq + o2);
+      wkl = *reinterpret_cast<const float4*>(swq + D + o1); wkh = *reinterpret_cast<const float4*>(swq + D + o2);
+    }
+    const int64_t tok0 = (int64_t)n * a.T + t0;
+    int tt = 0, pi = warp;
+    while (pi >= ppt) { pi -= ppt; ++tt; }
+    for (; tt < nt;) {
+      const int kind = pi < pq ? 0 : (pi < pq + pk ? 1 : 2);
+      const int head = 2 * (kind == 0 ? pi : (kind == 1 ? pi - pq : pi - pq - pk)) + hw;
+      const float* src = kind == 0 ? sq + ((int64_t)tt * a.Hq + head) * D
+                       : (kind == 1 ? sk : sv) + ((int64_t)tt * a.Hkv + head) * D;
+      float4 lo = *reinterpret_cast<const float4*>(src + o1);
+      float4 hi = *reinterpret_cast<const float4*>(src + o2);
+      if (kind < 2) {
+        const float4 wl = kind == 0 ? wql : wkl, wh = kind == 0 ? wqh : wkh;
+        auto norm = [&]() {
+          float ss = lo.x * lo.x;
+          ss = fmaf(lo.y, lo.y, ss); ss = fmaf(lo.z, lo.z, ss); ss = fmaf(lo.w, lo.w, ss);
+          float s2 = hi.x * hi.x;
+          s2 = fmaf(hi.y, hi.y, s2); s2 = fmaf(hi.z, hi.z, s2); s2 = fmaf(hi.w, hi.w, s2);
+          ss += s2;
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+          const float r = rsqrtf(ss * (1.0f / (float)D) + a.eps);
+          lo.x *= r * wl.x; lo.y *= r * wl.y; lo.z *= r * wl.z; lo.w *= r * wl.w;
+          hi.x *= r * wh.x; hi.y *= r * wh.y; hi.z *= r * wh.z; hi.w *= r * wh.w;
+        };
+        if (NORM == 1) norm();
+        if constexpr (ROT) {
+          const float4 c = *reinterpret_cast<const float4*>(&s_cs[st][0][tt * HALF + o1]);
+          const float4 sn = *reinterpret_cast<const float4*>(&s_cs[st][1][tt * HALF + o1]);
+          float l0 = lo.x, h0 = hi.x;
+          lo.x = fmaf(-h0, sn.x, l0 * c.x); hi.x = fmaf(l0, sn.x, h0 * c.x);
+          l0 = lo.y; h0 = hi.y;
+          lo.y = fmaf(-h0, sn.y, l0 * c.y); hi.y = fmaf(l0, sn.y, h0 * c.y);
+          l0 = lo.z; h0 = hi.z;
+          lo.z = fmaf(-h0, sn.z, l0 * c.z); hi.z = fmaf(l0, sn.z, h0 * c.z);
+          l0 = lo.w; h0 = hi.w;
+          lo.w = fmaf(-h0, sn.w, l0 * c.w); hi.w = fmaf(l0, sn.w, h0 * c.w);
+        }
+        if (NORM == 2) norm();
+      }
+      const float yl[4] = {lo.x, lo.y, lo.z, lo.w}, yh[4] = {hi.x, hi.y, hi.z, hi.w};
+      if (kind == 0) {
+        QOutT* dst = reinterpret_cast<QOutT*>(a.q_out) + ((tok0 + tt) * a.Hq + head) * D;
+        store4(dst + o1, yl);
+        store4(dst + o2, yh);
+      } else {
+        const int32_t slot = s_slot[st][tt];
+        if (slot >= 0 && slot < a.capacity) {
+          CacheT* dst = reinterpret_cast<CacheT*>(kind == 1 ? a.kc : a.vc) + (int64_t)n * a.inst_stride +
+                        ((int64_t)head * a.capacity + slot) * D;
+          store4(dst + o1, yl);
+          store4(dst + o2, yh);
+        }
+      }
+      pi += NC;
+      while (pi >= ppt) { pi -= ppt; ++tt; }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+}
+
+template <int NORM, bool ROT, typename QOutT, typename CacheT>
+cudaError_t launch_lean(const AppendArgs& a, int tb, int stage, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(append_lean_kernel<NORM, ROT, QOutT, CacheT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(STREAM_STAGES * (STREAM_STAGE_MAX + 2 * 128 * sizeof(float))));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int64_t items = (int64_t)a.N * ((a.T + tb - 1) / tb);
+  const int grid = (int)std::min<int64_t>(items, append_num_sms());
+  return launch_pdl(append_lean_kernel<NORM, ROT, QOutT, CacheT>, dim3(grid), dim3(STREAM_THREADS),
+                    (size_t)STREAM_STAGES * stage, s, a, tb, stage);
+}
+
+template <typename QOutT, typename CacheT>
+cudaError_t launch_lean_modes(const AppendArgs& a, int tb, int stage, cudaStream_t s) {
+  const bool rot = a.rope.kind == KVA_ROPE_1D || a.rope.kind == KVA_ROPE_SECTIONS;
+  const int norm = a.q_w == nullptr ? 0 : (a.after_rope ? 2 : 1);
+  if (rot) {
+    if (norm == 1) return launch_lean<1, true, QOutT, CacheT>(a, tb, stage, s);
+    if (norm == 2) return launch_lean<2, true, QOutT, CacheT>(a, tb, stage, s);
+    return launch_lean<0, true, QOutT, CacheT>(a, tb, stage, s);
+  }
+  if (norm == 1) return launch_lean<1, false, QOutT, CacheT>(a, tb, stage, s);
+  if (norm == 2) return launch_lean<2, false, QOutT, CacheT>(a, tb, stage, s);
+  return launch_lean<0, false, QOutT, CacheT>(a, tb, stage, s);
+}
+
 template <int D, typename InT, typename QOutT, typename CacheT>
 cudaError_t launch_tokens(const AppendArgs& a, cudaStream_t s) {
   if constexpr (D == 72) {
@@ -674,6 +876,12 @@ cudaError_t launch_tokens(const AppendArgs& a, cudaStream_t s) {
     const int64_t items = (int64_t)a.N * ((a.T + tb - 1) / tb);
     if (a.T >= tb && items >= 2 * append_num_sms() && tb * per_tok <= STREAM_STAGE_MAX) {
       const int stage = (int)(tb * per_tok + w_bytes);
+      if constexpr (D == 128 && sizeof(InT) == 4) {
+        // the lean form: rotate-half over the whole head (or none) and even head counts
+        const bool lean_rope = a.rope.kind == KVA_ROPE_1D || a.rope.kind == KVA_ROPE_SECTIONS ||
+                               a.rope.kind == KVA_ROPE_NONE;
+        if (lean_rope && a.Hq % 2 == 0 && a.Hkv % 2 == 0) return launch_lean_modes<QOutT, CacheT>(a, tb, stage, s);
+      }
       const size_t smem = (size_t)STREAM_STAGES * stage;
       static bool configured = false;                 // one attribute per template instance
       if (!configured) {
