@@ -4,9 +4,9 @@
 // Work unit: two 128-row query tiles ("slots") that read the same KV head: the two query
 // heads of a GQA group at the same rows when the group size is even (each K/V tile is loaded
 // once for both), otherwise two row tiles of one head paired so that causal work is balanced
-// (tiles t and n-1-t).  Units are numbered heaviest first; one CTA per SM walks units
-// b, 2P-1-b, 2P+b, ... (a snake over the P CTAs, which evens out the causal cost), so a
-// unit's epilogue overlaps the next unit's Q load and first Q K^T.
+// (tiles t and n-1-t).  One CTA per SM walks units b, 2P-1-b, 2P+b, ... (a snake over the P
+// CTAs, which evens out the causal cost), so a unit's epilogue overlaps the next unit's Q load
+// and first Q K^T.
 //
 // Twelve warps (three warpgroups) with fixed roles:
 //   warps 0-3, 4-7  softmax of slot 0 and slot 1: thread t of a group owns row t = TMEM lane
