@@ -5,7 +5,7 @@
 // KV head g, row tile rt, instance b).  Its 16 rows are r = rt*16 + (0..15) of the group's
 // G*k rows, row r = (block position i = r / G, query head g*G + r % G); row i sees slots
 // [0, L - k + i].  The CTA's four warps are independent: warp w takes the 16-key tiles w,
-// w+4, ... of the chunk through a private 3-stage TMA ring (K and V as [16 keys x 64 dims]
+// w+4, ... of the chunk through a private 2-stage TMA ring (K and V as [16 keys x 64 dims]
 // boxes, 128-byte swizzle), and per tile computes
 //   S = Q K^T      16 rows x 16 keys, 16 mma.sync m16n8k16 (both row halves live)
 //   online softmax per row in registers (each lane holds rows lane/4 and lane/4 + 8)
@@ -29,7 +29,7 @@ constexpr int D = DECODE_HEAD_DIM;
 constexpr int WARPS = 4;
 constexpr int THREADS = WARPS * 32;
 constexpr int KT = 16;                          // keys per warp tile
-constexpr int NS = 3;                           // ring stages per warp
+constexpr int NS = 2;                           // ring stages per warp (three CTAs fit an SM)
 constexpr int BOX = KT * 128;                   // one [16 keys x 64 dims] swizzled box, 2 KB
 constexpr int STAGE = 4 * BOX;                  // K lo, K hi, V lo, V hi
 constexpr int RING = NS * STAGE;                // per warp
@@ -58,7 +58,7 @@ __device__ __forceinline__ uint32_t q_pair(const void* q, kva_dtype dt, int64_t 
   return pack_bf16x2(f[0], f[1]);
 }
 
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, 3)
 verify_mma_kernel(const __grid_constant__ VerifyArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, kva_dtype q_dtype) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
