@@ -18,7 +18,7 @@ void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_rela
 int lmhead_max_hidden();
 bool prefill_simt_supports(int Dk, int Dv);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, kva_dtype dt, cudaStream_t s);
-bool prefill_tc_supports(int D, kva_dtype dt);
+bool prefill_tc_supports(int D, int Dv, kva_dtype dt);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 
 namespace {
@@ -347,7 +347,7 @@ kva_status kv_attn_prefill(
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   a.scale_log2 = sc * 1.4426950408889634f;
   cudaError_t e;
-  if (!asymmetric(cache) && prefill_tc_supports(D, cache.dtype)) {
+  if (prefill_tc_supports(D, cache.head_dim_v, cache.dtype)) {
     e = launch_prefill_tc(a, (cudaStream_t)stream);
   } else if (prefill_simt_supports(D, cache.head_dim_v)) {
     e = launch_prefill_simt(a, cache.dtype, (cudaStream_t)stream);

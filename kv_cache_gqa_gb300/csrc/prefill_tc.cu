@@ -59,18 +59,19 @@ constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 192, REGS_CONTROL = 120;
 static_assert(2 * REGS_SOFTMAX + REGS_CONTROL <= 3 * REGS_LAUNCH, "register split exceeds the launch total");
 static_assert(REGS_LAUNCH * THREADS <= 65536, "launch registers");
 constexpr int SUB = BM * 128;             // bytes of one [128 rows x 64 bf16] swizzled box
-constexpr int NSTAGE = 2;
 constexpr int ST_BYTES = 32 * 64;         // one staging tile: 32 rows x 16 fp32 (64-byte swizzle)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
 
-template <int D>
+// D: q and key width, DV: value width, NST: stages of the K and of the V ring.
+template <int D, int DV, int NST>
 struct Layout {
-  static constexpr int NSUB = (D + 63) / 64;                 // 64-column boxes per row tile
+  static constexpr int NSUB = (D + 63) / 64;                 // 64-column boxes of a q / key row
+  static constexpr int NSUBV = (DV + 63) / 64;               // 64-column boxes of a value row
   static constexpr int Q_OFF = 0;                            // [2 slots][NSUB boxes]
-  static constexpr int K_OFF = Q_OFF + 2 * NSUB * SUB;       // [NSTAGE][NSUB]
-  static constexpr int V_OFF = K_OFF + NSTAGE * NSUB * SUB;  // [NSTAGE][NSUB]
-  static constexpr int ST_OFF = V_OFF + NSTAGE * NSUB * SUB; // [softmax warp][2]
+  static constexpr int K_OFF = Q_OFF + 2 * NSUB * SUB;       // [NST][NSUB]
+  static constexpr int V_OFF = K_OFF + NST * NSUB * SUB;     // [NST][NSUBV]
+  static constexpr int ST_OFF = V_OFF + NST * NSUBV * SUB;   // [softmax warp][2]
   static constexpr int BAR_OFF = ST_OFF + SOFTMAX_WARPS * 2 * ST_BYTES;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;          // + slack to align the base to 1024
 };
@@ -233,27 +234,28 @@ __device__ __forceinline__ TileRanges tile_ranges(const PrefillArgs& a, const Sl
   return tr;
 }
 
-template <int D>
+template <int D, int DV, int NST>
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ) {
-  using LY = Layout<D>;
+  using LY = Layout<D, DV, NST>;
   constexpr int DK = (D + 15) / 16 * 16;      // MMA K extent of Q K^T (zero padded)
-  constexpr int DN = DK;                      // MMA N extent of P V
+  constexpr int DN = (DV + 15) / 16 * 16;     // MMA N extent of P V
   constexpr int KSTEPS = DK / 16;
-  constexpr int NSUB = LY::NSUB;
-  constexpr int NCH = (D + 15) / 16;          // 16-column output chunks
+  constexpr int NSUB = LY::NSUB, NSUBV = LY::NSUBV;
+  constexpr int NCH = (DV + 15) / 16;         // 16-column output chunks
   constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0, 0);
   constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, DN, 0, 1);
   static_assert(DN % 16 == 0 && DN <= 128, "N extent");
+  static_assert(NST == 1 || NST == 2, "ring stages (two barrier slots each)");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::BAR_OFF);
-  uint64_t* k_full = bars + 0;     // [NSTAGE] K tile landed
-  uint64_t* k_free = bars + 2;     // [NSTAGE] both slots' Q K^T of the tile done: K stage free
-  uint64_t* v_full = bars + 4;     // [NSTAGE] V tile landed
-  uint64_t* v_free = bars + 6;     // [NSTAGE] both slots' P V of the tile done: V stage free
+  uint64_t* k_full = bars + 0;     // [NST] K tile landed
+  uint64_t* k_free = bars + 2;     // [NST] both slots' Q K^T of the tile done: K stage free
+  uint64_t* v_full = bars + 4;     // [NST] V tile landed
+  uint64_t* v_free = bars + 6;     // [NST] both slots' P V of the tile done: V stage free
   uint64_t* s_full = bars + 8;     // [slot] S ready in TMEM
   uint64_t* p_full = bars + 10;    // [slot] P written to TMEM by the slot's 4 warps
   uint64_t* pv_done = bars + 12;   // [slot] P V of the slot's tile finished
@@ -321,38 +323,37 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         for (int j = tr.j0; j < tr.j1; j = tr.next_tile(j), ++it) {
           // K and V of a tile use separate stages: K is free again once both slots' Q K^T have
           // run (early in the tile), V only after both P V
-          const int st = it % NSTAGE;
-          const uint32_t ph = (uint32_t)((it / NSTAGE - 1) & 1);
+          const int st = it % NST;
+          const uint32_t ph = (uint32_t)((it / NST - 1) & 1);
           const int key0 = j * BN;
-          if (it >= NSTAGE && !mbar_wait_bounded(&k_free[st], ph)) { ok = false; break; }
+          if (it >= NST && !mbar_wait_bounded(&k_free[st], ph)) { ok = false; break; }
           mbar_arrive_expect_tx(&k_full[st], NSUB * SUB);
           for (int c = 0; c < NSUB; ++c)
             tc::tma_load_4d(sm + LY::K_OFF + (st * NSUB + c) * SUB, &tmK, c * 64, key0, g, sl.n, &k_full[st]);
-          if (it >= NSTAGE && !mbar_wait_bounded(&v_free[st], ph)) { ok = false; break; }
-          mbar_arrive_expect_tx(&v_full[st], NSUB * SUB);
-          for (int c = 0; c < NSUB; ++c)
-            tc::tma_load_4d(sm + LY::V_OFF + (st * NSUB + c) * SUB, &tmV, c * 64, key0, g, sl.n, &v_full[st]);
+          if (it >= NST && !mbar_wait_bounded(&v_free[st], ph)) { ok = false; break; }
+          mbar_arrive_expect_tx(&v_full[st], NSUBV * SUB);
+          for (int c = 0; c < NSUBV; ++c)
+            tc::tma_load_4d(sm + LY::V_OFF + (st * NSUBV + c) * SUB, &tmV, c * 64, key0, g, sl.n, &v_full[st]);
         }
         if (*s_abort) ok = false;
       }
       if (!ok) *s_abort = 1;
       // the copies this CTA issued have normally landed long ago; never leave one in flight
-      for (int e = max(0, it - NSTAGE); e < it; ++e) {
-        mbar_wait_bounded(&k_full[e % NSTAGE], (uint32_t)((e / NSTAGE) & 1));
-        mbar_wait_bounded(&v_full[e % NSTAGE], (uint32_t)((e / NSTAGE) & 1));
+      for (int e = max(0, it - NST); e < it; ++e) {
+        mbar_wait_bounded(&k_full[e % NST], (uint32_t)((e / NST) & 1));
+        mbar_wait_bounded(&v_full[e % NST], (uint32_t)((e / NST) & 1));
       }
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
-      static_assert(NSTAGE == 2, "descriptor selection assumes two stages");
       const uint64_t q_desc0 = tc::desc_at(DESC_KMAJ, smem_u32(sm + LY::Q_OFF));
       const uint64_t q_desc1 = tc::desc_at(DESC_KMAJ, smem_u32(sm + LY::Q_OFF + NSUB * SUB));
       const uint64_t k_desc0 = tc::desc_at(DESC_KMAJ, smem_u32(sm + LY::K_OFF));
-      const uint64_t k_desc1 = tc::desc_at(DESC_KMAJ, smem_u32(sm + LY::K_OFF + NSUB * SUB));
       const uint64_t v_desc0 = tc::desc_at(DESC_VMN, smem_u32(sm + LY::V_OFF));
-      const uint64_t v_desc1 = tc::desc_at(DESC_VMN, smem_u32(sm + LY::V_OFF + NSUB * SUB));
+      // descriptor start addresses advance by constant offsets (addresses stay below 2^18)
+      constexpr uint64_t K_STAGE = (uint64_t)(NSUB * SUB) >> 4, V_STAGE = (uint64_t)(NSUBV * SUB) >> 4;
       int it = 0;                               // ring entries consumed so far
       int ks[2] = {0, 0};                       // key tiles of each slot so far
       int nus[2] = {0, 0};                      // units in which each slot was active so far
@@ -368,7 +369,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         tc::fence_after_sync();
         auto issue_s = [&](int s, int e) {
           const uint64_t qd = s ? q_desc1 : q_desc0;
-          const uint64_t kd = (e & 1) ? k_desc1 : k_desc0;
+          const uint64_t kd = k_desc0 + (uint64_t)(e % NST) * K_STAGE;
 #pragma unroll
           for (int k = 0; k < KSTEPS; ++k) {
             // descriptor start addresses advance by constant offsets (addresses stay below 2^18)
@@ -379,15 +380,15 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           if (++s_issued == s_total) tc::mma_commit(q_free);   // the unit's last Q K^T
         };
         if (ok) {
-          ok = mbar_wait_bounded(&k_full[it % NSTAGE], (uint32_t)((it / NSTAGE) & 1));
+          ok = mbar_wait_bounded(&k_full[it % NST], (uint32_t)((it / NST) & 1));
           tc::fence_after_sync();
 #pragma unroll
           for (int s = 0; s < 2; ++s)
             if (ok && tr.active(s, tr.j0)) issue_s(s, it);
-          tc::mma_commit(&k_free[it % NSTAGE]);         // this K stage is free once those finish
+          tc::mma_commit(&k_free[it % NST]);            // this K stage is free once those finish
         }
         for (int j = tr.j0; ok && j < tr.j1; ++it) {
-          const int st = it % NSTAGE;
+          const int st = it % NST;
           const int jn = tr.next_tile(j);              // the tile loaded after j (entry it + 1)
           bool next_landed = false, v_landed = false;
 #pragma unroll
@@ -397,13 +398,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
               const int k = j - tr.js0[s];
               if (!mbar_wait_bounded(&p_full[s], (uint32_t)((ks[s] + k) & 1))) { ok = false; continue; }
               if (!v_landed) {
-                if (!mbar_wait_bounded(&v_full[st], (uint32_t)((it / NSTAGE) & 1))) { ok = false; continue; }
+                if (!mbar_wait_bounded(&v_full[st], (uint32_t)((it / NST) & 1))) { ok = false; continue; }
                 v_landed = true;
               }
               // the first P V of a unit overwrites O: the previous unit's O must have been read
               if (k == 0 && nus[s] > 0 && !mbar_wait_bounded(&o_free[s], (uint32_t)((nus[s] - 1) & 1))) { ok = false; continue; }
               tc::fence_after_sync();
-              const uint64_t vd = st ? v_desc1 : v_desc0;
+              const uint64_t vd = v_desc0 + (uint64_t)st * V_STAGE;
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk)
                 tc::mma_ts(tmem + 256 + s * 128, tmem + s * BN + kk * 8, vd + (uint64_t)(kk * 2048 >> 4),
@@ -413,7 +414,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
             }
             if (jn < tr.j1 && tr.active(s, jn)) {
               if (!next_landed) {
-                if (!mbar_wait_bounded(&k_full[(it + 1) % NSTAGE], (uint32_t)(((it + 1) / NSTAGE) & 1))) { ok = false; continue; }
+                if (!mbar_wait_bounded(&k_full[(it + 1) % NST], (uint32_t)(((it + 1) / NST) & 1))) { ok = false; continue; }
                 tc::fence_after_sync();
                 next_landed = true;
               }
@@ -422,7 +423,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           }
           if (!ok) break;
           tc::mma_commit(&v_free[st]);              // V of this tile: free once both P V are done
-          if (jn < tr.j1) tc::mma_commit(&k_free[(it + 1) % NSTAGE]);   // K of the next: after its Q K^T
+          if (jn < tr.j1) tc::mma_commit(&k_free[(it + 1) % NST]);   // K of the next: after its Q K^T
           j = jn;
         }
 #pragma unroll
@@ -595,7 +596,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
 #pragma unroll
         for (int p4 = 0; p4 < 4; ++p4) {
           const int rr = __shfl_sync(FULL_MASK, my_row, (lane >> 2) + 8 * p4);
-          orow[p4] = rr < 0 ? nullptr : a.out + (((int64_t)n * a.S + rr) * a.Hq + h) * D + (lane & 3) * 4;
+          orow[p4] = rr < 0 ? nullptr : a.out + (((int64_t)n * a.S + rr) * a.Hq + h) * DV + (lane & 3) * 4;
         }
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
@@ -611,7 +612,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           for (int p4 = 0; p4 < 4; ++p4) {
             const int rr = (lane >> 2) + 8 * p4, q = lane & 3;
             const float4 v = *reinterpret_cast<const float4*>(buf + rr * 64 + ((q ^ ((rr >> 1) & 3)) << 4));
-            if (orow[p4] != nullptr && c * 16 + q * 4 < D) *reinterpret_cast<float4*>(orow[p4] + c * 16) = v;
+            if (orow[p4] != nullptr && c * 16 + q * 4 < DV) *reinterpret_cast<float4*>(orow[p4] + c * 16) = v;
           }
         }
       }
@@ -631,8 +632,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         if (i >= a.S) continue;
         const int row = gather ? a.row_of_slot[i] : i;
         if (row < 0 || row >= a.S) continue;
-        float* o = a.out + (((int64_t)sl.n * a.S + row) * a.Hq + sl.h[s]) * D;
-        for (int d = 0; d < D; ++d) o[d] = NAN;
+        float* o = a.out + (((int64_t)sl.n * a.S + row) * a.Hq + sl.h[s]) * DV;
+        for (int d = 0; d < DV; ++d) o[d] = NAN;
       }
     }
   }
@@ -677,12 +678,12 @@ cudaError_t make_q_map(CUtensorMap* map, const PrefillArgs& a) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Cache view for TMA: dims (D, S valid slots, Hkv, N); rows >= S read as zeros.
-cudaError_t make_cache_map(CUtensorMap* map, const void* base, const PrefillArgs& a) {
+// Cache view for TMA: dims (width, S valid slots, Hkv, N); rows >= S read as zeros.
+cudaError_t make_cache_map(CUtensorMap* map, const void* base, const PrefillArgs& a, int width, int64_t inst_stride) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[4] = {(cuuint64_t)a.D, (cuuint64_t)a.S, (cuuint64_t)a.Hkv, (cuuint64_t)a.N};
-  const cuuint64_t strides[3] = {(cuuint64_t)a.D * 2, (cuuint64_t)a.capacity * a.D * 2, (cuuint64_t)a.inst_stride * 2};
+  const cuuint64_t dims[4] = {(cuuint64_t)width, (cuuint64_t)a.S, (cuuint64_t)a.Hkv, (cuuint64_t)a.N};
+  const cuuint64_t strides[3] = {(cuuint64_t)width * 2, (cuuint64_t)a.capacity * width * 2, (cuuint64_t)inst_stride * 2};
   const cuuint32_t box[4] = {64, BN, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
@@ -703,25 +704,25 @@ int prefill_num_sms() {
   return n[dev];
 }
 
-template <int D>
+template <int D, int DV, int NST>
 cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
-  constexpr int SMEM = Layout<D>::SMEM;
+  constexpr int SMEM = Layout<D, DV, NST>::SMEM;
   static_assert(SMEM <= 232448, "shared memory per CTA");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, DV, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     // the register split assumes the launch holds exactly REGS_LAUNCH per thread: with fewer,
     // the softmax warpgroups' setmaxnreg.inc could never be satisfied
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D, DV, NST>)) != cudaSuccess) return e;
     if (fa.numRegs != REGS_LAUNCH) return cudaErrorInvalidDeviceFunction;
     configured = true;
   }
   CUtensorMap mk, mv, mq;
-  cudaError_t e = make_cache_map(&mk, a.kc, a);
+  cudaError_t e = make_cache_map(&mk, a.kc, a, D, a.inst_stride);
   if (e != cudaSuccess) return e;
-  if ((e = make_cache_map(&mv, a.vc, a)) != cudaSuccess) return e;
+  if ((e = make_cache_map(&mv, a.vc, a, DV, a.inst_stride_v)) != cudaSuccess) return e;
   if ((e = make_q_map(&mq, a)) != cudaSuccess) return e;
   // units: the two heads of a GQA pair at one row tile, else two row tiles of one head
   const int nq = (a.S + BM - 1) / BM;
@@ -730,20 +731,23 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   if (units <= 0) return cudaSuccess;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)std::min<long long>(units, prefill_num_sms());
-  return launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, a, mk, mv, mq);
+  return launch_pdl(prefill_tc_kernel<D, DV, NST>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, a, mk, mv, mq);
 }
 
 }  // namespace
 
-bool prefill_tc_supports(int D, kva_dtype dt) {
-  return dt == KVA_BF16 && (D == 64 || D == 72 || D == 128) && encode_fn() != nullptr;
+bool prefill_tc_supports(int D, int Dv, kva_dtype dt) {
+  const bool shapes = (Dv == D && (D == 64 || D == 72 || D == 128)) || (D == 192 && Dv == 128);
+  return dt == KVA_BF16 && shapes && encode_fn() != nullptr;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
+  if (a.D == 192 && a.Dv == 128) return launch_d<192, 128, 1>(a, s);   // one K and one V stage fit
+  if (a.Dv != a.D) return cudaErrorInvalidValue;
   switch (a.D) {
-    case 64: return launch_d<64>(a, s);
-    case 72: return launch_d<72>(a, s);
-    case 128: return launch_d<128>(a, s);
+    case 64: return launch_d<64, 64, 2>(a, s);
+    case 72: return launch_d<72, 72, 2>(a, s);
+    case 128: return launch_d<128, 128, 2>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from helpers import assert_bf16_store, assert_fp32_close, bf16_bits, dev, host
+from helpers import assert_bf16_close, assert_bf16_store, assert_fp32_close, bf16_bits, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -152,7 +152,10 @@ def test_prefill_asymmetric(K, dt, S, mask, G):
     got = host(out)
     for n in range(N):
         ref = O.prefill(q[n], kc[n], vc[n], S, mask, seg)
-        assert_fp32_close(got[n], ref, f"asym prefill n={n} S={S} {mask}")
+        if dt == "f32":
+            assert_fp32_close(got[n], ref, f"asym prefill n={n} S={S} {mask}")
+        else:                      # tensor-core path: P enters P V as bf16 (bf16-cache tolerance)
+            assert_bf16_close(got[n], ref, f"asym prefill n={n} S={S} {mask}")
 
 
 # ----------------------------------------------------------------------------
@@ -218,7 +221,8 @@ def test_mla_append_prefill_decode_chain(K):
     # each stage against the oracle on that stage's own inputs: the stored queries and cache rows
     # (which the append check bounds against the oracle's to one bf16 rounding)
     assert_bf16_store(bf16_bits(q_out)[0], qr, "prompt q_out")
-    assert_fp32_close(host(out)[0], O.prefill(host(q_out)[0], host(kc)[0], host(vc)[0], S, "causal"),
+    # the bf16 prompt prefill runs on the tensor cores (P enters P V as bf16): bf16-cache tolerance
+    assert_bf16_close(host(out)[0], O.prefill(host(q_out)[0], host(kc)[0], host(vc)[0], S, "causal"),
                       "prompt prefill")
     ws = torch.zeros(K.decode_workspace_bytes(1, H, H, W, DV), dtype=torch.uint8, device="cuda")
     for s in range(steps):

@@ -44,10 +44,10 @@ def needed_tiles(u):
     return [j for j in range(lo, hi) if act(0, j) or act(1, j)], act
 
 
-def run(units, seed, gather=False, slow_mma=True, walk_all=False):
+def run(units, seed, gather=False, slow_mma=True, walk_all=False, ns=NS):
     rnd = random.Random(seed)
-    k_full = [Bar(1) for _ in range(NS)]; k_free = [Bar(1) for _ in range(NS)]
-    v_full = [Bar(1) for _ in range(NS)]; v_free = [Bar(1) for _ in range(NS)]
+    k_full = [Bar(1) for _ in range(ns)]; k_free = [Bar(1) for _ in range(ns)]
+    v_full = [Bar(1) for _ in range(ns)]; v_free = [Bar(1) for _ in range(ns)]
     s_full = [Bar(1), Bar(1)]; p_full = [Bar(1), Bar(1)]; pv_done = [Bar(1), Bar(1)]
     q_full = [Bar(1), Bar(1)]; o_full = [Bar(1), Bar(1)]; o_free = [Bar(1), Bar(1)]
     q_free = Bar(1)
@@ -72,12 +72,12 @@ def run(units, seed, gather=False, slow_mma=True, walk_all=False):
                         yield ("load", q_full[s])
             walk = list(range(tiles[0], tiles[-1] + 1)) if walk_all else tiles
             for j in walk:
-                st = it % NS
-                if it >= NS:
-                    yield lambda st=st, it=it: k_free[st].ready(it // NS - 1)
+                st = it % ns
+                if it >= ns:
+                    yield lambda st=st, it=it: k_free[st].ready(it // ns - 1)
                 yield ("load", k_full[st])
-                if it >= NS:
-                    yield lambda st=st, it=it: v_free[st].ready(it // NS - 1)
+                if it >= ns:
+                    yield lambda st=st, it=it: v_free[st].ready(it // ns - 1)
                 yield ("load", v_full[st])
                 it += 1
 
@@ -101,11 +101,11 @@ def run(units, seed, gather=False, slow_mma=True, walk_all=False):
             for s in range(2):
                 if u[s] is not None:
                     yield lambda s=s: q_full[s].ready(nus[s])
-            yield lambda it=it: k_full[it % NS].ready(it // NS)
+            yield lambda it=it: k_full[it % ns].ready(it // ns)
             for s in range(2):
                 if act(s, walk[0]):
                     issue_s(s)
-            mma_done(k_free[it % NS])
+            mma_done(k_free[it % ns])
             for idx, j in enumerate(walk):
                 jn = walk[idx + 1] if idx + 1 < len(walk) else None
                 next_landed = v_landed = False
@@ -114,7 +114,7 @@ def run(units, seed, gather=False, slow_mma=True, walk_all=False):
                         k = j - u[s][0]
                         yield lambda s=s, k=k: p_full[s].ready(ks[s] + k)
                         if not v_landed:
-                            yield lambda it=it: v_full[it % NS].ready(it // NS)
+                            yield lambda it=it: v_full[it % ns].ready(it // ns)
                             v_landed = True
                         if k == 0 and nus[s] > 0:
                             yield lambda s=s: o_free[s].ready(nus[s] - 1)
@@ -123,13 +123,13 @@ def run(units, seed, gather=False, slow_mma=True, walk_all=False):
                             mma_done(o_full[s])
                     if jn is not None and act(s, jn):
                         if not next_landed:
-                            yield lambda it=it: k_full[(it + 1) % NS].ready((it + 1) // NS)
+                            yield lambda it=it: k_full[(it + 1) % ns].ready((it + 1) // ns)
                             next_landed = True
                         issue_s(s)
                 # with walk_all, a tile neither slot needs frees its stages without waiting
-                mma_done(v_free[it % NS])
+                mma_done(v_free[it % ns])
                 if jn is not None:
-                    mma_done(k_free[(it + 1) % NS])
+                    mma_done(k_free[(it + 1) % ns])
                 it += 1
             for s in range(2):
                 if u[s] is not None:
@@ -215,13 +215,14 @@ def test_single_unit_phases_stay_in_step(seed):
         run([(ra, None)], seed, slow_mma=False)
 
 
+@pytest.mark.parametrize("ns", [1, 2])
 @pytest.mark.parametrize("gather", [False, True])
 @pytest.mark.parametrize("seed", [0, 1, 2])
-def test_persistent_unit_walk_phases_stay_in_step(seed, gather):
-    """Several units per CTA: the ring, the per-slot tile counters and the per-unit barriers
-    (q_full, q_free, o_full, o_free) carry their phases across units."""
+def test_persistent_unit_walk_phases_stay_in_step(seed, gather, ns):
+    """Several units per CTA: the rings (one or two stages), the per-slot tile counters and the
+    per-unit barriers (q_full, q_free, o_full, o_free) carry their phases across units."""
     for i, units in enumerate(_unit_lists(seed, 150)):
-        run(units, seed * 1000 + i, gather=gather)
+        run(units, seed * 1000 + i, gather=gather, ns=ns)
 
 
 def test_replay_catches_a_walk_over_unneeded_tiles():
