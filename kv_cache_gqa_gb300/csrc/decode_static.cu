@@ -2,9 +2,8 @@
 //
 // kv_attn_decode needs a caller-provided workspace for its split-KV partials and merge
 // counters.  Some callers have no way to obtain one: code running where cudaMalloc is
-// forbidden or unavailable (inside a stream capture in some runtimes, in a plugin whose
-// host framework owns every allocation, or in a latency-critical loop that must never
-// touch the allocator).  kv_attn_decode_static serves them: it runs the same decode kernel
+// forbidden or unavailable (a plugin whose host framework owns every device allocation, or
+// a latency-critical loop that must never touch the allocator).  kv_attn_decode_static serves them: it runs the same decode kernel
 // with its scratch taken from a fixed-size array that lives in this library's device image,
 // so the call itself allocates nothing.
 //
