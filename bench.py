@@ -296,13 +296,16 @@ def verify_bench(torch, K, stream):
             "block_tokens_per_s": round(B * k / (ms / 1e3), 1)}
 
 
-def serving_bench(torch, K, stream, W, lm_ws_bytes):
+def serving_bench(torch, K, stream, W, lm_ws_bytes, batch=None):
     """The batched serving step: 64 sequences with contexts uniform in [1024, 32768] (the same
     seeded draw as the parity tests), capacity ctx + 128; one step = the fused append + decode
     over all 64 caches and the batched lm_head argmax.  Caches are random bf16 (contents do not
-    change the work).  Timed as a graph of 8 back-to-back steps at the first step's lengths."""
+    change the work).  Timed as a graph of 8 back-to-back steps at the first step's lengths.
+    `batch` keeps only the first sequences of the draw (a smaller case for counter captures)."""
     import workloads as WL
     ctx = WL.serving_contexts(0)
+    if batch is not None:
+        ctx = ctx[:batch]
     B, cap = ctx.size, int(ctx.max()) + 128
     g = torch.Generator(device="cuda"); g.manual_seed(11)
     kc = torch.randn((B, HKV, cap, D), device="cuda", generator=g).to(torch.bfloat16)
@@ -416,10 +419,39 @@ def mla_bench(torch, K, stream):
             "decode_16x4096_algorithmic_bytes": big_bytes}
 
 
+def run_only(args, torch, K):
+    """One sub-benchmark alone (for counter captures of its kernels); prints its own JSON line."""
+    stream = torch.cuda.Stream()
+    if args.only == "verify":
+        res = verify_bench(torch, K, stream)
+    elif args.only == "mla":
+        res = mla_bench(torch, K, stream)
+    elif args.only == "lm64":                        # the batched lm_head alone, 64 hidden rows
+        g = torch.Generator(device="cuda"); g.manual_seed(3)
+        W = (torch.randn((VOCAB, HIDDEN), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        h = torch.randn((64, HIDDEN), device="cuda", generator=g)
+        ids = torch.empty((64,), dtype=torch.int32, device="cuda")
+        lws = torch.zeros(K.lmhead_workspace_bytes(64, HIDDEN), dtype=torch.uint8, device="cuda")
+        with torch.cuda.stream(stream):
+            K.lmhead_argmax(h, W, ids, lws)          # configures the kernel before capture
+        torch.cuda.synchronize()
+        ms = graph_avg_ms(torch, stream, lambda: K.lmhead_argmax(h, W, ids, lws), 8, reps=2)
+        res = {"lm_head_b64_us": round(ms * 1e3, 2), "GB/s": round(VOCAB * HIDDEN * 2 / (ms / 1e3) / 1e9, 1)}
+    else:                                            # serving16: the first 16 sequences of the draw
+        g = torch.Generator(device="cuda"); g.manual_seed(3)
+        W = (torch.randn((VOCAB, HIDDEN), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        res = serving_bench(torch, K, stream, W, None, batch=16)
+    print(json.dumps({"case": args.only, "result": res}), flush=True)
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import kv_cache_gqa_gb300 as K
     torch.cuda.set_device(local_rank)
+    if args.only:
+        if rank == 0:
+            run_only(args, torch, K)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
@@ -706,6 +738,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="kv_attn", choices=["kv_attn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", choices=["verify", "mla", "serving16", "lm64"], default=None,
+                    help="run one sub-benchmark alone and print its figures (for counter captures); "
+                         "not the benchmark line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
