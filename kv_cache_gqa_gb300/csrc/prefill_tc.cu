@@ -13,11 +13,14 @@
 //              t.  Per key tile it reads the row's 128 fp32 scores from TMEM, applies the
 //              row's visible-key range (causal, window segment or full), keeps the running
 //              max and sum, and writes P = exp2(S - m) back over the same columns as packed
-//              bf16 pairs.  O is rescaled only when the row max grows by more than 2^8 (the
-//              stale max keeps every P <= 256).  At the end of a unit it copies O out of
-//              TMEM (which frees it for the next unit's P V), divides by the row sum and
-//              writes the rows in 16-column chunks transposed through a 32 x 16 staging tile
-//              per warp, so each store instruction covers 8 rows x 64 contiguous bytes.
+//              bf16 pairs; 32-key chunks hidden from every row of the warp (most of a causal
+//              diagonal tile) are skipped and get P = 0.  O is rescaled only when the row max
+//              grows by more than 2^8 (the stale max keeps every P <= 256).  At the end of a
+//              unit it copies O out of TMEM (which frees it for the next unit's P V), divides
+//              by the row sum and sends the rows out in 16-column chunks through two 32 x 16
+//              staging tiles per warp: TMA tensor stores for token-order rows (the warp moves
+//              on while they drain), plain stores to each row's destination when the rows are
+//              permuted.
 //   warp 8     TMA producer: per unit the slots' Q tiles (once the previous unit's last
 //              Q K^T has read its Q), then K and V tiles (64-column, 128-byte swizzled boxes)
 //              into 2-stage K and V rings that run on across units (a K stage frees as soon
@@ -237,7 +240,8 @@ __device__ __forceinline__ TileRanges tile_ranges(const PrefillArgs& a, const Sl
 template <int D, int DV, int NST>
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmO) {
   using LY = Layout<D, DV, NST>;
   constexpr int DK = (D + 15) / 16 * 16;      // MMA K extent of Q K^T (zero padded)
   constexpr int DN = (DV + 15) / 16 * 16;     // MMA N extent of P V
@@ -286,6 +290,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   }
   if (warp == TMA_WARP && lane == 0) {
     tc::tma_prefetch_desc(&tmK); tc::tma_prefetch_desc(&tmV); tc::tma_prefetch_desc(&tmQ);
+    if (!gather) tc::tma_prefetch_desc(&tmO);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -496,6 +501,16 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         // every lane waits; the vote keeps the warp converged for the .aligned TMEM accesses
         if (!__all_sync(FULL_MASK, mbar_wait_bounded(&s_full[s], (uint32_t)(kk & 1)))) { ok = false; break; }
         tc::fence_after_sync();
+        // visible columns of this row in the tile: [clo, chi).  A 32-column chunk that no row
+        // of the warp sees is not exponentiated (its P is zero).
+        const int clo = rlo - kv0, chi = rhi - kv0;
+        unsigned live = 0u;
+        {
+          const int lo_min = __reduce_min_sync(FULL_MASK, clo), hi_max = __reduce_max_sync(FULL_MASK, chi);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            if (32 * cc < hi_max && 32 * cc + 32 > lo_min) live |= 1u << cc;
+        }
         {
           uint32_t r0[32], r1[32], r2[32], r3[32];
           tc::tmem_ld32(lane_base + s_col, r0);
@@ -509,8 +524,6 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
             x[64 + e] = __uint_as_float(r2[e]); x[96 + e] = __uint_as_float(r3[e]);
           }
         }
-        // visible columns of this row in the tile: [clo, chi)
-        const int clo = rlo - kv0, chi = rhi - kv0;
         if (clo > 0 || chi < BN) {
 #pragma unroll
           for (int e = 0; e < BN; ++e)
@@ -556,13 +569,18 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t w[16];
+          if ((live >> c) & 1u) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float x0, x1;
-            f2split(ffma2(f2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), sc2, nm2), x0, x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);         // hidden keys hold -inf: exp2 -> 0
-            lsum = fadd2(lsum, f2(p0, p1));
-            w[e] = cvt_bf16x2(p0, p1);
+            for (int e = 0; e < 16; ++e) {
+              float x0, x1;
+              f2split(ffma2(f2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), sc2, nm2), x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);       // hidden keys hold -inf: exp2 -> 0
+              lsum = fadd2(lsum, f2(p0, p1));
+              w[e] = cvt_bf16x2(p0, p1);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = 0u;
           }
           tmem_st16(lane_base + s_col + c * 16, w);
         }
@@ -585,12 +603,36 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[s]);
       const float inv = l > 0.f ? 1.0f / l : NAN;
-      // O / l goes out in 16-column chunks, transposed through this warp's staging tile so that
-      // every store instruction writes 8 rows x 64 contiguous bytes: lane r writes its row's
-      // chunk (16-byte piece k at position k ^ ((r >> 1) & 3), conflict-free), then lane
-      // 4 j + q stores piece q of rows j, j + 8, j + 16, j + 24.  Rows outside the sequence
-      // (and, for permuted rows, their token-order destination) are resolved per row.
-      {
+      // O / l goes out in 16-column chunks through this warp's two staging tiles (32 rows x
+      // 64 bytes, 16-byte piece k of row r at position k ^ ((r >> 1) & 3): the tensor map's
+      // 64-byte swizzle, and conflict-free for the row-per-lane writes).
+      if (!gather) {
+        // token-order rows: one TMA store per chunk (rows past the sequence and columns past
+        // the value width are clipped by the tensor map).  A staging tile is rewritten only
+        // once the store issued from it two chunks earlier has read it.
+        const int row0 = sl.qt[s] * BM + quarter * 32;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          uint8_t* buf = stage + (c & 1) * ST_BYTES;
+          if (lane == 0) tc::bulk_wait_read_1();
+          __syncwarp();
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float* xs = x + 16 * c + 4 * k4;
+            *reinterpret_cast<float4*>(buf + lane * 64 + ((k4 ^ ((lane >> 1) & 3)) << 4)) =
+                make_float4(xs[0] * inv, xs[1] * inv, xs[2] * inv, xs[3] * inv);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc::tma_store_4d(&tmO, buf, c * 16, h, row0, n);
+            tc::bulk_commit_group();
+          }
+        }
+      } else {
+        // permuted rows: transposed through the staging tile so that every store instruction
+        // writes 8 rows x 64 contiguous bytes (lane 4 j + q stores piece q of rows j, j + 8,
+        // j + 16, j + 24); each row's token-order destination is resolved per row.
         const int my_row = row_valid ? row : -1;
         float* orow[4];
 #pragma unroll
@@ -638,6 +680,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     }
   }
 
+  if (warp < SOFTMAX_WARPS && lane == 0) tc::bulk_wait_all();   // this warp's output stores are done
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -692,6 +735,22 @@ cudaError_t make_cache_map(CUtensorMap* map, const void* base, const PrefillArgs
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// out [N, S, Hq, Dv] fp32 as (Dv, Hq, S, N): boxes of [32 rows x 16 columns] of one head, with
+// 64-byte swizzle (the layout of the softmax warps' staging tiles).
+cudaError_t make_out_map(CUtensorMap* map, const PrefillArgs& a) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[4] = {(cuuint64_t)a.Dv, (cuuint64_t)a.Hq, (cuuint64_t)a.S, (cuuint64_t)a.N};
+  const cuuint64_t strides[3] = {(cuuint64_t)a.Dv * 4, (cuuint64_t)a.Hq * a.Dv * 4,
+                                 (cuuint64_t)a.S * a.Hq * a.Dv * 4};
+  const cuuint32_t box[4] = {16, 1, 32, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.out, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int prefill_num_sms() {
   static int n[64] = {};
   int dev = 0;
@@ -724,6 +783,9 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if ((e = make_cache_map(&mv, a.vc, a, DV, a.inst_stride_v)) != cudaSuccess) return e;
   if ((e = make_q_map(&mq, a)) != cudaSuccess) return e;
+  CUtensorMap mo;
+  std::memset(&mo, 0, sizeof(mo));           // unused when rows are permuted
+  if (a.row_of_slot == nullptr && (e = make_out_map(&mo, a)) != cudaSuccess) return e;
   // units: the two heads of a GQA pair at one row tile, else two row tiles of one head
   const int nq = (a.S + BM - 1) / BM;
   const int G = a.Hq / a.Hkv;
@@ -731,7 +793,7 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   if (units <= 0) return cudaSuccess;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)std::min<long long>(units, prefill_num_sms());
-  return launch_pdl(prefill_tc_kernel<D, DV, NST>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, a, mk, mv, mq);
+  return launch_pdl(prefill_tc_kernel<D, DV, NST>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, a, mk, mv, mq, mo);
 }
 
 }  // namespace

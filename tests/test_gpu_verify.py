@@ -1,6 +1,6 @@
 """GPU parity of the speculative-decoding verify block (kv_attn_verify) and its commit
 (kv_verify_commit) against the CPU oracle (verify_block, verify_accept): ragged lengths with NaN
-canaries past the valid prefix, block sizes 1..17 over one or two 16-row tiles, group sizes
+canaries past the valid prefix, block sizes 1..33 over one to five 16-row tiles, group sizes
 1/2/4, long contexts split into chunks, and a block of one token against kv_attn_decode."""
 import zlib
 
@@ -28,7 +28,7 @@ def _torch():
 
 @pytest.mark.parametrize("k,G,q_dt", [(1, 2, "bf16"), (2, 2, "bf16"), (5, 2, "f32"), (8, 2, "bf16"),
                                       (16, 2, "bf16"), (17, 2, "f32"), (3, 1, "bf16"), (16, 1, "bf16"),
-                                      (4, 4, "bf16"), (7, 4, "f32")])
+                                      (4, 4, "bf16"), (7, 4, "f32"), (32, 2, "bf16"), (33, 2, "f32")])
 def test_verify_parity(K, k, G, q_dt):
     torch = _torch()
     rng = np.random.default_rng(zlib.crc32(repr(("verify", k, G, q_dt)).encode()))
