@@ -8,7 +8,9 @@
 // tile = K and V as two [16 keys x 64 dims] boxes with 128-byte swizzle, so ldmatrix reads
 // are bank-conflict free) and the warp waits on its own mbarriers.  Per tile:
 //   S = q K^T      16 rows (the G query heads of the group, rest zero) x 16 keys, 16 MMAs
-//   online softmax per row in registers (two xor-shuffles across the row's 4 lanes)
+//   online softmax per row in registers against a reference max that moves only when a
+//   score exceeds it by more than 2^8 (then two xor-shuffles across the row's 4 lanes and an
+//   O rescale; after the first tiles this is rare)
 //   O += P V       P reused from the S accumulator as the A fragment, 16 MMAs
 // About 6 instructions per key and KV head instead of ~40 for CUDA-core dot products, so the
 // kernel is limited by HBM, not by issue.  The warps merge (max, sum, O) in shared memory;
@@ -35,6 +37,13 @@ constexpr int NS = 3;                           // ring stages per warp
 constexpr int BOX = KT * 128;                   // one [16 keys x 64 dims] swizzled box, 2 KB
 constexpr int STAGE = 4 * BOX;                  // K lo, K hi, V lo, V hi
 constexpr int RING = NS * STAGE;                // per warp
+constexpr float RESCALE_LOG2 = 8.0f;            // a row's reference max lags its true max by <= 2^8
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -256,7 +265,10 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   float o[16][4];
 #pragma unroll
   for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m = -INFINITY, l = 0.f;                 // statistics of row r (this lane's query head)
+  // statistics of row r (this lane's query head): m is a reference max, moved only when a score
+  // exceeds it by more than 2^8 (so every P <= 256; the quad's shuffles and the O rescale run
+  // only then); l is this lane's partial sum, reduced over the quad at the end
+  float m = -INFINITY, l = 0.f;
   bool ok = true;
 
   for (int u = 0; u < n_mine; ++u) {
@@ -312,22 +324,24 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
       for (int i = 0; i < 4; ++i) if (kx[i] >= nk) x[i] = -INFINITY;
     }
     float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mt = fmaxf(mt, __shfl_xor_sync(FULL_MASK, mt, 1));
-    mt = fmaxf(mt, __shfl_xor_sync(FULL_MASK, mt, 2));
-    const float m_new = fmaxf(m, mt);           // finite: every tile has a valid key
-    const float alpha = exp2f(m - m_new);       // 0 on the first tile
-    float p[4], ps = 0.f;
+    if (__any_sync(FULL_MASK, mt > m + RESCALE_LOG2)) {
+      mt = fmaxf(mt, __shfl_xor_sync(FULL_MASK, mt, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(FULL_MASK, mt, 2));
+      // quad-uniform (every tile has a valid key, so m is finite after the first tile, where
+      // m = -inf gives alpha = 0 over an empty O)
+      const bool grow = mt > m + RESCALE_LOG2;
+      const float alpha = grow ? ex2(m - mt) : 1.f;
+      if (grow) m = mt;
+      l *= alpha;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) { p[i] = exp2f(x[i] - m_new); }
+      for (int n = 0; n < 16; ++n) { o[n][0] *= alpha; o[n][1] *= alpha; }
+    }
+    float p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = ex2(x[i] - m);    // hidden keys hold -inf: 0
     const uint32_t pa0 = pack_bf16x2(p[0], p[1]);     // keys 2t, 2t+1
     const uint32_t pa2 = pack_bf16x2(p[2], p[3]);     // keys 8+2t, 9+2t
-    ps = bf16_lo(pa0) + bf16_hi(pa0) + bf16_lo(pa2) + bf16_hi(pa2);   // the weights P V uses
-    ps += __shfl_xor_sync(FULL_MASK, ps, 1);
-    ps += __shfl_xor_sync(FULL_MASK, ps, 2);
-    l = l * alpha + ps;
-    m = m_new;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) { o[n][0] *= alpha; o[n][1] *= alpha; }
+    l += (bf16_lo(pa0) + bf16_hi(pa0)) + (bf16_lo(pa2) + bf16_hi(pa2));   // the weights P V uses
 
     // ---- O += P V: 16 n-tiles of 8 dims; ldmatrix.trans gives V as the B fragment ----
     {
@@ -348,6 +362,8 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
       issue(u + NS);
     }
   }
+  l += __shfl_xor_sync(FULL_MASK, l, 1);
+  l += __shfl_xor_sync(FULL_MASK, l, 2);
 
   // ---- merge the warps (rows r < G live in lanes 4r..4r+3) ----
   __syncthreads();                              // rings drained: reuse them for the merge
