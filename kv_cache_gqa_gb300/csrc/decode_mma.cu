@@ -155,6 +155,28 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   if (FUSED && tid < D / 2) {
     r_ih = st.rope.inv_hi[tid]; r_il = st.rope.inv_lo[tid]; r_inv = st.rope.inv[tid]; r_axis = st.rope.axis[tid];
   }
+  // Warm L2 with what the first steps after the wait read: the length, the new token's rows
+  // and (chunk 0 starts at key 0 whatever the length) the warps' first K/V tiles.  Prefetches
+  // return no data, so they may run before the wait: a write by the kernel before this one
+  // still lands in L2, the point of coherence, where the loads after the wait read it.
+  if (tid == 0) prefetch_l2(a.lengths + b);
+  if constexpr (FUSED) {
+    const int eb = st.in_dtype == KVA_BF16 ? 2 : 4;
+    const int qlines = G * D * eb / 128, kvlines = D * eb / 128;   // 128-byte lines
+    const char* qrows = reinterpret_cast<const char*>(st.q) + ((int64_t)b * a.Hq + g * G) * D * eb;
+    const int64_t kvoff = ((int64_t)b * a.Hkv + g) * D * eb;
+    if (tid < qlines) prefetch_l2(qrows + tid * 128);
+    else if (tid < qlines + kvlines) prefetch_l2(reinterpret_cast<const char*>(st.k) + kvoff + (tid - qlines) * 128);
+    else if (tid < qlines + 2 * kvlines)
+      prefetch_l2(reinterpret_cast<const char*>(st.v) + kvoff + (tid - qlines - kvlines) * 128);
+  }
+  if (c == 0 && lane == 0)
+    for (int u = 0; u < NS; ++u) {
+      const int ks = (warp + u * WARPS) * KT;
+      if (ks >= a.capacity) break;
+      tc::tma_prefetch_l2_4d(&tmK, 0, ks, g, b); tc::tma_prefetch_l2_4d(&tmK, 64, ks, g, b);
+      tc::tma_prefetch_l2_4d(&tmV, 0, ks, g, b); tc::tma_prefetch_l2_4d(&tmV, 64, ks, g, b);
+    }
   griddep_wait();                               // inputs of this launch are complete from here on
   griddep_launch_dependents();
   const int L = a.lengths[b];
