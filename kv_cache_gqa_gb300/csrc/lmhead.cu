@@ -280,6 +280,15 @@ lmhead_b1_pipe_kernel(const __grid_constant__ LmheadArgs a, int rows_per_cta) {
     for (int st = 0; st < PIPE_STAGES; ++st) { mbar_init(&full[st], 1); mbar_init(&empty[st], PIPE_WARPS); }
     fence_mbar_init();
   }
+  // Warm L2 with the first stages of this CTA's slice and with h while the kernel before this
+  // one drains (prefetches return no data, so they may run before the wait: a write by that
+  // kernel still lands in L2, the point of coherence, where the copies after the wait read it)
+  if (tid < PIPE_STAGES && tid < n_st) {
+    const int rs = r0 + tid * RPS;
+    bulk_prefetch_l2(W + (int64_t)rs * ROWB, (uint32_t)(min(RPS, r1 - rs) * ROWB));
+  } else if (tid >= 32 && tid < 32 + H * 4 / 128) {
+    prefetch_l2(reinterpret_cast<const char*>(a.h) + (tid - 32) * 128);
+  }
   griddep_wait();                               // h (and the table) are complete from here on
   griddep_launch_dependents();
   if (tid == 0)
