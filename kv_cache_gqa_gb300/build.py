@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkv_attn.so")
 SOURCES = ["kv_attn_api.cu", "append.cu", "append_general.cu", "decode.cu", "decode_mma.cu", "decode_static.cu", "lmhead.cu", "lmhead_tc.cu", "lmhead_topk.cu",
-           "prefill_simt.cu", "prefill_tc.cu", "verify_mma.cu"]
+           "prefill_simt.cu", "prefill_tc.cu", "verify_mma.cu", "verify_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

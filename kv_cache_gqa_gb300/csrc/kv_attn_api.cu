@@ -520,7 +520,10 @@ kva_status kv_attn_verify(
       return fail(KVA_ECAPACITY, "length %d of instance %d outside [k=%d, %d]", L, b, k, cache.capacity);
     max_len = std::max(max_len, L);
   }
-  const int chunk = decode_plan_chunk(lengths_host, B, Hkv * RT, max_len);
+  // the tcgen05 form reads q and writes out with 16-byte accesses
+  const bool tc_form = verify_tc_supports(G, k) && aligned16(q) && aligned16(out);
+  const int chunk = tc_form ? verify_tc_plan_chunk(lengths_host, B, Hkv, max_len)
+                            : decode_plan_chunk(lengths_host, B, Hkv * RT, max_len);
   const int max_chunks = (max_len + chunk - 1) / chunk;
   const size_t need = decode_ws_bytes(B, Hkv * RT, Hkv * RT * 16, max_chunks, D);
   if (workspace_bytes < need)
@@ -536,7 +539,8 @@ kva_status kv_attn_verify(
   a.chunk = chunk; a.max_chunks = max_chunks; a.inst_stride = cache.inst_stride;
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   a.scale_log2 = sc * 1.4426950408889634f;
-  cudaError_t e = launch_verify(a, q_dtype, (cudaStream_t)stream);
+  cudaError_t e = tc_form ? launch_verify_tc(a, q_dtype, (cudaStream_t)stream)
+                          : launch_verify(a, q_dtype, (cudaStream_t)stream);
   if (e == cudaSuccess) count_launches(1);
   return cuda_status(e, "verify launch");
 }

@@ -87,6 +87,11 @@ struct VerifyArgs {
   float scale_log2;
 };
 cudaError_t launch_verify(const VerifyArgs& a, kva_dtype q_dtype, cudaStream_t s);
+// tcgen05 form (a group of G*k <= 128 rows on one 128-row MMA tile): persistent CTAs over
+// (chunk, KV head, instance) units.  `chunk` is planned by verify_tc_plan_chunk.
+bool verify_tc_supports(int G, int k);
+int verify_tc_plan_chunk(const int32_t* lengths_host, int B, int Hkv, int max_len);
+cudaError_t launch_verify_tc(const VerifyArgs& a, kva_dtype q_dtype, cudaStream_t s);
 // (D=128 bf16 cache) 4-D TMA map over a cache with boxes of [16 slots x 64 dims].
 cudaError_t decode_cache_map(CUtensorMap* map, const void* base, int capacity, int Hkv, int B, int64_t inst_stride);
 // Acceptance and commit of verify blocks (one thread per instance).
