@@ -18,7 +18,7 @@
 //              that the last unit of (b, g) to finish merges).  Query rows live in two buffers
 //              (units alternate); fp32 rows are rounded to bf16 and staged by slot 1 for the
 //              next unit as soon as it has published its statistics.
-//   warp 8     TMA producer: bf16 query rows of each unit (one [64 dims x G heads x k
+//   warp 10    TMA producer: bf16 query rows of each unit (one [64 dims x G heads x k
 //              positions] box per half row, landing in (position, head) row order), K and V
 //              tiles ([128 keys x 64 dims] boxes, 128-byte swizzle) of every unit in walk order
 //              into a 3-stage K ring and a 2-stage V ring.
@@ -45,8 +45,11 @@ namespace {
 constexpr int D = DECODE_HEAD_DIM;        // 128
 constexpr int BM = 128;                   // rows of the tile = TMEM lanes
 constexpr int BN = 128;                   // keys per tile
-constexpr int THREADS = 384;              // 8 softmax warps; TMA warp, MMA warp, 2 idle
-constexpr int TMA_WARP = 8, MMA_WARP = 9;
+// 8 softmax warps; warps 8-11: MMA (9) and TMA (10) issuers, two idle.  With a group of at
+// most 32 rows only warps 0 and 4 (both on sub-partition 0, the only ones that reach TMEM
+// lanes 0-31) do softmax work, so the issuers sit on sub-partitions 1 and 2.
+constexpr int THREADS = 384;
+constexpr int TMA_WARP = 10, MMA_WARP = 9;
 // Registers per thread: 168 at launch (three warps per SM sub-partition); the control
 // warpgroup gives up 48 per thread, which the two softmax warpgroups take:
 // 128 * (192 + 192 + 120) = 384 * 168, so the increase never waits on registers nobody frees.
