@@ -246,12 +246,12 @@ lmhead_b1_kernel(const __grid_constant__ LmheadArgs a) {
 
 // ---------------------------------------------------------------------------------
 // Batch-1 pipelined path: one CTA per SM owns a contiguous slice of the table and streams it
-// through a 4-stage shared-memory ring, one 32 KB bulk copy per stage (the slice's rows are
-// contiguous in memory).  Bytes in flight cost no registers, so each SM keeps ~96 KB moving.
+// through a 5-stage shared-memory ring, one 32 KB bulk copy per stage (the slice's rows are
+// contiguous in memory).  Bytes in flight cost no registers, so each SM keeps ~128 KB moving.
 // The 8 warps reduce the staged rows with conflict-free 128-bit shared-memory reads.
 // ---------------------------------------------------------------------------------
 constexpr int PIPE_STAGE_BYTES = 32768;
-constexpr int PIPE_STAGES = 4;
+constexpr int PIPE_STAGES = 5;
 constexpr int PIPE_THREADS = 256;
 constexpr int PIPE_WARPS = PIPE_THREADS / 32;
 
