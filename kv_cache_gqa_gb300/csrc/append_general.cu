@@ -55,6 +55,7 @@ append_general_kernel(const __grid_constant__ AppendArgs a) {
   const int n_rows = a.Hq + 2 * a.Hkv;
   const float* qw = a.q_w ? a.q_w + (int64_t)n * a.w_stride : nullptr;
   const float* kw = a.k_w ? a.k_w + (int64_t)n * a.w_stride : nullptr;
+  griddep_wait();                               // inputs of this launch are complete from here on
   const int32_t slot = a.slot[(int64_t)n * a.slot_stride + t];
   const int64_t tok = (int64_t)n * a.T + t;
 
@@ -149,6 +150,9 @@ append_general_kernel(const __grid_constant__ AppendArgs a) {
         store8(reinterpret_cast<CacheT*>(a.vc) + (int64_t)n * a.inst_stride_v + ((int64_t)head * a.capacity + slot) * Dv + e0, x);
     }
   }
+  // the next kernel may start its set-up only as this CTA finishes: a long (many-wave) append
+  // must not have its SMs taken by a waiting persistent kernel
+  griddep_launch_dependents();
 }
 
 int gen_num_sms() {
@@ -169,9 +173,8 @@ cudaError_t launch_c(const AppendArgs& a, kva_dtype cache_dtype, cudaStream_t s)
   const int max_groups = (n_rows + GEN_WARPS - 1) / GEN_WARPS;
   const int groups = (int)std::max<int64_t>(1, std::min<int64_t>(max_groups, 2 * gen_num_sms() / std::max<int64_t>(1, tokens)));
   dim3 grid(a.T, a.N, std::min(groups, 65535));
-  if (cache_dtype == KVA_BF16) append_general_kernel<InT, QOutT, bf16_t><<<grid, GEN_THREADS, 0, s>>>(a);
-  else append_general_kernel<InT, QOutT, float><<<grid, GEN_THREADS, 0, s>>>(a);
-  return cudaGetLastError();
+  if (cache_dtype == KVA_BF16) return launch_pdl(append_general_kernel<InT, QOutT, bf16_t>, grid, dim3(GEN_THREADS), 0, s, a);
+  return launch_pdl(append_general_kernel<InT, QOutT, float>, grid, dim3(GEN_THREADS), 0, s, a);
 }
 
 template <typename InT>

@@ -81,17 +81,28 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
 
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int L = a.lengths[b];
-  const int n_chunks = (L + a.chunk - 1) / a.chunk;
-  if (c >= n_chunks) return;
-  const int k0 = c * a.chunk;
-  const int k1 = min(L, k0 + a.chunk);
-  const int n_sub = (k1 - k0 + KT - 1) / KT;
-
   const unsigned char* Kg = reinterpret_cast<const unsigned char*>(a.kc) +
       ((int64_t)b * a.inst_stride + (int64_t)g * a.capacity * DK) * ES;
   const unsigned char* Vg = reinterpret_cast<const unsigned char*>(a.vc) +
       ((int64_t)b * a.inst_stride_v + (int64_t)g * a.capacity * D) * ES;
+  const int k0 = c * a.chunk;
+  // Warm L2 with the length and the chunk's first stages while the kernel before this one
+  // drains (prefetches return no data, so they may run before the wait: a write by that kernel
+  // still lands in L2, where the copies after the wait read it)
+  if (tid == 0) {
+    prefetch_l2(a.lengths + b);
+    if (k0 + NSTAGE * KT <= a.capacity) {
+      bulk_prefetch_l2(Kg + (int64_t)k0 * ROWK, (uint32_t)(NSTAGE * TILEK));
+      bulk_prefetch_l2(Vg + (int64_t)k0 * ROWB, (uint32_t)(NSTAGE * TILEB));
+    }
+  }
+  griddep_wait();                               // inputs of this launch are complete from here on
+  griddep_launch_dependents();
+  const int L = a.lengths[b];
+  const int n_chunks = (L + a.chunk - 1) / a.chunk;
+  if (c >= n_chunks) return;
+  const int k1 = min(L, k0 + a.chunk);
+  const int n_sub = (k1 - k0 + KT - 1) / KT;
 
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(&full[s], 1);
@@ -311,8 +322,7 @@ cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
     configured = true;
   }
   dim3 grid(a.max_chunks, a.Hkv, a.B);
-  decode_kernel<CacheT, G, DK><<<grid, THREADS, smem, s>>>(a, q_dtype);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel<CacheT, G, DK>, grid, dim3(THREADS), smem, s, a, q_dtype);
 }
 
 template <typename CacheT, int DK>
