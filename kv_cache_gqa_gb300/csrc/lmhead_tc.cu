@@ -43,6 +43,8 @@ lmhead_split_kernel(const float* __restrict__ h, const float* __restrict__ norm_
                     int B, int Bp, int H) {
   const int b = blockIdx.x, tid = threadIdx.x;
   __shared__ float s_part[8];
+  griddep_wait();                               // h is complete from here on
+  griddep_launch_dependents();
   float r = 1.f;
   if (norm_w && b < B) {
     float ss = 0.f;
@@ -107,11 +109,19 @@ lmhead_tc_kernel(const __grid_constant__ LmheadArgs a, const __grid_constant__ C
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_taddr;
+  // Warm L2 with this CTA's first W stages while the kernels before drain (prefetches return no
+  // data, so they may run before the wait), then wait for the split rows of h
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&tmW);
+    tc::tma_prefetch_desc(&tmH);
+    for (int it = 0; it < NSTAGE && it < my_tiles * kchunks; ++it)
+      tc::tma_prefetch_l2_4d(&tmW, (it % kchunks) * KC, (blockIdx.x + (it / kchunks) * gridDim.x) * TM, 0, 0);
+  }
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
-      tc::tma_prefetch_desc(&tmW);
-      tc::tma_prefetch_desc(&tmH);
       int it = 0;
       for (int lt = 0; lt < my_tiles; ++lt) {
         const int tile = blockIdx.x + lt * gridDim.x;
@@ -275,16 +285,14 @@ cudaError_t launch_bp(const LmheadArgs& a, uint16_t* hb, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  lmhead_split_kernel<<<BP, 256, 0, s>>>(a.h, a.norm_w, a.eps, hb, a.B, BP, a.H);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(lmhead_split_kernel, dim3(BP), dim3(256), 0, s, a.h, a.norm_w, a.eps, hb, a.B, BP, a.H);
   if (e != cudaSuccess) return e;
   CUtensorMap mw, mh;
   if ((e = make_map(&mw, a.W, a.H, a.V, TM)) != cudaSuccess) return e;
   if ((e = make_map(&mh, hb, a.H, N, N)) != cudaSuccess) return e;
   const int n_tiles = (a.V + TM - 1) / TM;
   const int grid = std::min(n_tiles, num_sms_tc());
-  lmhead_tc_kernel<BP><<<grid, THREADS, smem, s>>>(a, mw, mh);
-  return cudaGetLastError();
+  return launch_pdl(lmhead_tc_kernel<BP>, dim3(grid), dim3(THREADS), (size_t)smem, s, a, mw, mh);
 }
 
 }  // namespace
