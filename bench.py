@@ -525,6 +525,13 @@ def run_gpu(args, rank, world, local_rank):
         K.lmhead_topk(job.h[1], job.W, tk_ids8, tk_ws, norm_w=fn_w)   # configures the kernels before capture
     torch.cuda.synchronize()
     lm_norm_ms = graph_avg_ms(torch, stream, lambda: K.lmhead_topk(job.h[1], job.W, tk_ids1, tk_ws, norm_w=fn_w), 32)
+    # the prompt's append and prefill alone, each as a graph of back-to-back launches (inputs
+    # and outputs larger than L2); the in-job figures above also carry an event node's latency
+    app_iso_ms = graph_avg_ms(torch, stream, lambda: K.kv_cache_append_rope_qknorm(
+        job.q, job.k, job.v, job.pre_pos_d, job.pre_slot_d, job.pre_slot, job.cache, job.q_pre, job.rope,
+        q_norm_w=job.qw, k_norm_w=job.kw, eps=1e-6, norm_inst_stride=D), 8)
+    pre_iso_ms = graph_avg_ms(torch, stream, lambda: K.kv_attn_prefill(job.q_pre, job.cache, job.out_pre,
+                                                                        mask="causal"), 8)
     lm_top8_ms = graph_avg_ms(torch, stream, lambda: K.lmhead_topk(job.h[1], job.W, tk_ids8, tk_ws, norm_w=fn_w), 32)
 
     # speculative-decoding verify block on a cache larger than L2: 64 sequences x 2048 slots,
@@ -633,9 +640,13 @@ def run_gpu(args, rank, world, local_rank):
                                 "avg_launch_us": round(in_job["decode"] * 1e3, 2),
                                 "algorithmic_bytes_per_launch": int(np.mean(dec_bytes))},
                 "prefill_attn": {"TFLOP/s": round(pre_tf, 2), "frac_bf16": round(pre_tf / bf16, 4),
-                                 "launch_us": round(in_job["prefill"] * 1e3, 1), "flops": prefill_flops()},
+                                 "launch_us": round(in_job["prefill"] * 1e3, 1), "flops": prefill_flops(),
+                                 "alone_us": round(pre_iso_ms * 1e3, 1),
+                                 "alone_frac_bf16": round(prefill_flops() / (pre_iso_ms / 1e3) / 1e12 / bf16, 4)},
                 "append_prefill": {"GB/s": round(app_gbs, 1), "frac_hbm": round(app_gbs / hbm, 4),
-                                   "launch_us": round(in_job["append_pre"] * 1e3, 1)},
+                                   "launch_us": round(in_job["append_pre"] * 1e3, 1),
+                                   "alone_us": round(app_iso_ms * 1e3, 1),
+                                   "alone_frac_hbm": round(append_bytes(LAYERS * PROMPT) / (app_iso_ms / 1e3) / 1e9 / hbm, 4)},
                 "lm_head": {"GB/s": round(lm_gbs, 1), "frac_hbm": round(lm_gbs / hbm, 4),
                             "avg_launch_us": round(lm_iso_ms * 1e3, 2)},
                 "verify_block": dict(vb, frac_hbm=round(vb["GB/s"] / hbm, 4)),
