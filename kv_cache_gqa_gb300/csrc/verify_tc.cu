@@ -21,7 +21,8 @@
 //   warp 10    TMA producer: bf16 query rows of each unit (one [64 dims x G heads x k
 //              positions] box per half row, landing in (position, head) row order), K and V
 //              tiles ([128 keys x 64 dims] boxes, 128-byte swizzle) of every unit in walk order
-//              into a 3-stage K ring and a 2-stage V ring.
+//              into a 2-stage K ring and a 3-stage V ring (a K stage frees at its Q K^T, early;
+//              a V stage only at its P V, after the softmax).
 //   warp 9     MMA issuer (one thread): S_s = Q K^T into slot s's columns [128 s, 128 s + 128),
 //              O_s += P_s V into [256 + 128 s, ...); tensor-core operations of one thread run in
 //              issue order, so a slot's next Q K^T is issued right behind its P V.
@@ -55,7 +56,7 @@ constexpr int TMA_WARP = 10, MMA_WARP = 9;
 // 128 * (192 + 192 + 120) = 384 * 168, so the increase never waits on registers nobody frees.
 constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 192, REGS_CONTROL = 120;
 static_assert(2 * REGS_SOFTMAX + REGS_CONTROL <= 3 * REGS_LAUNCH, "register split exceeds the launch total");
-constexpr int NK = 3, NV = 2;             // K and V ring stages
+constexpr int NK = 2, NV = 3;             // K and V ring stages
 constexpr int SUB = BM * 128;             // one [128 rows x 64 bf16] swizzled box, 16 KB
 constexpr int Q_OFF = 0;                  // 2 buffers x 2 boxes (units alternate)
 constexpr int K_OFF = Q_OFF + 4 * SUB;    // NK x 2 boxes
@@ -130,20 +131,21 @@ verify_tc_kernel(const __grid_constant__ VerifyArgs a, const __grid_constant__ C
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + BAR_OFF);
-  uint64_t* k_full = bars + 0;     // [NK] K tile landed
-  uint64_t* k_free = bars + 3;     // [NK] its Q K^T done
-  uint64_t* v_full = bars + 6;     // [NV] V tile landed
-  uint64_t* v_free = bars + 8;     // [NV] its P V done
-  uint64_t* s_full = bars + 10;    // [slot] S in tensor memory
-  uint64_t* p_full = bars + 12;    // [slot] P written by the slot's row-holding warps
-  uint64_t* pv_done = bars + 14;   // [slot] the slot's last P V finished
-  uint64_t* o_full = bars + 16;    // [slot] the unit's last P V of the slot finished
-  uint64_t* o_free = bars + 18;    // [slot] O read out by slot 0's warps
-  uint64_t* q_full = bars + 20;    // [buffer] the unit's query rows staged
-  uint64_t* q_free = bars + 22;    // [buffer] the unit's last Q K^T done: the rows may be replaced
-  uint64_t* ml_ready = bars + 24;  // slot 1's row max and sum published
-  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(bars + 25);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 26);
+  uint64_t* k_full = bars;                     // [NK] K tile landed
+  uint64_t* k_free = k_full + NK;              // [NK] its Q K^T done
+  uint64_t* v_full = k_free + NK;              // [NV] V tile landed
+  uint64_t* v_free = v_full + NV;              // [NV] its P V done
+  uint64_t* s_full = v_free + NV;              // [slot] S in tensor memory
+  uint64_t* p_full = s_full + 2;               // [slot] P written by the slot's row-holding warps
+  uint64_t* pv_done = p_full + 2;              // [slot] the slot's last P V finished
+  uint64_t* o_full = pv_done + 2;              // [slot] the unit's last P V of the slot finished
+  uint64_t* o_free = o_full + 2;               // [slot] O read out by slot 0's warps
+  uint64_t* q_full = o_free + 2;               // [buffer] the unit's query rows staged
+  uint64_t* q_free = q_full + 2;               // [buffer] the unit's last Q K^T done: the rows may be replaced
+  uint64_t* ml_ready = q_free + 2;             // slot 1's row max and sum published
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(ml_ready + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(ml_ready + 2);
+  static_assert((2 * (NK + NV) + 17) * 8 <= 256, "barrier area");
   const bool tma_q = q_dtype == KVA_BF16;   // bf16 rows come by TMA, fp32 rows are staged by slot 1
   float* ml = reinterpret_cast<float*>(sm + ML_OFF);
 

@@ -2,7 +2,8 @@
 
 Roles: the TMA producer, the MMA issuer and the softmax warps of the two slots (each slot acts
 as one party).  A CTA walks a list of work units of n >= 1 key tiles; tile e of a unit belongs
-to slot e & 1.  K runs through a 3-stage ring and V through a 2-stage ring across units; the
+to slot e & 1.  K and V run through rings of 2 and 3 stages (the kernel; 3 and 2 are replayed
+too) across units; the
 query rows of consecutive units alternate between two buffers and come either by TMA (the
 producer, once the unit two back has run its last Q K^T) or from slot 1's threads (right after
 it has published the previous unit's row statistics).  At a unit's end slot 1 publishes its
@@ -16,7 +17,7 @@ import random
 
 import pytest
 
-NK, NV = 3, 2
+RINGS = [(2, 3), (3, 2)]      # (K stages, V stages): the kernel's, and the swapped depths
 
 
 class Bar:
@@ -41,7 +42,8 @@ def tiles(n, s):
     return (n - s + 1) // 2
 
 
-def run(units, seed, tma_q=True, ragged=(), rescale_p=0.3, drop_o_free_waits=False):
+def run(units, seed, tma_q=True, ragged=(), rescale_p=0.3, drop_o_free_waits=False, rings=(2, 3)):
+    NK, NV = rings
     rnd = random.Random(seed)
     k_full = [Bar(1) for _ in range(NK)]; k_free = [Bar(1) for _ in range(NK)]
     v_full = [Bar(1) for _ in range(NV)]; v_free = [Bar(1) for _ in range(NV)]
@@ -180,15 +182,16 @@ def _unit_lists(seed, count):
     return [[rnd.randint(1, 6) for _ in range(rnd.randint(1, 6))] for _ in range(count)]
 
 
+@pytest.mark.parametrize("rings", RINGS)
 @pytest.mark.parametrize("tma_q", [True, False])
 @pytest.mark.parametrize("seed", [0, 1, 2])
-def test_verify_unit_walk_phases_stay_in_step(seed, tma_q):
+def test_verify_unit_walk_phases_stay_in_step(seed, tma_q, rings):
     """Random unit lists (1 to 6 tiles per unit, odd counts leave slot 1 a tile short, a single
     tile leaves it none), both query paths, ragged last tiles and random O rescales."""
     for i, units in enumerate(_unit_lists(seed, 120)):
         rnd = random.Random(i)
         ragged = {u for u in range(len(units)) if rnd.random() < 0.5}
-        run(units, seed * 1000 + i, tma_q=tma_q, ragged=ragged)
+        run(units, seed * 1000 + i, tma_q=tma_q, ragged=ragged, rings=rings)
 
 
 def test_single_tile_units_leave_slot_one_idle():
