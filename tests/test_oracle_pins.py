@@ -159,6 +159,34 @@ def test_norm_rope_order():
     assert np.max(np.abs(a - b)) > 1e-3                          # the flag matters
 
 
+def test_norm_rope_order_direction_hand_worked():
+    # D = 4, base 100: inv = [1, 0.1]; position 1 turns pair (0, 2) by 1 rad and pair (1, 3)
+    # by 0.1 rad.  w = [2, 0.5, 1, 1], eps = 0.
+    #   x = e0:  norm first:  e0 / sqrt(1/4) * w = [4, 0, 0, 0]      -> RoPE [4 cos 1, 0, 4 sin 1, 0]
+    #            RoPE first:  [cos 1, 0, sin 1, 0] / (1/2) * w       -> [4 cos 1, 0, 2 sin 1, 0]
+    #   x = e1:  norm first:  [0, 1, 0, 0]                            -> [0, cos .1, 0, sin .1]
+    #            RoPE first:  [0, 2 cos .1, 0, 2 sin .1] * w          -> [0, cos .1, 0, 2 sin .1]
+    # Qwen3 normalises, then rotates (Penguin-VL port, section 5.4: q_proj, q_norm, q_rope);
+    # HunyuanOCR rotates, then normalises, before the cache write (HunyuanOCR v1.0 port,
+    # section five item 2).  The flag names the second order.
+    rope = O.Rope("1d", base=100.0)
+    w = np.array([2.0, 0.5, 1.0, 1.0])
+    x = np.zeros((2, 1, 4)); x[0, 0, 0] = 1.0; x[1, 0, 1] = 1.0
+    pos = np.array([[1], [1]])
+    c1, s1, c2, s2 = math.cos(1.0), math.sin(1.0), math.cos(0.1), math.sin(0.1)
+    norm_then_rope = [[4 * c1, 0, 4 * s1, 0], [0, c2, 0, s2]]
+    rope_then_norm = [[4 * c1, 0, 2 * s1, 0], [0, c2, 0, 2 * s2]]
+    a = O.qk_transform(x, pos, w, 0.0, rope, norm_after_rope=False)[:, 0]
+    b = O.qk_transform(x, pos, w, 0.0, rope, norm_after_rope=True)[:, 0]
+    np.testing.assert_allclose(a, norm_then_rope, rtol=1e-15, atol=1e-16)
+    np.testing.assert_allclose(b, rope_then_norm, rtol=1e-15, atol=1e-16)
+    # the cache append takes the same flag for q and for k
+    ck = np.zeros((1, 2, 4)); cv = np.zeros((1, 2, 4))
+    qr = O.cache_append(x, x, x, pos, [0, 1], w, w, 0.0, rope, True, ck, cv, "f32")
+    np.testing.assert_allclose(qr[:, 0], rope_then_norm, rtol=1e-15, atol=1e-16)
+    np.testing.assert_allclose(ck[0], np.float32(rope_then_norm).astype(np.float64), rtol=0, atol=0)
+
+
 # ----------------------------------------------------------------------------
 # bf16 storage
 # ----------------------------------------------------------------------------
