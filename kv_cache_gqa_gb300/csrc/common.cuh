@@ -64,10 +64,12 @@ __device__ __forceinline__ float load1(const bf16_t* p) { return __uint_as_float
 
 // ---------------------------------------------------------------------------
 // Ordered 64-bit keys for an argmax with ties toward the lowest index:
-// the high word orders float values, the low word holds ~index.
+// the high word orders float values, the low word holds ~index.  -0.0 is keyed as +0.0,
+// so a logit of -0 and one of +0 are equal and the lower index wins.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t float_order_bits(float f) {
-  const uint32_t u = __float_as_uint(f);
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ float float_from_order_bits(uint32_t k) {

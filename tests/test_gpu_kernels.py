@@ -403,3 +403,18 @@ def test_lmhead_ties_lowest_id_last_row_and_clamp(K):
     torch.cuda.synchronize()
     got = ids.cpu().numpy()
     assert got[0] == 17 and got[1] == 0 and got[2] == 17
+    # a +0 / -0 tie: with h = 2^-100 a row of -2^-100 weights gives products that round to
+    # -0, so its logit is -0.0; a row of zeros gives +0.0; every other row is negative.
+    # The two zeros are equal logits, so the lower id wins whichever sign it carries.
+    tiny = 2.0 ** -100
+    for lo_row, hi_row, lo_val, hi_val in ((5, 4000, -tiny, 0.0), (5, 4000, 0.0, -tiny)):
+        W = np.full((Vrows, H), -1.0, np.float32)
+        W[lo_row] = lo_val
+        W[hi_row] = hi_val
+        for Wd in (dev(W), dev(W).to(torch.bfloat16)):           # exact in both dtypes
+            for B in (1, 4):
+                hz = np.full((B, H), tiny, np.float32)
+                ids = torch.empty((B,), dtype=torch.int32, device="cuda")
+                K.lmhead_argmax(dev(hz), Wd, ids, ws, V=Vrows)
+                torch.cuda.synchronize()
+                assert np.all(ids.cpu().numpy() == lo_row), (Wd.dtype, B, lo_val, ids.cpu().numpy())
