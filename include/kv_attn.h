@@ -283,7 +283,9 @@ size_t kva_decode_workspace_zero_bytes(int32_t B, int32_t n_kv_heads);
  *   until the partials fit.
  *  The call allocates nothing (no cudaMalloc, no cudaFree).  The first call on a device
  *   looks up the array's device address (cudaGetSymbolAddress); make that first call
- *   before any stream capture.  Every call clears the merge counters it needs on `stream`.
+ *   before any stream capture.  The address is kept for the life of the process, so do not
+ *   use the library across a cudaDeviceReset.  Every call clears the merge counters it needs
+ *   on `stream`.
  *  All calls share the one array, which keeps the last call's contents: calls that
  *   overlap on the GPU (different streams, or concurrent graphs) race on it and must be
  *   serialised by the caller. */
@@ -339,6 +341,38 @@ size_t kva_lmhead_topk_workspace_size(int32_t B, int32_t H, int32_t V, int32_t t
 
 size_t kva_lmhead_workspace_size(int32_t B, int32_t H);
 size_t kva_lmhead_workspace_zero_bytes(int32_t B);
+
+/* ---------------------------------------------------------------------------------
+ * kva_workspace_size
+ *   One sizer for every call that takes a workspace (the boundary lists a single
+ *   kva_workspace_size(which, ...)); it returns what the per-call sizer above returns for
+ *   the same dimensions.  `which` names the call; the fields of `dims` it reads:
+ *     KVA_WS_DECODE        kv_attn_decode, kv_attn_decode_step:
+ *                          B, n_kv_heads, n_q_heads, max_len, head_dim (Dv)
+ *     KVA_WS_VERIFY        kv_attn_verify: the same plus block (k)
+ *     KVA_WS_LMHEAD        lmhead_argmax: B, hidden
+ *     KVA_WS_LMHEAD_TOPK   lmhead_topk: B, hidden, vocab, block (top_k)
+ *   Fields a kind does not read are ignored.  Returns 0 for an unknown kind, a NULL `dims` or
+ *   a dimension that is not positive. */
+typedef enum {
+  KVA_WS_DECODE = 0,
+  KVA_WS_VERIFY = 1,
+  KVA_WS_LMHEAD = 2,
+  KVA_WS_LMHEAD_TOPK = 3
+} kva_workspace_kind;
+
+typedef struct {
+  int32_t B;
+  int32_t n_kv_heads;
+  int32_t n_q_heads;
+  int32_t max_len;   /* largest valid length L any call will pass */
+  int32_t head_dim;  /* value head width Dv of the attention output */
+  int32_t hidden;    /* lm_head hidden size H */
+  int32_t vocab;     /* lm_head candidate rows V */
+  int32_t block;     /* verify block length k, or top_k */
+} kva_workspace_dims;
+
+size_t kva_workspace_size(int32_t which, const kva_workspace_dims* dims);
 
 /* ---------------------------------------------------------------------------------
  * Introspection */

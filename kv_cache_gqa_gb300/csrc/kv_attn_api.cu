@@ -247,6 +247,18 @@ size_t kva_lmhead_workspace_zero_bytes(int32_t B) {
   return lmhead_zero_bytes(B);
 }
 
+size_t kva_workspace_size(int32_t which, const kva_workspace_dims* d) {
+  if (!d) return 0;
+  switch (which) {
+    case KVA_WS_DECODE: return kva_decode_workspace_size(d->B, d->n_kv_heads, d->n_q_heads, d->max_len, d->head_dim);
+    case KVA_WS_VERIFY:
+      return kva_verify_workspace_size(d->B, d->n_kv_heads, d->n_q_heads, d->block, d->max_len, d->head_dim);
+    case KVA_WS_LMHEAD: return kva_lmhead_workspace_size(d->B, d->hidden);
+    case KVA_WS_LMHEAD_TOPK: return kva_lmhead_topk_workspace_size(d->B, d->hidden, d->vocab, d->block);
+  }
+  return 0;
+}
+
 kva_status kv_cache_append_rope_qknorm(
     const void* q, const void* k, const void* v, kva_dtype in_dtype,
     int32_t N, int32_t T, int32_t n_q_heads,

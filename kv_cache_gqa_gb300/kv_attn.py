@@ -46,6 +46,13 @@ class _Norm(C.Structure):
                 ("eps", C.c_float), ("after_rope", C.c_int32)]
 
 
+class _WorkspaceDims(C.Structure):
+    _fields_ = [("B", C.c_int32), ("n_kv_heads", C.c_int32), ("n_q_heads", C.c_int32), ("max_len", C.c_int32),
+                ("head_dim", C.c_int32), ("hidden", C.c_int32), ("vocab", C.c_int32), ("block", C.c_int32)]
+
+
+WORKSPACE_KINDS = {"decode": 0, "verify": 1, "lmhead": 2, "lmhead_topk": 3}
+
 _lib = None
 
 
@@ -87,6 +94,8 @@ def lib() -> C.CDLL:
         L.kva_lmhead_workspace_size.restype = sz
         L.kva_lmhead_workspace_zero_bytes.argtypes = [i32]
         L.kva_lmhead_workspace_zero_bytes.restype = sz
+        L.kva_workspace_size.argtypes = [i32, C.POINTER(_WorkspaceDims)]
+        L.kva_workspace_size.restype = sz
         L.kva_strerror.argtypes = [C.c_int]
         L.kva_strerror.restype = C.c_char_p
         L.kva_last_error.restype = C.c_char_p
@@ -230,6 +239,14 @@ def decode_workspace_bytes(B: int, n_kv_heads: int, n_q_heads: int, max_len: int
 
 def lmhead_workspace_bytes(B: int, H: int = 1024) -> int:
     return int(lib().kva_lmhead_workspace_size(B, H))
+
+
+def workspace_bytes(kind: str, B: int = 0, n_kv_heads: int = 0, n_q_heads: int = 0, max_len: int = 0,
+                    head_dim: int = 0, hidden: int = 0, vocab: int = 0, block: int = 0) -> int:
+    """kva_workspace_size: the workspace of the call `kind` names ('decode', 'verify', 'lmhead',
+    'lmhead_topk'); 0 for dimensions that are not positive."""
+    d = _WorkspaceDims(B, n_kv_heads, n_q_heads, max_len, head_dim, hidden, vocab, block)
+    return int(lib().kva_workspace_size(WORKSPACE_KINDS[kind], C.byref(d)))
 
 
 def kv_attn_decode(q, cache: KVCache, lengths, lengths_host, out, workspace, scale: float = 0.0,

@@ -40,6 +40,28 @@ def test_exports_every_declared_symbol(K):
         assert hasattr(K.lib(), n), f"libkv_attn.so does not export {n}"
 
 
+def test_workspace_size_dispatcher_matches_the_per_call_sizers(K):
+    L = K.lib()
+    for B, Hkv, Hq, Lmax, D in ((1, 8, 16, 80, 128), (28, 8, 16, 768, 128), (64, 8, 16, 32896, 128),
+                                (16, 32, 32, 512, 128), (3, 2, 8, 5000, 128)):
+        want = L.kva_decode_workspace_size(B, Hkv, Hq, Lmax, D)
+        assert want > 0 and K.workspace_bytes("decode", B=B, n_kv_heads=Hkv, n_q_heads=Hq, max_len=Lmax,
+                                              head_dim=D) == want
+        for k in (1, 4, 17):
+            assert K.workspace_bytes("verify", B=B, n_kv_heads=Hkv, n_q_heads=Hq, max_len=Lmax, head_dim=D,
+                                     block=k) == L.kva_verify_workspace_size(B, Hkv, Hq, k, Lmax, D) > 0
+    for B, H, V in ((1, 1024, 151936), (64, 1024, 151936), (5, 512, 4099)):
+        assert K.workspace_bytes("lmhead", B=B, hidden=H) == L.kva_lmhead_workspace_size(B, H) > 0
+        for k in (1, 8):
+            assert K.workspace_bytes("lmhead_topk", B=B, hidden=H, vocab=V, block=k) == \
+                L.kva_lmhead_topk_workspace_size(B, H, V, k) > 0
+    # an unknown kind, a NULL descriptor or a dimension that is not positive: 0
+    assert L.kva_workspace_size(7, C.byref(K._WorkspaceDims(1, 8, 16, 80, 128, 1024, 100, 1))) == 0
+    assert L.kva_workspace_size(0, None) == 0
+    assert K.workspace_bytes("decode", B=0, n_kv_heads=8, n_q_heads=16, max_len=80, head_dim=128) == 0
+    assert K.workspace_bytes("lmhead", B=2, hidden=0) == 0
+
+
 def test_strerror_and_version(K):
     L = K.lib()
     for s in range(7):
