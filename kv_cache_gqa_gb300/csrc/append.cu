@@ -834,13 +834,13 @@ append_lean_kernel(const __grid_constant__ AppendArgs a, int tb, int stage_bytes
 
 template <int NORM, bool ROT, typename QOutT, typename CacheT>
 cudaError_t launch_lean(const AppendArgs& a, int tb, int stage, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     const cudaError_t e = cudaFuncSetAttribute(append_lean_kernel<NORM, ROT, QOutT, CacheT>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)(STREAM_STAGES * (STREAM_STAGE_MAX + 2 * 128 * sizeof(float))));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.mark();
   }
   const int64_t items = (int64_t)a.N * ((a.T + tb - 1) / tb);
   const int grid = (int)std::min<int64_t>(items, append_num_sms());
@@ -883,13 +883,13 @@ cudaError_t launch_tokens(const AppendArgs& a, cudaStream_t s) {
         if (lean_rope && a.Hq % 2 == 0 && a.Hkv % 2 == 0) return launch_lean_modes<QOutT, CacheT>(a, tb, stage, s);
       }
       const size_t smem = (size_t)STREAM_STAGES * stage;
-      static bool configured = false;                 // one attribute per template instance
-      if (!configured) {
+      static DeviceOnce configured;                 // one attribute per template instance
+      if (!configured.done()) {
         const cudaError_t e = cudaFuncSetAttribute(append_stream_kernel<D, InT, QOutT, CacheT>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)(STREAM_STAGES * (STREAM_STAGE_MAX + w_bytes)));
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured.mark();
       }
       const int grid = (int)std::min<int64_t>(items, append_num_sms());
       return launch_pdl(append_stream_kernel<D, InT, QOutT, CacheT>, dim3(grid), dim3(STREAM_THREADS), smem, s, a,

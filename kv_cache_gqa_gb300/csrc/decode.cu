@@ -314,12 +314,12 @@ size_t decode_smem_bytes() {
 template <typename CacheT, int G, int DK>
 cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
   const size_t smem = decode_smem_bytes<CacheT, G, DK>();
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<CacheT, G, DK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.mark();
   }
   dim3 grid(a.max_chunks, a.Hkv, a.B);
   return launch_pdl(decode_kernel<CacheT, G, DK>, grid, dim3(THREADS), smem, s, a, q_dtype);

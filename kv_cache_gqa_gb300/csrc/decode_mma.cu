@@ -489,12 +489,12 @@ cudaError_t make_map(CUtensorMap* map, const void* base, const DecodeArgs& a) {
 template <int G, bool FUSED>
 cudaError_t launch_g(const DecodeArgs& a, const StepArgs& st, kva_dtype q_dtype, cudaStream_t s) {
   const size_t smem = (size_t)WARPS * RING + WARPS * NS * 8 + 1024;
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.mark();
   }
   CUtensorMap mk, mv;
   cudaError_t e = make_map(&mk, a.kc, a);

@@ -7,9 +7,12 @@
 // with its scratch taken from a fixed-size array that lives in this library's device image,
 // so the call itself allocates nothing.
 //
-// The array below is a host-side stand-in in host code: its device address is looked up
-// once per device with cudaGetSymbolAddress (the first call on that device does it) and
-// that address is what the kernel receives.
+// The array below lives in device memory, one copy per GPU that loads the library.  Host
+// code can name it only through its host-side shadow symbol, which is not a device address:
+// the device address is looked up once per device with cudaGetSymbolAddress (the first call
+// on that device does it, with that device current) and that address is what the kernel
+// receives.  The looked-up addresses are kept for the life of the process, so the library
+// must not be used across a cudaDeviceReset.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -101,7 +104,7 @@ kva_status kv_attn_decode_static(
     return static_fail(KVA_EWORKSPACE, "B * n_q_heads too large for the fixed 4 MiB decode scratch");
   const int fit_chunks = (int)std::min<size_t>(64, (STATIC_SCRATCH_BYTES - zero_bytes - 256) / per_chunk);
   // Same split rule as kv_attn_decode, then widened until the partials fit in the fixed scratch.
-  long long chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len);
+  long long chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len, (double)(2 * D) * es, 2);
   chunk = std::max<long long>(chunk, (max_len + fit_chunks - 1) / fit_chunks);
   chunk = std::max<long long>(64, (chunk + 63) / 64 * 64);
   const int max_chunks = (int)((max_len + chunk - 1) / chunk);

@@ -5,9 +5,33 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kv_attn.h"
 
 namespace kva {
+
+// Set-up that a launcher does once per device, such as raising a kernel's shared-memory
+// limit: function attributes belong to each device's context, so a process that drives
+// several GPUs sets them on each.  done() tells whether the current device is set up and
+// mark() records it (devices past 63 are set up on every call; repeating it is harmless).
+// Per-device state lives for the whole process: the library is not meant to be used across
+// a cudaDeviceReset.
+struct DeviceOnce {
+  std::atomic<unsigned long long> mask{0};
+  static int current() {
+    int d = 0;
+    return cudaGetDevice(&d) == cudaSuccess ? d : 64;
+  }
+  bool done() const {
+    const int d = current();
+    return d < 64 && ((mask.load(std::memory_order_acquire) >> d) & 1ull);
+  }
+  void mark() {
+    const int d = current();
+    if (d < 64) mask.fetch_or(1ull << d, std::memory_order_release);
+  }
+};
 
 constexpr int MAX_ROPE_FREQ = 128;  // D/2 for D <= 256
 

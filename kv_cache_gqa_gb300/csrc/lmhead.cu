@@ -387,13 +387,13 @@ cudaError_t launch_b1(const LmheadArgs& a, cudaStream_t s) {
 template <typename WT>
 cudaError_t launch_t(const LmheadArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(float) * (size_t)BG * a.H;
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<WT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(sizeof(float) * BG * MAX_H));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.mark();
   }
   dim3 grid((a.V + ROWS_PER_CTA - 1) / ROWS_PER_CTA, (a.B + BG - 1) / BG);
   lmhead_kernel<WT><<<grid, THREADS, smem, s>>>(a);
@@ -420,12 +420,12 @@ int lmhead_max_hidden() { return MAX_H; }
 
 template <int H>
 cudaError_t launch_b1_pipe(const LmheadArgs& a, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(lmhead_b1_pipe_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PIPE_STAGES * PIPE_STAGE_BYTES);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.mark();
   }
   const int grid = num_sms_lm();
   const int rows_per_cta = (a.V + grid - 1) / grid;

@@ -279,11 +279,11 @@ template <int BP>
 cudaError_t launch_bp(const LmheadArgs& a, uint16_t* hb, cudaStream_t s) {
   constexpr int N = 2 * BP;
   const int smem = Stages<BP>::value * (A_BYTES + N * 128) + TM * (BP + 1) * 4 + 64 + 128 + 1024;
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<BP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.mark();
   }
   cudaError_t e = launch_pdl(lmhead_split_kernel, dim3(BP), dim3(256), 0, s, a.h, a.norm_w, a.eps, hb, a.B, BP, a.H);
   if (e != cudaSuccess) return e;

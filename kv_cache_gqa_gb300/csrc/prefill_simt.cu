@@ -220,12 +220,12 @@ size_t simt_smem() { return sizeof(float) * ((size_t)BQ * D + BK * (D + 4) + BK 
 template <int D, int DV, typename T>
 cudaError_t launch_dt(const PrefillArgs& a, cudaStream_t s) {
   const size_t smem = simt_smem<D, DV>();
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<D, DV, T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.mark();
   }
   dim3 grid((a.S + BQ - 1) / BQ, a.Hq, a.N);
   prefill_simt_kernel<D, DV, T><<<grid, THREADS, smem, s>>>(a);

@@ -767,8 +767,8 @@ template <int D, int DV, int NST>
 cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   constexpr int SMEM = Layout<D, DV, NST>::SMEM;
   static_assert(SMEM <= 232448, "shared memory per CTA");
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, DV, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     // the register split assumes the launch holds exactly REGS_LAUNCH per thread: with fewer,
@@ -776,7 +776,7 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D, DV, NST>)) != cudaSuccess) return e;
     if (fa.numRegs != REGS_LAUNCH) return cudaErrorInvalidDeviceFunction;
-    configured = true;
+    configured.mark();
   }
   CUtensorMap mk, mv, mq;
   cudaError_t e = make_cache_map(&mk, a.kc, a, D, a.inst_stride);

@@ -307,11 +307,11 @@ __global__ void verify_commit_kernel(const int32_t* posterior, const int32_t* bl
 
 cudaError_t launch_verify(const VerifyArgs& a, kva_dtype q_dtype, cudaStream_t s) {
   const size_t smem = (size_t)WARPS * RING + WARPS * NS * 8 + 1024;
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(verify_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.mark();
   }
   CUtensorMap mk, mv;
   cudaError_t e = decode_cache_map(&mk, a.kc, a.capacity, a.Hkv, a.B, a.inst_stride);

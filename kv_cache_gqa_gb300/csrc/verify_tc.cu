@@ -650,15 +650,15 @@ int verify_tc_plan_chunk(const int32_t* lengths_host, int B, int Hkv, int max_le
 }
 
 cudaError_t launch_verify_tc(const VerifyArgs& a, kva_dtype q_dtype, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
+  static DeviceOnce configured;
+  if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     // the register split assumes the launch holds exactly REGS_LAUNCH per thread
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, verify_tc_kernel)) != cudaSuccess) return e;
     if (fa.numRegs != REGS_LAUNCH) return cudaErrorInvalidDeviceFunction;
-    configured = true;
+    configured.mark();
   }
   CUtensorMap mk, mv;
   cudaError_t e = make_map_vtc(&mk, a.kc, a);
