@@ -1,5 +1,8 @@
-"""GPU parity of the whole hot path on the five synthetic workloads at their full sizes, in the
-launch configuration the benchmark uses, against the CPU oracle on identical seeded inputs.
+"""GPU parity of the whole hot path on the five synthetic workloads at their full sizes, against
+the CPU oracle on identical seeded inputs.  The Qwen3-shaped and the batched serving workloads
+run twice: once through the fused decode-step call the benchmark times, in its launch
+configuration (28 layer instances or 64 sequences per launch), and once through the separate
+append and decode calls.
 Where the oracle cannot cover every output at full size it checks sampled outputs (every
 layer / head of sampled rows and steps, sampled sequences)."""
 import numpy as np
@@ -96,7 +99,11 @@ def test_tiny_fp32_prefill_decode(K):
 # ----------------------------------------------------------------------------
 # 2. Qwen3-0.6B-shaped: 28 layers, 512 prefill, 256 decode steps, lm_head every step
 # ----------------------------------------------------------------------------
-def test_qwen3_28_layers_full(K):
+@pytest.mark.parametrize("fused", [True, False], ids=["decode_step", "append_then_decode"])
+def test_qwen3_28_layers_full(K, fused):
+    """fused: each decode step is one kv_attn_decode_step launch over the 28 layer caches, with
+    the benchmark's arguments (raw fp32 projections, one shared position id, per-layer norm
+    weights); otherwise the append and the decode are separate calls."""
     torch = T()
     w = WL.qwen3_layers(0)
     NL, P, S_dec, W = 28, w["prompt"], w["steps"], w["capacity"]
@@ -126,12 +133,17 @@ def test_qwen3_28_layers_full(K):
         t = P + s
         qd = torch.empty((NL, 1, Hq, D), device="cuda", dtype=torch.bfloat16)
         sl = np.array([[t]], np.int32)
-        K.kv_cache_append_rope_qknorm(dev(w["dq"][s][:, None]), dev(w["dk"][s][:, None]), dev(w["dv"][s][:, None]),
-                                      dev(sl[:, :, None]), dev(sl), sl, cache, qd, rope, q_norm_w=qw, k_norm_w=kw,
-                                      eps=w["eps"], norm_inst_stride=D)
         o = torch.empty((NL, Hq, D), device="cuda")
         L = np.full(NL, t + 1, np.int32)
-        K.kv_attn_decode(qd[:, 0], cache, dev(L), L, o, dec_ws)
+        if fused:
+            K.kv_attn_decode_step(dev(w["dq"][s]), dev(w["dk"][s]), dev(w["dv"][s]), dev(sl), cache, dev(L), L, o,
+                                  dec_ws, rope, q_norm_w=qw, k_norm_w=kw, eps=w["eps"], norm_inst_stride=D,
+                                  q_out=qd[:, 0])
+        else:
+            K.kv_cache_append_rope_qknorm(dev(w["dq"][s][:, None]), dev(w["dk"][s][:, None]),
+                                          dev(w["dv"][s][:, None]), dev(sl[:, :, None]), dev(sl), sl, cache, qd, rope,
+                                          q_norm_w=qw, k_norm_w=kw, eps=w["eps"], norm_inst_stride=D)
+            K.kv_attn_decode(qd[:, 0], cache, dev(L), L, o, dec_ws)
         if s in sample_steps:
             dec_out[s] = (o, qd)
         K.lmhead_argmax(dev(hs[s + 1]), Wd, ids[s + 1:s + 2], lm_ws)
@@ -158,8 +170,11 @@ def test_qwen3_28_layers_full(K):
             allowed[a_i, :r + 1] = True
         ref = O.attend(qr[rows], ck, cv, allowed)
         assert_bf16_close(host(out_pre[n])[rows], ref, f"prefill layer {n}")
-        for s, (o, _) in dec_out.items():
+        for s, (o, qd) in dec_out.items():
             assert_bf16_close(host(o[n]), O.decode(qdec[s], ck, cv, P + s + 1), f"decode layer {n} step {s}")
+            assert_bf16_store(bf16_bits(qd[n]), qdec[s][None], f"decode q layer {n} step {s}")
+        # the V rows every step wrote (bit-exact: v is stored as given)
+        np.testing.assert_array_equal(host(vc[n])[:, :P + S_dec], cv[:, :P + S_dec].astype(np.float64))
 
     got = ids.cpu().numpy()
     chk = [0, 1, 100, 256]
@@ -256,7 +271,10 @@ def test_vision_windowed(K, dt):
 # ----------------------------------------------------------------------------
 # 5. batched serving decode: B=64, contexts uniform in [1024, 32768], 128 steps
 # ----------------------------------------------------------------------------
-def test_batched_serving_decode(K):
+@pytest.mark.parametrize("fused", [True, False], ids=["decode_step", "append_then_decode"])
+def test_batched_serving_decode(K, fused):
+    """fused: each step is one kv_attn_decode_step launch (the benchmark's serving step) with a
+    position id per sequence; otherwise the append and the decode are separate calls."""
     torch = T()
     seed, B, steps = 0, 64, 128
     Hq, Hkv, D = 16, 8, 128
@@ -289,12 +307,16 @@ def test_batched_serving_decode(K):
         inputs.append(x)
         t = (ctx + s).astype(np.int32)
         qd = torch.empty((B, 1, Hq, D), device="cuda", dtype=torch.bfloat16)
-        K.kv_cache_append_rope_qknorm(dev(x["q"][:, None]), dev(x["k"][:, None]), dev(x["v"][:, None]),
-                                      dev(t[:, None, None]), dev(t[:, None]), t[:, None], cache, qd, rope,
-                                      q_norm_w=qw, k_norm_w=kw, eps=WL.QWEN3_RMS_EPS)
         o = torch.empty((B, Hq, D), device="cuda")
         L = t + 1
-        K.kv_attn_decode(qd[:, 0], cache, dev(L), L, o, dec_ws)
+        if fused:
+            K.kv_attn_decode_step(dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(t[:, None]), cache, dev(L), L, o,
+                                  dec_ws, rope, q_norm_w=qw, k_norm_w=kw, eps=WL.QWEN3_RMS_EPS)
+        else:
+            K.kv_cache_append_rope_qknorm(dev(x["q"][:, None]), dev(x["k"][:, None]), dev(x["v"][:, None]),
+                                          dev(t[:, None, None]), dev(t[:, None]), t[:, None], cache, qd, rope,
+                                          q_norm_w=qw, k_norm_w=kw, eps=WL.QWEN3_RMS_EPS)
+            K.kv_attn_decode(qd[:, 0], cache, dev(L), L, o, dec_ws)
         ids = torch.empty((B,), dtype=torch.int32, device="cuda")
         K.lmhead_argmax(dev(x["h"]), Wd, ids, lm_ws)
         if s in sample_steps:
