@@ -229,6 +229,10 @@ def test_attention_large_logits_stable():
     V = np.array([[[1.0, 0.0], [0.0, 2.0]]])
     o = O.attend(q, K, V, np.array([[True, True]]), scale=1.0)
     np.testing.assert_allclose(o[0, 0], [0.25, 1.5], rtol=1e-12)
+    # logits near 1e5: exp of anything but (logit - row max) overflows float64
+    q = np.array([[[1.0e5, math.log(3.0)]]])
+    o = O.attend(q, K, V, np.array([[True, True]]), scale=1.0)
+    np.testing.assert_allclose(o[0, 0], [0.25, 1.5], rtol=1e-12)
 
 
 def _rand_case(seed, S=9, Hq=4, Hkv=2, D=8, W=12):
