@@ -69,8 +69,13 @@ def test_static_decode_matches_workspace_decode_twice(K, B, W, lens, dt):
         st = _call_static(K, q, cache, lengths_d, lengths, out)
         assert st == 0, K.lib().kva_last_error()
         torch.cuda.synchronize()
-        err = row_rel_err(host(out), host(ref))
-        assert err <= FP32_ROW_REL, f"call {call}: static decode differs from workspace decode ({err:.3e})"
+        if dt == "f32":
+            err = row_rel_err(host(out), host(ref))
+            assert err <= FP32_ROW_REL, f"call {call}: static decode differs from workspace decode ({err:.3e})"
+        else:
+            # a widened plan cuts the keys into other chunks, so the bf16 probabilities the
+            # tensor-core kernel rounds differ: the bf16-cache tolerance applies
+            assert_bf16_close(host(out), host(ref), f"call {call}: static vs workspace decode")
 
 
 @pytest.mark.gpu
