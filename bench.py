@@ -59,6 +59,11 @@ def decode_bytes(L):
     return kv + LAYERS * ((HQ + 2 * HKV) * D * 4 + 2 * HKV * D * 2 + HQ * D * 4)
 
 
+def prefill_min_bytes():
+    """Bytes the prefill must move at least: bf16 q and the prompt's bf16 K/V rows in, fp32 out."""
+    return LAYERS * PROMPT * (HQ * D * 2 + 2 * HKV * D * 2 + HQ * D * 4)
+
+
 def lmhead_bytes(B=1):
     return VOCAB * HIDDEN * 2 + B * (HIDDEN * 4 + 4)
 
@@ -191,6 +196,19 @@ class Qwen3Job:
         self.dec_ws = torch.zeros(K.decode_workspace_bytes(LAYERS, HKV, HQ, WINDOW, D), dtype=torch.uint8, device=dev)
         self.lm_ws = torch.zeros(K.lmhead_workspace_bytes(1, HIDDEN), dtype=torch.uint8, device=dev)
         self.events = None
+        self._views = {}
+
+    def step_views(self):
+        """Per-step argument views of the decode loop, made once per input set (a serving loop
+        holds its buffers; slicing tensors per call would only add host time)."""
+        key = (id(self.dq), id(self.dk), id(self.dv), id(self.h))
+        v = self._views.get(key)
+        if v is None:
+            v = [(self.dq[s, :, 0], self.dk[s, :, 0], self.dv[s, :, 0], self.step_slot_d[s], self.len_d[s],
+                  self.out_dec[s], self.h[s + 1], self.ids[s + 1:s + 2]) for s in range(STEPS)]
+            v.append((self.h[0], self.ids[0:1]))
+            self._views[key] = v
+        return v
 
     def _ev(self, key):
         if self.events is not None:
@@ -211,14 +229,15 @@ class Qwen3Job:
         self._ev("append_pre")
         K.kv_attn_prefill(self.q_pre, c, self.out_pre, mask="causal")
         self._ev("prefill")
-        K.lmhead_argmax(self.h[0], self.W, self.ids[0:1], self.lm_ws)
+        views = self.step_views()
+        K.lmhead_argmax(views[STEPS][0], self.W, views[STEPS][1], self.lm_ws)
         self._ev("lm_head")
         for s in range(STEPS):
-            K.kv_attn_decode_step(self.dq[s, :, 0], self.dk[s, :, 0], self.dv[s, :, 0], self.step_slot_d[s], c,
-                                  self.len_d[s], self.len_host[s], self.out_dec[s], self.dec_ws, self.rope,
+            dq, dk, dv, pos, lens, out, h, ids = views[s]
+            K.kv_attn_decode_step(dq, dk, dv, pos, c, lens, self.len_host[s], out, self.dec_ws, self.rope,
                                   q_norm_w=self.qw, k_norm_w=self.kw, eps=1e-6, norm_inst_stride=D)
             self._ev("decode")
-            K.lmhead_argmax(self.h[s + 1], self.W, self.ids[s + 1:s + 2], self.lm_ws)
+            K.lmhead_argmax(h, self.W, ids, self.lm_ws)
             self._ev("lm_head")
 
     def kernel_times_ms(self):
@@ -265,6 +284,219 @@ def graph_avg_ms(torch, stream, launch, n, reps=4):
         e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / (n * reps)
+
+
+def graph_seq_ms(torch, stream, fns, reps=4):
+    """Average duration of one launch of the sequence `fns` (callables, each one launch),
+    captured back to back in one graph and replayed `reps` times between two events on the
+    launching stream (after one warm replay).  Launches that rotate over copies of their data
+    whose total exceeds L2 read cold data, as inside a long job."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for f in fns:
+            f()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (len(fns) * reps)
+
+
+# FP32 FFMA peak of the SIMT (fp32-cache) paths: 152 SMs x 128 FMA lanes x 2 flop x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def decode_step_bench(torch, K, stream, job, copies=4):
+    """kv_attn_decode_step alone as the job runs it (28 layer caches, 256 steps at L = 513..768,
+    the job's inputs and per-layer norm weights), timed directly: one graph of the 256 launches,
+    step s on cache copy s % copies (each copy 117 MB, so every launch reads its K/V from HBM as
+    in the job, where the lm_head's 311 MB stream sits between two decode steps)."""
+    g = torch.Generator(device="cuda"); g.manual_seed(21)
+    caches = []
+    for _ in range(copies):
+        kc = torch.randn((LAYERS, HKV, WINDOW, D), device="cuda", generator=g).to(torch.bfloat16)
+        vc = torch.randn((LAYERS, HKV, WINDOW, D), device="cuda", generator=g).to(torch.bfloat16)
+        caches.append(K.KVCache(kc, vc))
+
+    def step(s):
+        return lambda: K.kv_attn_decode_step(job.dq[s, :, 0], job.dk[s, :, 0], job.dv[s, :, 0], job.step_slot_d[s],
+                                             caches[s % copies], job.len_d[s], job.len_host[s], job.out_dec[s],
+                                             job.dec_ws, job.rope, q_norm_w=job.qw, k_norm_w=job.kw, eps=1e-6,
+                                             norm_inst_stride=D)
+    fns = [step(s) for s in range(STEPS)]
+    ms = graph_seq_ms(torch, stream, fns, reps=4)
+    dec_bytes = [decode_bytes(PROMPT + s + 1) for s in range(STEPS)]
+    del caches
+    return {"avg_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": int(np.mean(dec_bytes)),
+            "GB/s": round(np.mean(dec_bytes) / (ms / 1e3) / 1e9, 1),
+            "timing": f"graph of the 256 launches of the job's decode loop (L = 513..768), step s on cache "
+                      f"copy s % {copies} ({copies} x 117 MB, larger than L2), CUDA events around 4 replays"}
+
+
+def configs_bench(torch, K, stream, hbm, bf16):
+    """The other workloads' hot paths, each timed as a CUDA graph on the launching stream:
+      tiny fp32 layer (latency: 64-token append + prefill, then 16 steps of append + decode);
+      image-span prefill (xdRoPE, norm after RoPE, causal, 512 tokens) and its 64 decode steps;
+      vision windowed attention (1288 patches, 16 heads, D = 72): window pass and full pass,
+      bf16 and fp32 caches.
+    Prefill and vision launches rotate over copies of their buffers larger than L2 in total."""
+    import workloads as WL
+    res = {}
+    dv = lambda a, dt=None: (torch.from_numpy(np.ascontiguousarray(a)).cuda() if dt is None
+                             else torch.from_numpy(np.ascontiguousarray(a)).cuda().to(dt))
+
+    # ---- 1. tiny fp32 single layer: prefill 64, 16 decode steps ----
+    w = WL.tiny_fp32(0)
+    W_, P_ = w["capacity"], w["n_prefill"]
+    kc = torch.zeros((1, HKV, W_, D), device="cuda"); vc = torch.zeros_like(kc)
+    cache = K.KVCache(kc, vc)
+    rope = K.Rope("1d", w["base"])
+    qw, kw = dv(w["q_norm_w"]), dv(w["k_norm_w"])
+    q_all, k_all, v_all, pos_all = dv(w["q"][None]), dv(w["k"][None]), dv(w["v"][None]), dv(w["pos"][None])
+    slot_h = np.arange(W_, dtype=np.int32)[None]
+    slot_d = dv(slot_h)
+    q_pre = torch.empty((1, P_, HQ, D), device="cuda"); o_pre = torch.empty_like(q_pre)
+    q_dec = torch.empty((1, 1, HQ, D), device="cuda"); o_dec = torch.empty((W_ - P_, HQ, D), device="cuda")
+    lens_h = [np.array([t + 1], np.int32) for t in range(W_)]
+    lens_d = [dv(x) for x in lens_h]                 # one small tensor per step (aligned)
+    pos_t = [dv(w["pos"][None, t:t + 1]) for t in range(W_)]
+    slot_t = [dv(slot_h[:, t:t + 1]) for t in range(W_)]
+    ws = torch.zeros(K.decode_workspace_bytes(1, HKV, HQ, W_, D), dtype=torch.uint8, device="cuda")
+
+    def tiny_prefill():
+        K.kv_cache_append_rope_qknorm(q_all[:, :P_], k_all[:, :P_], v_all[:, :P_], pos_all[:, :P_], slot_d[:, :P_],
+                                      slot_h[:, :P_], cache, q_pre, rope, q_norm_w=qw, k_norm_w=kw, eps=w["eps"])
+        K.kv_attn_prefill(q_pre, cache, o_pre, mask="causal")
+
+    def tiny_run():
+        tiny_prefill()
+        for t in range(P_, W_):
+            K.kv_cache_append_rope_qknorm(q_all[:, t:t + 1], k_all[:, t:t + 1], v_all[:, t:t + 1], pos_t[t],
+                                          slot_t[t], slot_h[:, t:t + 1], cache, q_dec, rope, q_norm_w=qw,
+                                          k_norm_w=kw, eps=w["eps"])
+            K.kv_attn_decode(q_dec[:, 0], cache, lens_d[t], lens_h[t], o_dec[t - P_:t - P_ + 1], ws)
+    with torch.cuda.stream(stream):
+        tiny_run()
+    torch.cuda.synchronize()
+    run_ms = graph_seq_ms(torch, stream, [tiny_run], reps=20)
+    pre_ms = graph_seq_ms(torch, stream, [tiny_prefill], reps=20)
+    res["tiny_fp32"] = {
+        "config": "1 layer, 16/8 heads, D=128, fp32 cache of 80 slots: 64-token append + causal prefill, then "
+                  "16 steps of append + decode (34 launches)",
+        "run_us": round(run_ms * 1e3, 1), "prefill_phase_us": round(pre_ms * 1e3, 1),
+        "decode_step_us": round((run_ms - pre_ms) * 1e3 / (W_ - P_), 2),
+        "note": "latency-bound (17 MFLOP, ~3 MB): no roofline; the data stays in L2"}
+    del kc, vc
+
+    # ---- 3. image-span prefill and its 64 decode steps ----
+    w = WL.image_span_prefill(0)
+    S3, W3, steps3 = w["pos"].shape[0], w["capacity"], w["dq"].shape[0]
+    rope3 = K.Rope("sections", w["base"], w["sections"])
+    qw3, kw3 = dv(w["q_norm_w"]), dv(w["k_norm_w"])
+    n3 = 16                                          # 16 copies x 10 MB (q, window K/V, output)
+    kc3 = torch.zeros((n3, HKV, W3, D), device="cuda", dtype=torch.bfloat16); vc3 = torch.zeros_like(kc3)
+    q3 = torch.empty((n3, S3, HQ, D), device="cuda", dtype=torch.bfloat16)
+    o3 = torch.empty((n3, S3, HQ, D), device="cuda")
+    c3 = [K.KVCache(kc3[i:i + 1], vc3[i:i + 1]) for i in range(n3)]
+    sl3_h = np.arange(S3, dtype=np.int32)[None]
+    sl3, pos3 = dv(sl3_h), dv(w["pos"][None])
+    qi, ki, vi = dv(w["q"][None]), dv(w["k"][None]), dv(w["v"][None])
+    app3 = lambda i: K.kv_cache_append_rope_qknorm(qi, ki, vi, pos3, sl3, sl3_h, c3[i], q3[i:i + 1], rope3,
+                                                   q_norm_w=qw3, k_norm_w=kw3, eps=w["eps"], norm_after_rope=True)
+    with torch.cuda.stream(stream):
+        for i in range(n3):
+            app3(i)
+    torch.cuda.synchronize()
+    pre3 = [(lambda i: (lambda: K.kv_attn_prefill(q3[i:i + 1], c3[i], o3[i:i + 1], mask="causal")))(i)
+            for i in range(n3)]
+    with torch.cuda.stream(stream):
+        pre3[0]()
+    torch.cuda.synchronize()
+    pre3_ms = graph_seq_ms(torch, stream, pre3, reps=4)
+    app3_ms = graph_seq_ms(torch, stream, [(lambda i: (lambda: app3(i)))(i) for i in range(n3)], reps=4)
+    flops3 = 4 * D * HQ * (S3 * (S3 + 1) // 2)
+    dq3, dk3, dv3, dpos3 = dv(w["dq"]), dv(w["dk"]), dv(w["dv"]), dv(w["dpos"])
+    lens3_h = [np.array([S3 + s + 1], np.int32) for s in range(steps3)]
+    lens3_d = [dv(x) for x in lens3_h]
+    o3d = torch.empty((steps3, HQ, D), device="cuda")
+    ws3 = torch.zeros(K.decode_workspace_bytes(1, HKV, HQ, W3, D), dtype=torch.uint8, device="cuda")
+    dec3 = [(lambda s: (lambda: K.kv_attn_decode_step(
+        dq3[s:s + 1], dk3[s:s + 1], dv3[s:s + 1], dpos3[s:s + 1], c3[0], lens3_d[s], lens3_h[s], o3d[s:s + 1],
+        ws3, rope3, q_norm_w=qw3, k_norm_w=kw3, eps=w["eps"], norm_after_rope=True)))(s) for s in range(steps3)]
+    with torch.cuda.stream(stream):
+        dec3[0]()
+    torch.cuda.synchronize()
+    dec3_ms = graph_seq_ms(torch, stream, dec3, reps=4)
+    dec3_bytes = sum(HKV * (S3 + s + 1) * D * 2 * 2 + (HQ + 2 * HKV) * D * 4 + 2 * HKV * D * 2 + HQ * D * 4
+                     for s in range(steps3)) / steps3
+    pre3_tf = flops3 / (pre3_ms / 1e3) / 1e12
+    res["image_span"] = {
+        "config": f"1 layer, {S3} tokens (20 text + 274 image rows + 218 text), 4-axis xdRoPE [16,16,16,16] base "
+                  f"1.11588e7, norm after RoPE, causal, 16/8 heads, D=128, bf16 window of {W3}; then {steps3} fused "
+                  f"decode steps (L = {S3 + 1}..{S3 + steps3})",
+        "prefill_us": round(pre3_ms * 1e3, 2), "prefill_TFLOP/s": round(pre3_tf, 1),
+        "prefill_frac_bf16": round(pre3_tf / bf16, 4), "prefill_flops": flops3,
+        "append_us": round(app3_ms * 1e3, 2),
+        "append_GB/s": round(append_bytes(S3) / (app3_ms / 1e3) / 1e9, 1),
+        "decode_step_us": round(dec3_ms * 1e3, 2),
+        "decode_GB/s": round(dec3_bytes / (dec3_ms / 1e3) / 1e9, 1),
+        "decode_frac_hbm": round(dec3_bytes / (dec3_ms / 1e3) / 1e9 / hbm, 4),
+        "timing": "prefill and append: graphs of 16 launches over 16 buffer copies (160 MB); decode: graph of "
+                  "the 64 steps (one layer, ~2.3 MB per step: launch-latency bound, read from L2)"}
+    del kc3, vc3, q3, o3
+
+    # ---- 4. vision windowed attention: window pass and full pass, bf16 and fp32 ----
+    w = WL.vision_windowed(0)
+    lay = w["layout"]
+    S4, H4, D4 = lay.pos_rc.shape[0], WL.VISION_HEADS, WL.VISION_HEAD_DIM
+    seg_sizes = np.bincount(lay.segment)
+    flops_win = int(4 * D4 * H4 * int(np.sum(seg_sizes.astype(np.int64) ** 2)))
+    flops_full = 4 * D4 * H4 * S4 * S4
+    seg_d, ros_d = dv(lay.segment), dv(lay.row_of_slot)
+    sl4_h = lay.slot[None]
+    sl4, pos4 = dv(sl4_h), dv(lay.pos_rc[None])
+    qi4, ki4, vi4 = dv(w["q"][None]), dv(w["k"][None]), dv(w["v"][None])
+    rope4 = K.Rope("2d", w["base"])
+    vis = {}
+    for name, tdt in (("bf16", torch.bfloat16), ("f32", torch.float32)):
+        n4 = 10                                      # 10 copies: 148 MB (bf16) / 237 MB (fp32)
+        kc4 = torch.zeros((n4, H4, S4, D4), device="cuda", dtype=tdt); vc4 = torch.zeros_like(kc4)
+        q4 = torch.empty((n4, S4, H4, D4), device="cuda", dtype=tdt)
+        o4 = torch.empty((n4, S4, H4, D4), device="cuda")
+        c4 = [K.KVCache(kc4[i:i + 1], vc4[i:i + 1]) for i in range(n4)]
+        with torch.cuda.stream(stream):
+            for i in range(n4):
+                K.kv_cache_append_rope_qknorm(qi4, ki4, vi4, pos4, sl4, sl4_h, c4[i], q4[i:i + 1], rope4)
+        torch.cuda.synchronize()
+        win = [(lambda i: (lambda: K.kv_attn_prefill(q4[i:i + 1], c4[i], o4[i:i + 1], mask="segment", segment=seg_d,
+                                                     segment_host=lay.segment, row_of_slot=ros_d)))(i)
+               for i in range(n4)]
+        full = [(lambda i: (lambda: K.kv_attn_prefill(q4[i:i + 1], c4[i], o4[i:i + 1], mask="full",
+                                                      row_of_slot=ros_d)))(i) for i in range(n4)]
+        with torch.cuda.stream(stream):
+            win[0](); full[0]()
+        torch.cuda.synchronize()
+        win_ms = graph_seq_ms(torch, stream, win, reps=4)
+        full_ms = graph_seq_ms(torch, stream, full, reps=4)
+        peak = bf16 if name == "bf16" else FP32_ALU_TFLOPS
+        tw, tf = flops_win / (win_ms / 1e3) / 1e12, flops_full / (full_ms / 1e3) / 1e12
+        vis[name] = {"window_us": round(win_ms * 1e3, 2), "window_TFLOP/s": round(tw, 2),
+                     "window_frac": round(tw / peak, 4), "full_us": round(full_ms * 1e3, 2),
+                     "full_TFLOP/s": round(tf, 2), "full_frac": round(tf / peak, 4),
+                     "peak_TFLOP/s": round(peak, 1),
+                     "peak": "measured bf16 dense (tensor cores)" if name == "bf16" else
+                             "FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (derived)"}
+        del kc4, vc4, q4, o4
+    res["vision"] = dict(vis, config=f"{S4} patches (14x92 grid, windows of 8x8 merged 2x2 groups: "
+                                     f"{'/'.join(str(int(x)) for x in seg_sizes)} patches), {H4} heads = KV heads, "
+                                     f"D={D4}, 2D RoPE, bidirectional; window pass (block-diagonal) and full pass",
+                         window_flops=flops_win, full_flops=flops_full,
+                         timing="graphs of 10 launches over 10 buffer copies (larger than L2)")
+    return res
 
 
 VERIFY_B, VERIFY_L, VERIFY_K = 64, 2048, 16
@@ -539,6 +771,10 @@ def run_gpu(args, rank, world, local_rank):
     vb = verify_bench(torch, K, stream)
     sv = serving_bench(torch, K, stream, job.W, None)
     mla = mla_bench(torch, K, stream)
+    ds = decode_step_bench(torch, K, stream, job)
+    peaks0, _ = load_peaks()
+    cfg = configs_bench(torch, K, stream, float(peaks0.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+                        float(peaks0.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
 
     # ---- end to end: inputs from pinned host memory, ids back to the host, every step ----
     # Two device input sets, each with its own graph of the job: step i copies its inputs into
@@ -590,17 +826,55 @@ def run_gpu(args, rank, world, local_rank):
     e2e_ms = reduce_max(e0.elapsed_time(e1), world, device=torch.device("cuda", local_rank))
     e2e_value = aggregate_throughput(TOKENS_PER_JOB * args.steps, world, e2e_ms / 1e3)
 
+    # ---- end to end, eager: the same copies, and every step calls the four entry points through the
+    # C ABI (515 calls: host validation and planning each time), no graph ----
+    def e2e_eager_step(i):
+        j = i % 2
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(done[j])
+            for n in names:
+                dev_sets[j][n].copy_(host_in[n], non_blocking=True)
+            ready[j].record(copy_stream)
+        stream.wait_event(ready[j])
+        for n in names:
+            setattr(job, n, dev_sets[j][n])
+        job.record()
+        done[j].record(stream)
+        ids_host.copy_(job.ids, non_blocking=True)
+
+    n_eager0 = K.launch_count()
+    with torch.cuda.stream(stream):
+        for i in range(max(2, args.warmup)):
+            e2e_eager_step(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        copy_stream.wait_event(e0)
+        n_eager0 = K.launch_count()
+        t_host0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_eager_step(i)
+        t_host = time.perf_counter() - t_host0
+        e1.record(stream)
+        torch.cuda.synchronize()
+    eager_launches = K.launch_count() - n_eager0
+    for n in names:
+        setattr(job, n, dev_sets[0][n])
+    eager_ms = reduce_max(e0.elapsed_time(e1), world, device=torch.device("cuda", local_rank))
+    eager_value = aggregate_throughput(TOKENS_PER_JOB * args.steps, world, eager_ms / 1e3)
+
     if rank == 0:
         peaks, peak_src = load_peaks()
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        # An event node adds a launch latency to the kernel it brackets, so the short decode
-        # launches are timed by difference: the timed job minus the prefill-phase kernels (event
-        # nodes) and the lm_head launches (their stand-alone graph time).
+        # The decode step is timed directly (a graph of the job's 256 launches over rotating cache
+        # copies); the difference of the job and its other kernels is kept beside it as a check.
         totals = {k: sum(v) for k, v in kt.items()}
         job_ms = max_ms / args.steps
-        in_job = {"lm_head": lm_iso_ms, "prefill": kt["prefill"][0], "append_pre": kt["append_pre"][0]}
-        in_job["decode"] = (job_ms - in_job["prefill"] - in_job["append_pre"] - TOKENS_PER_JOB * lm_iso_ms) / STEPS
+        in_job = {"lm_head": lm_iso_ms, "prefill": kt["prefill"][0], "append_pre": kt["append_pre"][0],
+                  "decode": ds["avg_launch_us"] / 1e3}
+        dec_by_diff_ms = (job_ms - in_job["prefill"] - in_job["append_pre"] - TOKENS_PER_JOB * lm_iso_ms) / STEPS
         dec_bytes = [decode_bytes(PROMPT + s + 1) for s in range(STEPS)]
         dec_gbs = np.mean(dec_bytes) / (in_job["decode"] / 1e3) / 1e9
         lm_gbs = lmhead_bytes() / (lm_iso_ms / 1e3) / 1e9
@@ -616,33 +890,46 @@ def run_gpu(args, rank, world, local_rank):
             roof.update({"kernel": "kv_attn_decode_step", "achieved": round(dec_gbs, 1),
                          "frac": round(dec_gbs / hbm, 4), "traffic": None,
                          "algorithmic_bytes_per_launch": int(np.mean(dec_bytes)),
-                         "avg_launch_us": round(in_job["decode"] * 1e3, 2), "timing": "job time by difference"})
+                         "avg_launch_us": round(in_job["decode"] * 1e3, 2), "timing": ds["timing"]})
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "Qwen3-0.6B-shaped attention step: 28 layers x (512-token causal prefill + "
-                                   "256 decode steps), 1024-slot bf16 window, tied lm_head 151936x1024 bf16 argmax",
-                       "layers": LAYERS, "prompt": PROMPT, "decode_steps": STEPS, "window": WINDOW,
-                       "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "vocab": VOCAB, "batch": 1,
-                       "step": "one whole job (prefill + 256 decode steps) as one CUDA graph replay",
-                       "l2": "inputs larger than L2: the 311 MB lm_head table streams through the 129 MB L2 "
-                             "between decode steps"},
-            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "config": job_config(),
+            "e2e": {"value": round(eager_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h),
+                    "leg": "eager C-ABI calls",
                     "copies": "each step's inputs copied from pinned host memory on a copy stream while "
-                              "the previous step runs (two device input sets, one job graph each); "
-                              "ids read back after every step"},
+                              "the previous step runs (two device input sets); ids read back after every step",
+                    "legs": {
+                        "eager_c_abi": {"value": round(eager_value, 1), "ms_per_step": round(eager_ms / args.steps, 3),
+                                        "host_ms_per_step": round(t_host * 1e3 / args.steps, 3),
+                                        "launches_per_step": int(eager_launches // args.steps),
+                                        "what": "every step calls the four entry points through the C ABI "
+                                                "(515 calls, host validation and planning each time), no graph"},
+                        "graph_replay": {"value": round(e2e_value, 1), "ms_per_step": round(e2e_ms / args.steps, 3),
+                                         "what": "the job captured once through the same calls, replayed as one "
+                                                 "CUDA graph per step"}}},
             "gpu_launches": int(launches_per_job * args.steps),
             "roofline": roof,
             "kernels": {
                 "decode_step": {"GB/s": round(dec_gbs, 1), "frac_hbm": round(dec_gbs / hbm, 4),
                                 "avg_launch_us": round(in_job["decode"] * 1e3, 2),
-                                "algorithmic_bytes_per_launch": int(np.mean(dec_bytes))},
+                                "algorithmic_bytes_per_launch": int(np.mean(dec_bytes)), "timing": ds["timing"],
+                                "by_difference_us": round(dec_by_diff_ms * 1e3, 2)},
                 "prefill_attn": {"TFLOP/s": round(pre_tf, 2), "frac_bf16": round(pre_tf / bf16, 4),
                                  "launch_us": round(in_job["prefill"] * 1e3, 1), "flops": prefill_flops(),
                                  "alone_us": round(pre_iso_ms * 1e3, 1),
-                                 "alone_frac_bf16": round(prefill_flops() / (pre_iso_ms / 1e3) / 1e12 / bf16, 4)},
+                                 "alone_frac_bf16": round(prefill_flops() / (pre_iso_ms / 1e3) / 1e12 / bf16, 4),
+                                 "min_bytes": prefill_min_bytes(),
+                                 "byte_floor_us": round(prefill_min_bytes() / (hbm * 1e9) * 1e6, 1),
+                                 "flop_floor_us": round(prefill_flops() / (bf16 * 1e12) * 1e6, 1),
+                                 "alone_frac_of_roofline": round(max(prefill_min_bytes() / (hbm * 1e9),
+                                                                     prefill_flops() / (bf16 * 1e12))
+                                                                 / (pre_iso_ms / 1e3), 4)},
+                "tiny_fp32": cfg["tiny_fp32"],
+                "image_span": cfg["image_span"],
+                "vision": cfg["vision"],
                 "append_prefill": {"GB/s": round(app_gbs, 1), "frac_hbm": round(app_gbs / hbm, 4),
                                    "launch_us": round(in_job["append_pre"] * 1e3, 1),
                                    "alone_us": round(app_iso_ms * 1e3, 1),
@@ -658,8 +945,8 @@ def run_gpu(args, rank, world, local_rank):
                 "time_share": {k: round(v / sum(totals.values()), 4) for k, v in totals.items()},
                 "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": peak_src},
                 "timing": ("lm_head: graph of 32 back-to-back launches; prefill, append: " + kt_source +
-                           "; decode step: (timed job - prefill - append - 257 lm_head) / 256; verify block: "
-                           "graph of 8 back-to-back launches (outside the job)"),
+                           "; decode step: graph of the job's 256 decode launches over 4 rotating cache copies; "
+                           "verify block: graph of 8 back-to-back launches (outside the job)"),
                 "event_node_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in kt.items()},
             },
             "clocks": clk,
@@ -733,36 +1020,152 @@ def oracle_sample_times(rows_pf=32, dec_layers=1, lm_rows=8192, seed=0):
     return job_s, sample
 
 
-def cpu_baseline(target_s=12.0):
-    """Oracle (single thread, float64) on repeated bounded samples for ~target_s seconds."""
+ORACLE_SAMPLE = dict(rows_pf=64, dec_layers=2, lm_rows=16384)   # the one sample recipe of both oracle legs
+
+
+def host_info():
+    """Host cores available to this process and the CPU model (lscpu, else /proc/cpuinfo)."""
+    try:
+        nproc = len(os.sched_getaffinity(0))
+    except Exception:
+        nproc = os.cpu_count()
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Vendor ID") and ":" in line:
+                model = (model + " / " if model else "") + line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            model = "unknown"
+    return {"nproc": nproc, "cpu_model": model, "machine": os.uname().machine}
+
+
+def oracle_full_configs():
+    """The oracle on the small workloads in full, no sampling: seconds for the tiny fp32 layer
+    (64-token prefill + 16 decode steps), the image-span layer (512-token append + prefill + 64
+    decode steps) and the vision pass (append, window pass and full pass) in fp32 and bf16."""
+    import oracle as O
+    import workloads as WL
+    out = {}
+    w = WL.tiny_fp32(0)
+    W_, P_ = w["capacity"], w["n_prefill"]
+    rope = O.Rope("1d", w["base"])
+    t0 = time.perf_counter()
+    ck = np.zeros((HKV, W_, D)); cv = np.zeros((HKV, W_, D))
+    qr = O.cache_append(w["q"][:P_], w["k"][:P_], w["v"][:P_], w["pos"][:P_], np.arange(P_), w["q_norm_w"],
+                        w["k_norm_w"], w["eps"], rope, False, ck, cv, "f32")
+    O.prefill(qr, ck, cv, P_, "causal")
+    for t in range(P_, W_):
+        qd = O.cache_append(w["q"][t:t + 1], w["k"][t:t + 1], w["v"][t:t + 1], w["pos"][t:t + 1], [t], w["q_norm_w"],
+                            w["k_norm_w"], w["eps"], rope, False, ck, cv, "f32")
+        O.decode(qd[0], ck, cv, t + 1)
+    out["tiny_fp32_s"] = round(time.perf_counter() - t0, 4)
+    w = WL.image_span_prefill(0)
+    S3, W3, steps3 = w["pos"].shape[0], w["capacity"], w["dq"].shape[0]
+    rope = O.Rope("sections", w["base"], w["sections"])
+    t0 = time.perf_counter()
+    ck = np.zeros((HKV, W3, D)); cv = np.zeros((HKV, W3, D))
+    qr = O.cache_append(w["q"], w["k"], w["v"], w["pos"], np.arange(S3), w["q_norm_w"], w["k_norm_w"], w["eps"],
+                        rope, True, ck, cv, "bf16")
+    t1 = time.perf_counter()
+    O.prefill(qr, ck, cv, S3, "causal")
+    out["image_span_prefill_s"] = round(time.perf_counter() - t1, 4)
+    for st in range(steps3):
+        qd = O.cache_append(w["dq"][st:st + 1], w["dk"][st:st + 1], w["dv"][st:st + 1], w["dpos"][st:st + 1], [S3 + st],
+                            w["q_norm_w"], w["k_norm_w"], w["eps"], rope, True, ck, cv, "bf16")
+        O.decode(qd[0], ck, cv, S3 + st + 1)
+    out["image_span_s"] = round(time.perf_counter() - t0, 4)
+    w = WL.vision_windowed(0)
+    lay = w["layout"]
+    S4 = lay.pos_rc.shape[0]
+    for dt in ("f32", "bf16"):
+        t0 = time.perf_counter()
+        ck = np.zeros((WL.VISION_HEADS, S4, WL.VISION_HEAD_DIM)); cv = np.zeros_like(ck)
+        qr = O.cache_append(w["q"], w["k"], w["v"], lay.pos_rc, lay.slot, None, None, 0.0, O.Rope("2d", w["base"]),
+                            False, ck, cv, dt)
+        qs = O.store(qr, dt)[lay.row_of_slot]
+        t1 = time.perf_counter()
+        O.prefill(qs, ck, cv, S4, "segment", lay.segment)
+        t2 = time.perf_counter()
+        O.prefill(qs, ck, cv, S4, "full")
+        t3 = time.perf_counter()
+        out[f"vision_{dt}_window_s"] = round(t2 - t1, 4)
+        out[f"vision_{dt}_full_s"] = round(t3 - t2, 4)
+        out[f"vision_{dt}_s"] = round(t3 - t0, 4)
+    return out
+
+
+def oracle_job_samples(target_s=None, n=None, warmup=0):
+    """Repeated samples of the job with ORACLE_SAMPLE: either for about target_s seconds or
+    exactly warmup + n samples (the first warmup not kept).  Returns the per-sample seconds, the
+    extrapolated job seconds of each kept sample, and the sample's description."""
     t_start = time.perf_counter()
-    jobs, sample = [], ""
-    while not jobs or time.perf_counter() - t_start < target_s:
-        js, sample = oracle_sample_times(seed=len(jobs))
-        jobs.append(js)
+    wall, jobs, sample, i = [], [], "", 0
+    while True:
+        t0 = time.perf_counter()
+        js, sample = oracle_sample_times(seed=i, **ORACLE_SAMPLE)
+        if i >= warmup:
+            wall.append(time.perf_counter() - t0)
+            jobs.append(js)
+        i += 1
+        if n is not None and len(jobs) >= n:
+            break
+        if n is None and jobs and time.perf_counter() - t_start >= target_s:
+            break
+    return wall, jobs, sample
+
+
+def cpu_baseline(target_s=12.0):
+    """Oracle (single thread, float64) on repeated bounded samples of the job for ~target_s
+    seconds, plus the small workloads timed in full."""
+    t_start = time.perf_counter()
+    wall, jobs, sample = oracle_job_samples(target_s=target_s, warmup=1)
     job_s = statistics.median(jobs)
+    full = oracle_full_configs()
     return {"value": round(TOKENS_PER_JOB / job_s, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{len(jobs)} samples; {sample}", "job_seconds_extrapolated": round(job_s, 2),
+            "host": host_info(),
+            "sample": f"{len(jobs)} samples of {statistics.median(wall):.2f} s each (after one warm-up sample); "
+                      f"{sample}", "job_seconds_extrapolated": round(job_s, 2),
+            "full_configs_seconds": full,
             "cpu_seconds": round(time.perf_counter() - t_start, 1)}
 
 
+def job_config():
+    return {"workload": "Qwen3-0.6B-shaped attention step: 28 layers x (512-token causal prefill + "
+                        "256 decode steps), 1024-slot bf16 window, tied lm_head 151936x1024 bf16 argmax",
+            "layers": LAYERS, "prompt": PROMPT, "decode_steps": STEPS, "window": WINDOW,
+            "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "vocab": VOCAB, "batch": 1,
+            "step": "one whole job (prefill + 256 decode steps) as one CUDA graph replay",
+            "l2": "inputs larger than L2: the 311 MB lm_head table streams through the 129 MB L2 "
+                  "between decode steps"}
+
+
 def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one bounded sample of the job (the same
+    recipe as the cpu_baseline block of the main line); the value is the job's tokens/s that the
+    sample's time extrapolates to, and ms_per_step the sample's own wall time."""
     if rank != 0:
         return
-    per_step = []
-    for i in range(args.warmup + args.steps):
-        js, sample = oracle_sample_times(rows_pf=8, dec_layers=1, lm_rows=2048, seed=i)
-        if i >= args.warmup:
-            per_step.append(js)
-    job_s = statistics.median(per_step)
+    wall, jobs, sample = oracle_job_samples(n=args.steps, warmup=args.warmup)
+    job_s = statistics.median(jobs)
     value = TOKENS_PER_JOB / job_s
+    cfg = job_config()
+    cfg["step"] = "one bounded oracle sample of the job (see cpu_baseline.sample)"
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(job_s * 1e3, 1),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.median(wall) * 1e3, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "Qwen3-0.6B-shaped attention step: 28 layers x (512-token causal prefill + "
-                                   "256 decode steps), 1024-slot bf16 window, tied lm_head 151936x1024 bf16 argmax"},
+            "config": cfg,
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "host": host_info(), "sample": sample,
+                             "job_seconds_extrapolated": round(job_s, 2)},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

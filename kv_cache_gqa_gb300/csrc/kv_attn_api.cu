@@ -133,12 +133,22 @@ kva_status build_rope(const kva_rope& r, int D, RopeTable* t) {
 }
 
 kva_status build_rope_table(const kva_rope& r, int D, RopeTable* t) {
+  // A decode loop passes the same rotary layout on every call: the last table built on this
+  // host thread is reused when the layout and width match (the D/2 pow() calls cost microseconds).
+  thread_local kva_rope last_r{};
+  thread_local int last_D = -1;
+  thread_local RopeTable last_t;
+  if (last_D == D && std::memcmp(&last_r, &r, sizeof(r)) == 0) {
+    *t = last_t;
+    return KVA_OK;
+  }
   const kva_status st = build_rope(r, D, t);
   if (st != KVA_OK) return st;
   for (int j = 0; j < MAX_ROPE_FREQ; ++j) {
     t->inv_hi[j] = (float)t->inv[j];
     t->inv_lo[j] = (float)(t->inv[j] - (double)t->inv_hi[j]);
   }
+  last_r = r; last_D = D; last_t = *t;
   return KVA_OK;
 }
 

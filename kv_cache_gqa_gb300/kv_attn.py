@@ -112,8 +112,19 @@ def _check(status: int):
         raise KvaError(status, lib().kva_last_error().decode())
 
 
+_torch = None
+
+
+def _t():
+    global _torch
+    if _torch is None:
+        import torch
+        _torch = torch
+    return _torch
+
+
 def _dtype_code(t) -> int:
-    import torch
+    torch = _t()
     if t.dtype == torch.float32:
         return KVA_F32
     if t.dtype == torch.bfloat16:
@@ -133,14 +144,15 @@ def _ptr(t) -> Optional[int]:
 
 def _host_i32(a) -> np.ndarray:
     """Host mirror (int32, C-contiguous) of an index array given as numpy or a CPU tensor."""
+    if type(a) is np.ndarray and a.dtype == np.int32 and a.flags.c_contiguous:
+        return a
     if hasattr(a, "detach"):
         a = a.detach().cpu().numpy()
     return np.ascontiguousarray(a, dtype=np.int32)
 
 
 def _stream(stream) -> Optional[int]:
-    import torch
-    s = stream if stream is not None else torch.cuda.current_stream()
+    s = stream if stream is not None else _t().cuda.current_stream()
     return s.cuda_stream
 
 
@@ -151,8 +163,19 @@ class KVCache:
     k: object
     v: object
 
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        object.__setattr__(self, "_struct", None)        # rebuilt on the next call
+
     @property
     def struct(self) -> _Cache:
+        st = getattr(self, "_struct", None)
+        if st is None:
+            st = self._build_struct()
+            object.__setattr__(self, "_struct", st)
+        return st
+
+    def _build_struct(self) -> _Cache:
         k, v = self.k, self.v
         if k.dim() != 4 or v.dim() != 4 or v.shape[:3] != k.shape[:3] or v.dtype != k.dtype:
             raise KvaError(KVA_EINVAL, "cache k/v must be [N, Hkv, W, Dk] / [N, Hkv, W, Dv] tensors of one dtype")
@@ -194,11 +217,19 @@ class Rope:
     def n_axes(self) -> int:
         return {"none": 0, "1d": 1, "2d": 2, "interleaved": 1}.get(self.kind, len(self.sections))
 
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        object.__setattr__(self, "_struct", None)        # rebuilt on the next call
+
     @property
     def struct(self) -> _Rope:
-        secs = (C.c_int32 * 4)(*(list(self.sections) + [0] * (4 - len(self.sections))))
-        return _Rope(ROPE_KINDS[self.kind], self.n_axes, secs, float(self.base), int(self.rot_offset),
-                     int(self.rot_dim))
+        st = getattr(self, "_struct", None)
+        if st is None:
+            secs = (C.c_int32 * 4)(*(list(self.sections) + [0] * (4 - len(self.sections))))
+            st = _Rope(ROPE_KINDS[self.kind], self.n_axes, secs, float(self.base), int(self.rot_offset),
+                       int(self.rot_dim))
+            object.__setattr__(self, "_struct", st)
+        return st
 
 
 def kv_cache_append_rope_qknorm(q, k, v, pos, slot, slot_host, cache: KVCache, q_out, rope: Rope,
