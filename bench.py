@@ -730,6 +730,13 @@ def run_gpu(args, rank, world, local_rank):
     ms = start.elapsed_time(end)
     max_ms = reduce_max(ms, world, device=torch.device("cuda", local_rank))
     value = aggregate_throughput(TOKENS_PER_JOB * args.steps, world, max_ms / 1e3)
+    if args.job_only:                       # counter captures: the timed job and nothing else
+        if rank == 0:
+            print(json.dumps({"case": "job_only", "ms_per_step": round(max_ms / args.steps, 4),
+                              "value": round(value, 1), "unit": UNIT}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     if in_graph_events:                     # per-kernel times: one replay of the instrumented graph
         with torch.cuda.stream(stream):
             graph_ev.replay()
@@ -961,13 +968,16 @@ def run_gpu(args, rank, world, local_rank):
 
 def lm_traffic():
     """DRAM bytes per lm_head launch from the committed ncu summary, if it was taken on the
-    current kernel source (else null)."""
+    current sources of the kernel (its .cu file and the headers it includes; else null)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)["lmhead_argmax"]
-        src = open(os.path.join(ROOT, "kv_cache_gqa_gb300", "csrc", "lmhead.cu"), "rb").read()
-        if d.get("source_sha256") == hashlib.sha256(src).hexdigest():
+        h = hashlib.sha256()
+        for rel in d["sources"]:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        if d.get("source_sha256") == h.hexdigest():
             return d["dram_bytes_per_launch"]
     except Exception:
         pass
@@ -1178,6 +1188,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="kv_attn", choices=["kv_attn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--job-only", action="store_true",
+                    help="time the job only and print a short line (for counter captures); not the benchmark line")
     ap.add_argument("--only", choices=["verify", "mla", "serving16", "lm64"], default=None,
                     help="run one sub-benchmark alone and print its figures (for counter captures); "
                          "not the benchmark line")
