@@ -384,6 +384,20 @@ uint64_t kva_launch_count(void);
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 int32_t kva_version(void);
 
+/* ---------------------------------------------------------------------------------
+ * Failure detection (no counterpart on the pages).  Every wait of a kernel on an mbarrier (a
+ * copy landing, another warp's hand-off) gives up after about 2 s of GPU time instead of
+ * hanging; the kernel then abandons its work and writes NaN into the outputs it owns (-1 into
+ * the lm_head's ids), and the device stays usable.
+ * kva_wait_timeouts: how many thread-level waits have given up on the current device since the
+ *   last reset (0 in normal operation; one abandoned kernel usually counts many), or -1 if the
+ *   count could not be read.  reset != 0 clears it.  Synchronise the streams that ran the
+ *   kernels before reading; the call is synchronous and must not be made during stream capture.
+ * kva_selftest_wait_timeout: launches one kernel whose wait nothing satisfies, so that it gives
+ *   up after the limit: a test of the timeout path that neither hangs nor faults the GPU. */
+int64_t kva_wait_timeouts(int32_t reset);
+kva_status kva_selftest_wait_timeout(kva_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -161,9 +161,13 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait: polls the barrier and gives up after WAIT_LIMIT_NS of wall time,
-// returning false (the caller records a timeout and stops using the buffer), so a lost
-// transaction can never hang the GPU.
+// Waits that gave up in the kernels of this translation unit since the last reset (each unit
+// has its own copy; the host side sums them, see register_wait_counter below).
+static __device__ unsigned int g_wait_timeouts;
+
+// Bounded wait: polls the barrier and gives up after WAIT_LIMIT_NS of wall time, counts the
+// give-up in g_wait_timeouts and returns false (the caller stops using the buffer and marks
+// its outputs), so a lost transaction can never hang the GPU.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase) {
   if (mbar_try_wait(bar, phase)) return true;
@@ -171,9 +175,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase)
   for (;;) {
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, phase)) return true;
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+      atomicAdd(&g_wait_timeouts, 1u);
+      return false;
+    }
   }
 }
+
+// Host side: every translation unit that includes this header registers a reader of its
+// g_wait_timeouts when the library loads; kva_wait_timeouts() sums them.
+void register_wait_counter(cudaError_t (*read)(unsigned* value, bool reset));
+namespace {
+cudaError_t read_wait_timeouts_here(unsigned* value, bool reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_wait_timeouts, sizeof(unsigned));
+  if (e == cudaSuccess && reset) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero));
+  }
+  return e;
+}
+struct WaitCounterRegistration {
+  WaitCounterRegistration() { register_wait_counter(&read_wait_timeouts_here); }
+};
+const WaitCounterRegistration g_wait_counter_registration;
+}  // namespace
 
 // 1-D bulk copy global -> shared, completion signalled on `bar` as transaction bytes.
 // dst, src 16-byte aligned, bytes a multiple of 16.
@@ -183,9 +208,5 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-// Device-side status word written when a bounded wait gives up.
-struct DeviceStatus {
-  unsigned int timeouts;
-};
 
 }  // namespace kva

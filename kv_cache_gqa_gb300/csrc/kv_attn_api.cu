@@ -7,12 +7,33 @@
 #include <cstdio>
 #include <cstring>
 
+#include <vector>
+
+#include "common.cuh"
 #include "kv_attn.h"
 #include "launch.h"
 
 namespace kva {
 
 static std::atomic<unsigned long long> g_launches{0};
+
+// Readers of the per-translation-unit wait give-up counters (registered at library load).
+static std::vector<cudaError_t (*)(unsigned*, bool)>& wait_counters() {
+  static std::vector<cudaError_t (*)(unsigned*, bool)> v;
+  return v;
+}
+void register_wait_counter(cudaError_t (*read)(unsigned*, bool)) { wait_counters().push_back(read); }
+
+// One thread waits on a barrier that nothing arrives on: the wait gives up after its limit.
+__global__ void selftest_wait_kernel() {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0u);
+}
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int lmhead_max_hidden();
@@ -233,6 +254,23 @@ const char* kva_strerror(kva_status s) {
 }
 
 const char* kva_last_error(void) { return g_msg; }
+
+int64_t kva_wait_timeouts(int32_t reset) {
+  int64_t total = 0;
+  for (auto read : wait_counters()) {
+    unsigned v = 0;
+    if (read(&v, reset != 0) != cudaSuccess) return -1;
+    total += v;
+  }
+  return total;
+}
+
+kva_status kva_selftest_wait_timeout(kva_stream stream) {
+  selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(1);
+  return cuda_status(e, "self-test launch");
+}
 uint64_t kva_launch_count(void) { return g_launches.load(); }
 int32_t kva_version(void) { return 100; }
 

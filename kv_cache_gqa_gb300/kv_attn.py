@@ -101,6 +101,10 @@ def lib() -> C.CDLL:
         L.kva_last_error.restype = C.c_char_p
         L.kva_launch_count.restype = C.c_uint64
         L.kva_version.restype = C.c_int32
+        L.kva_wait_timeouts.argtypes = [i32]
+        L.kva_wait_timeouts.restype = i64
+        L.kva_selftest_wait_timeout.argtypes = [vp]
+        L.kva_selftest_wait_timeout.restype = C.c_int
         for f in ("kv_cache_append_rope_qknorm", "kv_attn_prefill", "kv_attn_decode", "lmhead_argmax"):
             getattr(L, f).restype = C.c_int
         _lib = L
@@ -365,6 +369,12 @@ def launch_count() -> int:
 
 def version() -> int:
     return int(lib().kva_version())
+
+
+def wait_timeouts(reset: bool = False) -> int:
+    """kva_wait_timeouts: kernel waits that gave up on the current device since the last reset
+    (synchronise first); -1 if the count could not be read."""
+    return int(lib().kva_wait_timeouts(1 if reset else 0))
 
 
 # Raw C entry points for callers that marshal pointers themselves (tests of the ABI).
