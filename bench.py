@@ -1167,14 +1167,15 @@ def run_reference(args, rank, world):
     wall, jobs, sample = oracle_job_samples(n=args.steps, warmup=args.warmup)
     job_s = statistics.median(jobs)
     value = TOKENS_PER_JOB / job_s
-    cfg = job_config()
-    cfg["step"] = "one bounded oracle sample of the job (see cpu_baseline.sample)"
+    cfg = job_config()                      # the same workload and keys as the GPU arm's line
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.median(wall) * 1e3, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": cfg,
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "host": host_info(), "sample": sample,
+                             "step": "one bounded sample of the job per step; ms_per_step is the sample's "
+                                     "wall time, value the job throughput it extrapolates to",
                              "job_seconds_extrapolated": round(job_s, 2)},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

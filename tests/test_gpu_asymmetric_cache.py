@@ -252,3 +252,51 @@ def test_mla_append_prefill_decode_chain(K):
     np.testing.assert_array_equal(kh[:, :n, :128], ck[:, :n, :128])
     np.testing.assert_array_equal(host(vc)[0][:, :n], cv[:, :n])
     assert not np.any(kh[:, n:]) and not np.any(host(vc)[0][:, n:])
+
+
+def test_mla_benchmark_shapes_full_window(K):
+    """The shapes the benchmark times for the MLA-expanded cache: a 512-token prompt filling the
+    512-slot window (append + causal prefill), then a token written into the last slot and
+    decoded over the whole window; sampled prompt rows and the token against the oracle."""
+    torch = T()
+    rng = np.random.default_rng(78)
+    H, W = 32, 512
+    rope_o = _orope("interleaved", 1e6, 128, 64)
+    rope_k = K.Rope(**MLA_ROPE)
+    kc = torch.zeros((1, H, W, DK), device="cuda", dtype=torch.bfloat16)
+    vc = torch.zeros((1, H, W, DV), device="cuda", dtype=torch.bfloat16)
+    cache = K.KVCache(kc, vc)
+    q = O.store(rng.standard_normal((1, W, H, DK)), "bf16")
+    k = O.store(rng.standard_normal((1, W, H, DK)), "bf16")
+    v = O.store(rng.standard_normal((1, W, H, DV)), "bf16")
+    pos = np.arange(W, dtype=np.int32).reshape(1, W, 1)
+    slot = np.arange(W, dtype=np.int32).reshape(1, W)
+    q_out = torch.empty((1, W, H, DK), device="cuda", dtype=torch.bfloat16)
+    K.kv_cache_append_rope_qknorm(dev(q, torch.bfloat16), dev(k, torch.bfloat16), dev(v, torch.bfloat16), dev(pos),
+                                  dev(slot), slot, cache, q_out, rope_k)
+    out = torch.empty((1, W, H, DV), device="cuda")
+    K.kv_attn_prefill(q_out, cache, out, mask="causal")
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 127, 128, 255, 256, 383, 384, 510, 511])
+    kh, vh, qh = host(kc)[0], host(vc)[0], host(q_out)[0]
+    allowed = np.zeros((rows.size, W), bool)
+    for i, r in enumerate(rows):
+        allowed[i, :r + 1] = True
+    assert_bf16_close(host(out)[0][rows], O.attend(qh[rows], kh, vh, allowed), "prompt prefill rows")
+    # the token: written into slot W - 1 (position W - 1), decode over all W slots
+    qn = O.store(rng.standard_normal((1, 1, H, DK)), "bf16")
+    kn = O.store(rng.standard_normal((1, 1, H, DK)), "bf16")
+    vn = O.store(rng.standard_normal((1, 1, H, DV)), "bf16")
+    p = np.array([[[W - 1]]], np.int32)
+    sl = np.array([[W - 1]], np.int32)
+    qo = torch.empty((1, 1, H, DK), device="cuda", dtype=torch.bfloat16)
+    K.kv_cache_append_rope_qknorm(dev(qn, torch.bfloat16), dev(kn, torch.bfloat16), dev(vn, torch.bfloat16), dev(p),
+                                  dev(sl), sl, cache, qo, rope_k)
+    lens = np.array([W], np.int32)
+    ws = torch.zeros(K.decode_workspace_bytes(1, H, H, W, DV), dtype=torch.uint8, device="cuda")
+    o = torch.empty((1, H, DV), device="cuda")
+    K.kv_attn_decode(qo[:, 0], cache, dev(lens), lens, o, ws)
+    torch.cuda.synchronize()
+    kex = O.qk_transform(kn[0], p[0], None, 1e-6, rope_o, False)            # [1, H, DK]
+    assert_bf16_store(bf16_bits(kc)[0][:, W - 1:W], kex.transpose(1, 0, 2), "token K row")
+    assert_fp32_close(host(o)[0], O.decode(host(qo)[0, 0], host(kc)[0], host(vc)[0], W), "token decode")

@@ -31,6 +31,7 @@ CASES = [
     # B, H, V, wdt, top_k, norm
     (1, 1024, 151936, "bf16", 1, True),
     (1, 1024, 151936, "bf16", 5, True),
+    (1, 1024, 151936, "bf16", 8, True),     # the benchmark's final-norm top-8
     (1, 1024, 151936, "bf16", 32, False),
     (1, 2048, 40000, "bf16", 8, True),
     (1, 2560, 9001, "bf16", 1, True),

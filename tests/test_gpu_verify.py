@@ -57,6 +57,27 @@ def test_verify_parity(K, k, G, q_dt):
         assert_bf16_close(got[b].reshape(-1, D), ref.reshape(-1, D), f"verify b={b} L={L} k={k}")
 
 
+def test_verify_benchmark_configuration(K):
+    """The launch the benchmark times: 64 sequences x 2048 valid slots, 16-token blocks, 16/8 heads,
+    bf16 queries (the tcgen05 form); sampled sequences against the oracle's verify block."""
+    torch = _torch()
+    B, Hkv, Hq, D, L, k = 64, 8, 16, 128, 2048, 16
+    g = torch.Generator(device="cuda"); g.manual_seed(7)
+    kc = torch.randn((B, Hkv, L, D), device="cuda", generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, Hkv, L, D), device="cuda", generator=g).to(torch.bfloat16)
+    q = torch.randn((B, k, Hq, D), device="cuda", generator=g).to(torch.bfloat16)
+    lengths = np.full(B, L, np.int32)
+    ws = torch.zeros(K.verify_workspace_bytes(B, Hkv, Hq, k, L, D), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, k, Hq, D), float("nan"), device="cuda")
+    K.kv_attn_verify(q, K.KVCache(kc, vc), dev(lengths), lengths, out, ws)
+    torch.cuda.synchronize()
+    got = host(out)
+    assert np.all(np.isfinite(got))
+    for b in (0, 1, 31, 63):
+        ref = O.verify_block(host(q[b]), host(kc[b]), host(vc[b]), L)
+        assert_bf16_close(got[b].reshape(-1, D), ref.reshape(-1, D), f"verify b={b}")
+
+
 def test_verify_single_token_equals_decode(K):
     torch = _torch()
     rng = np.random.default_rng(5)

@@ -185,7 +185,9 @@ def test_qwen3_28_layers_full(K, fused):
 # ----------------------------------------------------------------------------
 # 3. VLM image span: xdRoPE sections, norm after RoPE, causal, then 64 decode steps
 # ----------------------------------------------------------------------------
-def test_image_span_xdrope(K):
+@pytest.mark.parametrize("fused", [True, False], ids=["decode_step", "append_then_decode"])
+def test_image_span_xdrope(K, fused):
+    """fused: the 64 decode steps through kv_attn_decode_step, as the benchmark times them."""
     torch = T()
     w = WL.image_span_prefill(0)
     S, W, steps = w["pos"].shape[0], w["capacity"], w["dq"].shape[0]
@@ -207,12 +209,18 @@ def test_image_span_xdrope(K):
         t = S + s
         qd = torch.empty((1, 1, Hq, D), device="cuda", dtype=torch.bfloat16)
         sl = np.array([[t]], np.int32)
-        K.kv_cache_append_rope_qknorm(dev(w["dq"][None, s:s + 1]), dev(w["dk"][None, s:s + 1]),
-                                      dev(w["dv"][None, s:s + 1]), dev(w["dpos"][None, s:s + 1]), dev(sl), sl, cache,
-                                      qd, rope, q_norm_w=qw, k_norm_w=kw, eps=w["eps"], norm_after_rope=True)
         o = torch.empty((1, Hq, D), device="cuda")
         L = np.array([t + 1], np.int32)
-        K.kv_attn_decode(qd[:, 0], cache, dev(L), L, o, ws)
+        if fused:
+            K.kv_attn_decode_step(dev(w["dq"][s:s + 1]), dev(w["dk"][s:s + 1]), dev(w["dv"][s:s + 1]),
+                                  dev(w["dpos"][s:s + 1]), cache, dev(L), L, o, ws, rope, q_norm_w=qw, k_norm_w=kw,
+                                  eps=w["eps"], norm_after_rope=True)
+        else:
+            K.kv_cache_append_rope_qknorm(dev(w["dq"][None, s:s + 1]), dev(w["dk"][None, s:s + 1]),
+                                          dev(w["dv"][None, s:s + 1]), dev(w["dpos"][None, s:s + 1]), dev(sl), sl,
+                                          cache, qd, rope, q_norm_w=qw, k_norm_w=kw, eps=w["eps"],
+                                          norm_after_rope=True)
+            K.kv_attn_decode(qd[:, 0], cache, dev(L), L, o, ws)
         dec.append(o)
     torch.cuda.synchronize()
 
