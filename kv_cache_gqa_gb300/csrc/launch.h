@@ -198,6 +198,7 @@ struct PrefillArgs {
   int Dv;                     // V row width (= D unless asymmetric)
   int64_t inst_stride_v;
   float scale_log2;
+  int single_slot;            // tcgen05 form: one query tile per work unit (set by its launcher)
 };
 int lmhead_max_hidden();
 cudaError_t launch_prefill(const PrefillArgs& a, kva_dtype dtype, cudaStream_t s);

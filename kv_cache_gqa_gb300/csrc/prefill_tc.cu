@@ -151,18 +151,23 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 // Unit geometry: units are numbered x fastest (KV-head pair or head), then instance, then
-// the row-tile index z, with z = 0 the heaviest causal tiles.
+// the row-tile index z, with z = 0 the heaviest causal tiles.  When even one tile per unit
+// leaves SMs idle (a short prompt of one layer), every unit holds a single query tile (slot 1
+// empty), so twice as many SMs share the work.
 struct Units {
   int X, Z, total;
 };
-__device__ __forceinline__ Units unit_geometry(const PrefillArgs& a) {
-  const int nq = (a.S + BM - 1) / BM;
-  const bool pair_heads = (a.Hq / a.Hkv) % 2 == 0;
+__host__ __device__ __forceinline__ Units unit_geometry_of(int N, int S, int Hq, int Hkv, bool single) {
+  const int nq = (S + BM - 1) / BM;
+  const bool pair_heads = (Hq / Hkv) % 2 == 0;
   Units g;
-  g.X = pair_heads ? a.Hq / 2 : a.Hq;
-  g.Z = pair_heads ? nq : (nq + 1) / 2;
-  g.total = g.X * a.N * g.Z;
+  g.X = (single || !pair_heads) ? Hq : Hq / 2;
+  g.Z = (single || pair_heads) ? nq : (nq + 1) / 2;
+  g.total = g.X * N * g.Z;
   return g;
+}
+__device__ __forceinline__ Units unit_geometry(const PrefillArgs& a) {
+  return unit_geometry_of(a.N, a.S, a.Hq, a.Hkv, a.single_slot != 0);
 }
 // The r-th unit of CTA b out of P (snake order), or -1 past the end.
 __device__ __forceinline__ int unit_of(int r, int b, int P, int total) {
@@ -179,7 +184,11 @@ __device__ __forceinline__ Slots unit_slots(const PrefillArgs& a, const Units& g
   const int nq = (a.S + BM - 1) / BM;
   const int x = u % g.X, n = (u / g.X) % a.N, z = u / (g.X * a.N);
   sl.n = n;
-  if ((a.Hq / a.Hkv) % 2 == 0) {   // the two heads of a pair, heaviest row tiles first
+  if (a.single_slot) {             // one query tile, heaviest row tiles first
+    sl.h[0] = sl.h[1] = x;
+    sl.qt[0] = nq - 1 - z;
+    sl.qt[1] = -1;
+  } else if ((a.Hq / a.Hkv) % 2 == 0) {   // the two heads of a pair, heaviest row tiles first
     sl.h[0] = 2 * x; sl.h[1] = 2 * x + 1;
     sl.qt[0] = sl.qt[1] = nq - 1 - z;
   } else {                         // row tiles z and nq-1-z of one head
@@ -786,14 +795,19 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   CUtensorMap mo;
   std::memset(&mo, 0, sizeof(mo));           // unused when rows are permuted
   if (a.row_of_slot == nullptr && (e = make_out_map(&mo, a)) != cudaSuccess) return e;
-  // units: the two heads of a GQA pair at one row tile, else two row tiles of one head
-  const int nq = (a.S + BM - 1) / BM;
+  // units: the two heads of a GQA pair at one row tile, else two row tiles of one head; one
+  // query tile per unit when even that many units would fill at most one wave
+  const long long nq = (a.S + BM - 1) / BM;
   const int G = a.Hq / a.Hkv;
-  const long long units = (G % 2 == 0) ? (long long)(a.Hq / 2) * a.N * nq : (long long)a.Hq * a.N * ((nq + 1) / 2);
-  if (units <= 0) return cudaSuccess;
+  const long long paired = (G % 2 == 0) ? (long long)(a.Hq / 2) * a.N * nq : (long long)a.Hq * a.N * ((nq + 1) / 2);
+  if (paired <= 0) return cudaSuccess;
+  const long long singles = (long long)a.Hq * a.N * nq;
+  PrefillArgs b = a;
+  b.single_slot = singles <= prefill_num_sms() ? 1 : 0;
+  const long long units = b.single_slot ? singles : paired;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)std::min<long long>(units, prefill_num_sms());
-  return launch_pdl(prefill_tc_kernel<D, DV, NST>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, a, mk, mv, mq, mo);
+  return launch_pdl(prefill_tc_kernel<D, DV, NST>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, b, mk, mv, mq, mo);
 }
 
 }  // namespace

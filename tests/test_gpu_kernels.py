@@ -236,16 +236,25 @@ def test_prefill_bf16_ragged(K, S, mask):
     _prefill_case(K, 128, S, mask, "bf16", 2, seed=S * 11 + len(mask))
 
 
+@pytest.mark.parametrize("mask", ["causal", "full", "segment"])
+@pytest.mark.parametrize("G", [1, 2])
+def test_prefill_bf16_many_instances(K, mask, G):
+    """Enough instances that the tensor-core prefill pairs two query tiles per work unit (the
+    small cases above give one tile per unit): the heads of a GQA pair, or row tiles t and
+    n-1-t of one head."""
+    _prefill_case(K, 128, 300, mask, "bf16", G, seed=500 + G + len(mask), N=48, Hkv=2)
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("mask", ["full", "segment"])
 def test_prefill_d72_mha_permuted(K, dt, mask):
     _prefill_case(K, 72, 150, mask, dt, 1, seed=99, Hkv=3, perm=True)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("dt,N", [("bf16", 2), ("f32", 2), ("bf16", 48)])
 @pytest.mark.parametrize("layout", ["image", "spans"])
-def test_prefill_causal_segment(K, dt, layout):
-    """Causal mask with image spans fully visible to their own rows."""
+def test_prefill_causal_segment(K, dt, N, layout):
+    """Causal mask with image spans fully visible to their own rows (N = 48: paired tiles)."""
     torch = T()
     rng = np.random.default_rng(zlib.crc32(repr(("cseg", dt, layout)).encode()))
     if layout == "image":
@@ -254,7 +263,7 @@ def test_prefill_causal_segment(K, dt, layout):
         seg = np.arange(300, dtype=np.int32)
         for s0, s1 in ((5, 40), (120, 130), (131, 256), (290, 300)):
             seg[s0:s1] = s0
-    S, N, Hkv, Hq, D = seg.size, 2, 2, 4, 128
+    S, Hkv, Hq, D = seg.size, 2, 4, 128
     q = O.store(rng.standard_normal((N, S, Hq, D)), dt)
     kc = O.store(rng.standard_normal((N, Hkv, S + 8, D)), dt)
     vc = O.store(rng.standard_normal((N, Hkv, S + 8, D)), dt)
