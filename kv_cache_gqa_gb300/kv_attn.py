@@ -295,6 +295,20 @@ def kv_attn_decode(q, cache: KVCache, lengths, lengths_host, out, workspace, sca
         _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+_norm_cache = {}
+
+
+def _norm_struct(q_norm_w, k_norm_w, inst_stride, eps, after):
+    """The QK-Norm descriptor (cached: a decode loop passes the same weights every step)."""
+    key = (_ptr(q_norm_w), _ptr(k_norm_w), int(inst_stride), float(eps), int(after))
+    st = _norm_cache.get(key)
+    if st is None:
+        if len(_norm_cache) > 64:
+            _norm_cache.clear()
+        st = _norm_cache[key] = _Norm(key[0], key[1], key[2], key[3], key[4])
+    return st
+
+
 def kv_attn_decode_step(q, k, v, pos, cache: KVCache, lengths, lengths_host, out, workspace, rope: Rope,
                         q_norm_w=None, k_norm_w=None, eps: float = 1e-6, norm_after_rope: bool = False,
                         norm_inst_stride: int = 0, pos_inst_stride: Optional[int] = None, q_out=None,
@@ -306,7 +320,7 @@ def kv_attn_decode_step(q, k, v, pos, cache: KVCache, lengths, lengths_host, out
     if pos_inst_stride is None:
         pos_inst_stride = 0 if (pos is None or pos.dim() < 2 or pos.shape[0] == 1) else pos.shape[-1]
     lh = _host_i32(lengths_host)
-    norm = _Norm(_ptr(q_norm_w), _ptr(k_norm_w), norm_inst_stride, eps, 1 if norm_after_rope else 0)
+    norm = _norm_struct(q_norm_w, k_norm_w, norm_inst_stride, eps, 1 if norm_after_rope else 0)
     _check(lib().kv_attn_decode_step(
         _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(pos), pos_inst_stride, norm, rope.struct, cache.struct,
         _ptr(lengths), lh.ctypes.data, B, Hq, float(scale), _ptr(q_out),
