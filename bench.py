@@ -374,11 +374,10 @@ def configs_bench(torch, K, stream, hbm, bf16):
 
     def tiny_run():
         tiny_prefill()
-        for t in range(P_, W_):
-            K.kv_cache_append_rope_qknorm(q_all[:, t:t + 1], k_all[:, t:t + 1], v_all[:, t:t + 1], pos_t[t],
-                                          slot_t[t], slot_h[:, t:t + 1], cache, q_dec, rope, q_norm_w=qw,
-                                          k_norm_w=kw, eps=w["eps"])
-            K.kv_attn_decode(q_dec[:, 0], cache, lens_d[t], lens_h[t], o_dec[t - P_:t - P_ + 1], ws)
+        for t in range(P_, W_):                      # fused append + decode, one launch per step
+            K.kv_attn_decode_step(q_all[0, t:t + 1], k_all[0, t:t + 1], v_all[0, t:t + 1], pos_t[t][0], cache,
+                                  lens_d[t], lens_h[t], o_dec[t - P_:t - P_ + 1], ws, rope, q_norm_w=qw, k_norm_w=kw,
+                                  eps=w["eps"])
     with torch.cuda.stream(stream):
         tiny_run()
     torch.cuda.synchronize()
@@ -386,7 +385,7 @@ def configs_bench(torch, K, stream, hbm, bf16):
     pre_ms = graph_seq_ms(torch, stream, [tiny_prefill], reps=20)
     res["tiny_fp32"] = {
         "config": "1 layer, 16/8 heads, D=128, fp32 cache of 80 slots: 64-token append + causal prefill, then "
-                  "16 steps of append + decode (34 launches)",
+                  "16 fused append + decode steps (18 launches)",
         "run_us": round(run_ms * 1e3, 1), "prefill_phase_us": round(pre_ms * 1e3, 1),
         "decode_step_us": round((run_ms - pre_ms) * 1e3 / (W_ - P_), 2),
         "note": "latency-bound (17 MFLOP, ~3 MB): no roofline; the data stays in L2"}
@@ -616,10 +615,9 @@ def mla_bench(torch, K, stream):
     o = torch.empty((1, H, DVm), device="cuda")
     ws = torch.zeros(K.decode_workspace_bytes(1, H, H, W, DVm), dtype=torch.uint8, device="cuda")
 
-    def token():
+    def token():                                     # fused append + decode per layer
         for c in caches:
-            K.kv_cache_append_rope_qknorm(qn, kn, vn, pn, sn, sn_h, c, qo, rope)
-            K.kv_attn_decode(qo[:, 0], c, lens, lens_h, o, ws)
+            K.kv_attn_decode_step(qn[0], kn[0], vn[0], pn[0], c, lens, lens_h, o, ws, rope)
 
     B2, L2 = 16, 4096
     kb = torch.randn((B2, H, L2, DKm), device="cuda", generator=g).to(bf)
@@ -642,7 +640,7 @@ def mla_bench(torch, K, stream):
     del kb, vb, kc, vc
     return {"config": f"{Lr} layers, {H}/{H} heads, K {DKm} / V {DVm}, {W}-slot bf16 window, interleaved RoPE "
                       f"on dims 128..191; prompt = {W} tokens (append + causal prefill per layer), token = one "
-                      f"decode step at the full window (append + decode per layer)",
+                      f"decode step at the full window (one fused append + decode launch per layer)",
             "prompt_ms": round(prompt_ms, 3), "prompt_tokens_per_s": round(W / (prompt_ms / 1e3), 1),
             "token_us": round(token_ms * 1e3, 1), "token_per_layer_us": round(token_ms * 1e3 / Lr, 2),
             "token_cache_GB/s": round(tok_bytes / (token_ms / 1e3) / 1e9, 1),

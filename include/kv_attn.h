@@ -215,14 +215,17 @@ kva_status kv_attn_decode(
  *   Youtu-VL-4B ncnn port, step 6; each step attends to the whole prefix: step 8).  Every
  *   CTA derives the normalised, rotated query rows of its group itself; the CTA that owns the
  *   last chunk of an instance also writes the new K/V row into slot L_b - 1.
- *  q        [B,Hq,D], k, v [B,Hkv,D] of in_dtype: the new token's projections (device)
+ *  q        [B,Hq,Dk], k [B,Hkv,Dk], v [B,Hkv,Dv] of in_dtype: the new token's projections (device)
  *  pos      [.., n_axes] int32 position ids (device); instance b reads pos + b*pos_inst_stride
  *  lengths  [B] valid slots including the new token (device) + lengths_host (host mirror)
- *  q_out    nullable [B,Hq,D] of q_out_dtype: the transformed queries, if wanted
- *  out      [B,Hq,D] float32;  workspace as for kv_attn_decode
- *  Requires a symmetric bf16 cache with head_dim 128, RoPE over the whole head and Hq/Hkv in
- *  {1, 2, 4} (else KVA_EUNSUPPORTED: call the two entry points).  Errors as the two calls it
- *  replaces. */
+ *  q_out    nullable [B,Hq,Dk] of q_out_dtype: the transformed queries, if wanted
+ *  out      [B,Hq,Dv] float32;  workspace as for kv_attn_decode
+ *  Built for (Dk, Dv) = (128, 128) bf16 or fp32 caches and the asymmetric (192, 128) cache,
+ *  any RoPE kind over the whole head or a sub-range (rope.rot_offset, rope.rot_dim), and
+ *  Hq/Hkv in {1, 2, 4} (else KVA_EUNSUPPORTED: call the two entry points).  A symmetric bf16
+ *  cache with whole-head RoPE runs on the tensor-core decode kernel, the other forms on the
+ *  CUDA-core one.  workspace: kva_decode_workspace_size with head_dim = Dv.  Errors as the two
+ *  calls it replaces. */
 kva_status kv_attn_decode_step(
     const void* q, const void* k, const void* v, kva_dtype in_dtype,
     const int32_t* pos, int64_t pos_inst_stride,

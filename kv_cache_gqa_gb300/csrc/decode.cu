@@ -52,9 +52,80 @@ template <> __device__ __forceinline__ void chunk_to_f32<float, 4>(uint4 w, floa
   x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
 }
 
-template <typename CacheT, int G, int DK>
+// One row of the new token (q of one head, k or v) held 8 elements per lane at dims
+// [8 lane, 8 lane + 8): QK-Norm and RoPE in the configured order for q/k rows, none for v.  The
+// rotation covers dims [ro, ro + rw) in rotate-half, 2D-halves or de-interleaved form; `mirror`
+// (the row's shared buffer) lets every element read its partner wherever it sits.
+__device__ __forceinline__ void step_row_general(float (&x)[8], int e0, bool on, int width, const float* w,
+                                                 bool qk, const StepArgs& st, const float* cs, const float* sn,
+                                                 float* mirror) {
+  if (!qk) return;
+  auto apply_norm = [&]() {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+    if (w != nullptr && on) {
+      float wv[8];
+      load8(w + e0, wv);
+      const float rinv = 1.0f / sqrtf(ss / (float)width + st.eps);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = x[i] * rinv * wv[i];
+    }
+  };
+  if (!st.after_rope) apply_norm();
+  const int kind_r = st.rope.kind;
+  if (kind_r != KVA_ROPE_NONE) {
+    const int ro = st.rot_offset, rw = st.rot_dim, half = rw / 2, quarter = rw / 4;
+    if (on) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mirror[e0 + i] = x[i];
+    }
+    __syncwarp();
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int dd = e0 + i - ro;
+      y[i] = x[i];
+      if (on && dd >= 0 && dd < rw) {
+        const float* xr = mirror + ro;
+        if (kind_r == KVA_ROPE_INTERLEAVED) {
+          const int j = dd < half ? dd : dd - half;
+          const float ev = xr[2 * j], od = xr[2 * j + 1];
+          y[i] = dd < half ? ev * cs[j] - od * sn[j] : od * cs[j] + ev * sn[j];
+        } else if (kind_r == KVA_ROPE_2D) {
+          const int bb = dd / half, e2 = dd - bb * half;
+          const bool lo = e2 < quarter;
+          const int j = bb * quarter + (lo ? e2 : e2 - quarter);
+          const float pv = xr[lo ? dd + quarter : dd - quarter];
+          y[i] = x[i] * cs[j] + (lo ? -pv : pv) * sn[j];
+        } else {
+          const bool lo = dd < half;
+          const int j = lo ? dd : dd - half;
+          const float pv = xr[lo ? dd + half : dd - half];
+          y[i] = x[i] * cs[j] + (lo ? -pv : pv) * sn[j];
+        }
+      }
+    }
+    __syncwarp();                               // mirror reads done before it is rewritten
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = y[i];
+  }
+  if (st.after_rope) apply_norm();
+}
+
+__device__ __forceinline__ void load8_dt(const void* p, int dt, int64_t i, float (&x)[8]) {
+  if (dt == KVA_BF16) load8(reinterpret_cast<const bf16_t*>(p) + i, x);
+  else load8(reinterpret_cast<const float*>(p) + i, x);
+}
+
+__device__ __forceinline__ void store1(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store1(bf16_t* p, float v) { p->bits = (uint16_t)f32_to_bf16_rne(v); }
+
+template <typename CacheT, int G, int DK, bool FUSED>
 __global__ void __launch_bounds__(THREADS, DK > D ? 1 : 2)   // wide K tiles: one CTA per SM by smem
-decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
+decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype, const __grid_constant__ StepArgs st) {
   constexpr int ES = ElemSize<CacheT>::value;
   constexpr int KT = DecodeTile<CacheT>::KT;   // keys per stage
   constexpr int ROWK = DK * ES;                // bytes per K row
@@ -120,6 +191,53 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
     }
   }
 
+  // ---- fused step: the new token's rows, transformed while the first copies are in flight.
+  // Warps 0..G-1 take the group's query rows; in the last chunk warps G and G+1 take k and v,
+  // write them into slot L-1 of the cache and keep them for the stage that holds that slot
+  // (patched in shared memory: the copy may have read the slot before the write landed).
+  constexpr int NROW = FUSED ? G + 2 : 1;
+  constexpr int RW = FUSED ? 256 : 8;
+  __shared__ float f_cos[FUSED ? MAX_ROPE_FREQ : 1], f_sin[FUSED ? MAX_ROPE_FREQ : 1];
+  __shared__ __align__(16) float f_rows[NROW][RW];
+  const bool last_chunk = (c == n_chunks - 1);
+  if constexpr (FUSED) {
+    if (st.rope.kind != KVA_ROPE_NONE)
+      for (int j = tid; j < st.rot_dim / 2; j += THREADS) {
+        const int32_t p = st.pos[(int64_t)b * st.pos_stride + st.rope.axis[j]];
+        rope_cos_sin(p, st.rope.inv_hi[j], st.rope.inv_lo[j], st.rope.inv[j], &f_cos[j], &f_sin[j]);
+      }
+    __syncthreads();
+    if (warp < G || (last_chunk && warp < G + 2)) {
+      const int kind = warp < G ? 0 : (warp == G ? 1 : 2);   // q, k, v
+      const int width = kind == 2 ? D : DK;
+      const int e0 = lane * 8;
+      const bool on = e0 < width;
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const int64_t row = kind == 0 ? ((int64_t)b * a.Hq + g * G + warp) * DK
+                                    : ((int64_t)b * a.Hkv + g) * (kind == 1 ? DK : D);
+      if (on) load8_dt(kind == 0 ? st.q : (kind == 1 ? st.k : st.v), st.in_dtype, row + e0, x);
+      const float* w = kind == 0 ? (st.q_w ? st.q_w + (int64_t)b * st.w_stride : nullptr)
+                                 : (st.k_w ? st.k_w + (int64_t)b * st.w_stride : nullptr);
+      step_row_general(x, e0, on, width, w, kind <= 1, st, f_cos, f_sin, f_rows[warp]);
+      if (on) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f_rows[warp][e0 + i] = x[i];
+        if (kind == 0 && st.q_out && c == 0) {
+          if (st.q_out_dtype == KVA_BF16) store8(reinterpret_cast<bf16_t*>(st.q_out) + row + e0, x);
+          else store8(reinterpret_cast<float*>(st.q_out) + row + e0, x);
+        }
+        if (kind >= 1 && L - 1 < a.capacity) {
+          CacheT* dst = kind == 1 ? reinterpret_cast<CacheT*>(const_cast<void*>(a.kc)) +
+                                        (int64_t)b * a.inst_stride + ((int64_t)g * a.capacity + (L - 1)) * DK
+                                  : reinterpret_cast<CacheT*>(const_cast<void*>(a.vc)) +
+                                        (int64_t)b * a.inst_stride_v + ((int64_t)g * a.capacity + (L - 1)) * D;
+          store8(dst + e0, x);
+        }
+      }
+    }
+    __syncthreads();
+  }
+
   // Query registers for the QK phase: lane owns DK/8 dims, NCH chunks of CH elements at
   // element offsets CH*(lane&7) + 8*CH*i.  Pre-scaled so dots are log2-domain logits.
   const int l8 = lane & 7;
@@ -131,7 +249,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
     for (int i = 0; i < NCH; ++i)
 #pragma unroll
       for (int e = 0; e < CH; ++e)
-        qv[hh][i * CH + e] = load_q(a.q, q_dtype, qbase + CH * l8 + 8 * CH * i + e) * a.scale_log2;
+        qv[hh][i * CH + e] = (FUSED ? f_rows[FUSED ? hh : 0][(CH * l8 + 8 * CH * i + e) % RW]
+                                    : load_q(a.q, q_dtype, qbase + CH * l8 + 8 * CH * i + e)) * a.scale_log2;
   }
 
   float acc[G][4];
@@ -149,6 +268,16 @@ decode_kernel(const __grid_constant__ DecodeArgs a, kva_dtype q_dtype) {
     __syncthreads();
     if (s_flag) { timed_out = true; break; }
     const int nk = min(KT, k1 - (k0 + it * KT));
+    if constexpr (FUSED) {
+      const int prow = (L - 1) - (k0 + it * KT);   // the new token's slot in this stage
+      if (last_chunk && prow >= 0 && prow < nk) {
+        CacheT* pk = reinterpret_cast<CacheT*>(sK + stage * TILEK + prow * ROWK);
+        CacheT* pv = reinterpret_cast<CacheT*>(sV + stage * TILEB + prow * ROWB);
+        for (int e = tid; e < DK; e += THREADS) store1(pk + e, f_rows[FUSED ? G : 0][e % RW]);
+        for (int e = tid; e < D; e += THREADS) store1(pv + e, f_rows[FUSED ? G + 1 : 0][e % RW]);
+        __syncthreads();
+      }
+    }
     const unsigned char* tK = sK + stage * TILEK;
     const unsigned char* tV = sV + stage * TILEB;
 
@@ -311,26 +440,26 @@ size_t decode_smem_bytes() {
          sizeof(float) * (2 * G * KT + 3 * G) + 16;
 }
 
-template <typename CacheT, int G, int DK>
-cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
+template <typename CacheT, int G, int DK, bool FUSED>
+cudaError_t launch_g(const DecodeArgs& a, kva_dtype q_dtype, const StepArgs& st, cudaStream_t s) {
   const size_t smem = decode_smem_bytes<CacheT, G, DK>();
   static DeviceOnce configured;
   if (!configured.done()) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<CacheT, G, DK>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<CacheT, G, DK, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured.mark();
   }
   dim3 grid(a.max_chunks, a.Hkv, a.B);
-  return launch_pdl(decode_kernel<CacheT, G, DK>, grid, dim3(THREADS), smem, s, a, q_dtype);
+  return launch_pdl(decode_kernel<CacheT, G, DK, FUSED>, grid, dim3(THREADS), smem, s, a, q_dtype, st);
 }
 
-template <typename CacheT, int DK>
-cudaError_t launch_t(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s) {
+template <typename CacheT, int DK, bool FUSED = false>
+cudaError_t launch_t(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s, const StepArgs& st = StepArgs{}) {
   switch (a.Hq / a.Hkv) {
-    case 1: return launch_g<CacheT, 1, DK>(a, q_dtype, s);
-    case 2: return launch_g<CacheT, 2, DK>(a, q_dtype, s);
-    case 4: return launch_g<CacheT, 4, DK>(a, q_dtype, s);
+    case 1: return launch_g<CacheT, 1, DK, FUSED>(a, q_dtype, st, s);
+    case 2: return launch_g<CacheT, 2, DK, FUSED>(a, q_dtype, st, s);
+    case 4: return launch_g<CacheT, 4, DK, FUSED>(a, q_dtype, st, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -352,7 +481,6 @@ int decode_num_sms() {
   return n;
 }
 
-bool decode_mma_supported();
 cudaError_t launch_decode_mma(const DecodeArgs& a, kva_dtype q_dtype, cudaStream_t s);
 
 // bf16 caches: tensor-core tiles (decode_mma.cu); fp32 caches: the CUDA-core kernel above.
@@ -370,6 +498,25 @@ cudaError_t launch_decode_asym(const DecodeArgs& a, int Dk, int Dv, kva_dtype q_
   if (!decode_asym_supported(Dk, Dv)) return cudaErrorInvalidValue;
   if (cache_dtype == KVA_BF16) return launch_t<bf16_t, 192>(a, q_dtype, s);
   return launch_t<float, 192>(a, q_dtype, s);
+}
+
+bool decode_step_simt_supported(int Dk, int Dv, int G) {
+  return (G == 1 || G == 2 || G == 4) && ((Dk == D && Dv == D) || decode_asym_supported(Dk, Dv));
+}
+
+// The fused decode step on the CUDA-core kernel: fp32 caches, the asymmetric cache, and RoPE
+// over a sub-range of the head.
+cudaError_t launch_decode_step_simt(const DecodeArgs& a, const StepArgs& st, int Dk, kva_dtype cache_dtype,
+                                    cudaStream_t s) {
+  if (Dk == D) {
+    if (cache_dtype == KVA_BF16) return launch_t<bf16_t, D, true>(a, KVA_BF16, s, st);
+    return launch_t<float, D, true>(a, KVA_F32, s, st);
+  }
+  if (Dk == 192) {
+    if (cache_dtype == KVA_BF16) return launch_t<bf16_t, 192, true>(a, KVA_BF16, s, st);
+    return launch_t<float, 192, true>(a, KVA_F32, s, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kva

@@ -494,10 +494,18 @@ kva_status kv_attn_decode_step(
     return fail(KVA_EINVAL, "q and k norm weights must both be given or both be NULL");
   if (norm.q_w && (!(norm.eps >= 0.f) || norm.inst_stride < 0)) return fail(KVA_EINVAL, "bad QK-Norm eps/stride");
   const int G = n_q_heads / Hkv;
-  if (cache.dtype != KVA_BF16 || D != DECODE_HEAD_DIM || asymmetric(cache) || !decode_step_supported(G))
-    return fail(KVA_EUNSUPPORTED, "fused step needs a symmetric bf16 cache, head_dim 128, Hq/Hkv in {1,2,4}");
-  if (rope.kind != KVA_ROPE_NONE && (rope.rot_offset != 0 || (rope.rot_dim != 0 && rope.rot_dim != D)))
-    return fail(KVA_EUNSUPPORTED, "fused step rotates the whole head (no rotary sub-range)");
+  const int Dv = cache.head_dim_v;
+  int rot_off = 0, rot_w = D;
+  st = rope_range(rope, D, &rot_off, &rot_w);
+  if (st != KVA_OK) return st;
+  const bool whole_head = rope.kind == KVA_ROPE_NONE || (rot_off == 0 && rot_w == D);
+  // tensor-core form: bf16 symmetric D = 128 with whole-head RoPE; CUDA-core form: fp32 caches,
+  // the asymmetric 192/128 cache and rotary sub-ranges
+  const bool mma_form = cache.dtype == KVA_BF16 && D == DECODE_HEAD_DIM && !asymmetric(cache) &&
+                        decode_step_supported(G) && whole_head && decode_mma_supported();
+  if (!mma_form && !decode_step_simt_supported(D, Dv, G))
+    return fail(KVA_EUNSUPPORTED, "fused step: head dims %d/%d with Hq/Hkv %d (built: 128/128 and 192/128, "
+                "Hq/Hkv in {1,2,4})", D, Dv, G);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (q_out && !aligned16(q_out)))
     return fail(KVA_EALIGN, "q/k/v/out/q_out must be 16-byte aligned");
   if (norm.q_w && (!aligned16(norm.q_w) || !aligned16(norm.k_w) || (norm.inst_stride * 4) % 16 != 0))
@@ -506,8 +514,10 @@ kva_status kv_attn_decode_step(
   if (!aligned16(workspace)) return fail(KVA_EALIGN, "workspace must be 16-byte aligned");
   if (B > 65535) return fail(KVA_EUNSUPPORTED, "decode step: B > 65535");
   StepArgs sa{};
-  st = build_rope_table(rope, D, &sa.rope);
+  st = build_rope_table(rope, rot_w, &sa.rope);
   if (st != KVA_OK) return st;
+  sa.rot_offset = rot_off;
+  sa.rot_dim = rot_w;
   int max_len = 0;
   for (int b = 0; b < B; ++b) {
     const int L = lengths_host[b];
@@ -515,9 +525,11 @@ kva_status kv_attn_decode_step(
       return fail(KVA_ECAPACITY, "length %d of instance %d outside [1, %d]", L, b, cache.capacity);
     max_len = std::max(max_len, L);
   }
-  const int chunk = decode_plan_chunk(lengths_host, B, Hkv, max_len);
+  const int chunk = mma_form ? decode_plan_chunk(lengths_host, B, Hkv, max_len)
+                             : decode_plan_chunk(lengths_host, B, Hkv, max_len, (double)(D + Dv) * elem_size(cache.dtype),
+                                                 asymmetric(cache) ? 1 : 2);
   const int max_chunks = (max_len + chunk - 1) / chunk;
-  const size_t need = decode_ws_bytes(B, Hkv, n_q_heads, max_chunks, D);
+  const size_t need = decode_ws_bytes(B, Hkv, n_q_heads, max_chunks, Dv);
   if (workspace_bytes < need)
     return fail(KVA_EWORKSPACE, "decode step workspace %zu bytes < %zu needed", workspace_bytes, need);
   DecodeArgs a{};
@@ -537,7 +549,8 @@ kva_status kv_attn_decode_step(
   sa.q_w = norm.q_w; sa.k_w = norm.k_w; sa.w_stride = norm.inst_stride; sa.eps = norm.eps;
   sa.after_rope = norm.after_rope ? 1 : 0;
   sa.q_out = q_out; sa.q_out_dtype = (int)q_out_dtype;
-  cudaError_t e = launch_decode_step(a, sa, (cudaStream_t)stream);
+  cudaError_t e = mma_form ? launch_decode_step(a, sa, (cudaStream_t)stream)
+                           : launch_decode_step_simt(a, sa, D, cache.dtype, (cudaStream_t)stream);
   if (e == cudaSuccess) count_launches(1);
   return cuda_status(e, "decode step launch");
 }

@@ -137,11 +137,17 @@ struct StepArgs {
   int after_rope;
   void* q_out;            // optional [B, Hq, D] transformed queries
   int q_out_dtype;
-  RopeTable rope;
+  int rot_offset, rot_dim;  // rotated dims [rot_offset, rot_offset + rot_dim) of a q/k row
+  RopeTable rope;           // frequencies of a rot_dim-wide block
 };
 
 constexpr int DECODE_HEAD_DIM = 128;
 int decode_subtile(kva_dtype cache_dtype);   // keys per pipeline stage
+// The fused decode step on the CUDA-core kernel (fp32 caches, the 192/128 cache, rotary
+// sub-ranges); the tensor-core form is launch_decode_step.
+bool decode_step_simt_supported(int Dk, int Dv, int G);
+cudaError_t launch_decode_step_simt(const DecodeArgs& a, const StepArgs& st, int Dk, kva_dtype cache_dtype,
+                                    cudaStream_t s);
 int decode_num_sms();
 // Split-KV plan: `chunk` = target keys per CTA (instance b is cut into ceil(L_b / chunk)
 // nearly equal chunks), a multiple of 64, with at most 64 chunks per instance.
@@ -156,6 +162,7 @@ cudaError_t launch_decode_asym(const DecodeArgs& a, int Dk, int Dv, kva_dtype q_
                                cudaStream_t s);
 // Fused append + decode (bf16 cache, D = 128, G in {1, 2, 4}); false if this build cannot.
 bool decode_step_supported(int G);
+bool decode_mma_supported();
 cudaError_t launch_decode_step(const DecodeArgs& a, const StepArgs& st, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------

@@ -133,12 +133,19 @@ def test_asymmetric_cache_and_rotary_range_validation(K):
     lh = np.array([3], np.int32)
     ac = _cache(FAKE, hkv=32, d=192, dv=64, cap=64)
     assert L.kv_attn_decode(FAKE, 1, ac, FAKE, lh.ctypes.data, 1, 32, 0.0, FAKE, FAKE, 1 << 30, None) == K.KVA_EUNSUPPORTED
+    # the fused step takes the 192/128 cache and rotary sub-ranges (the CUDA-core form): validation
+    # passes, and without a GPU the launch itself is what fails
     ac = _cache(FAKE, hkv=32, d=192, dv=128, cap=64)
     assert L.kv_attn_decode_step(FAKE, FAKE, FAKE, 0, FAKE, 0, _norm(), _rope(), ac, FAKE, lh.ctypes.data, 1, 32,
+                                 0.0, None, 0, FAKE, FAKE, 1 << 30, None) in (K.KVA_OK, K.KVA_ECUDA)
+    bad = _cache(FAKE, hkv=32, d=192, dv=64, cap=64)                      # value width not built
+    assert L.kv_attn_decode_step(FAKE, FAKE, FAKE, 0, FAKE, 0, _norm(), _rope(), bad, FAKE, lh.ctypes.data, 1, 32,
                                  0.0, None, 0, FAKE, FAKE, 1 << 30, None) == K.KVA_EUNSUPPORTED
     sc = _cache(FAKE, cap=64)
     assert L.kv_attn_decode_step(FAKE, FAKE, FAKE, 0, FAKE, 0, _norm(), _rope(rot_offset=64, rot_dim=64), sc, FAKE,
-                                 lh.ctypes.data, 1, 16, 0.0, None, 0, FAKE, FAKE, 1 << 30, None) == K.KVA_EUNSUPPORTED
+                                 lh.ctypes.data, 1, 16, 0.0, None, 0, FAKE, FAKE, 1 << 30, None) in (K.KVA_OK, K.KVA_ECUDA)
+    assert L.kv_attn_decode_step(FAKE, FAKE, FAKE, 0, FAKE, 0, _norm(), _rope(rot_offset=64, rot_dim=96), sc, FAKE,
+                                 lh.ctypes.data, 1, 16, 0.0, None, 0, FAKE, FAKE, 1 << 30, None) == K.KVA_EINVAL
     assert L.kv_attn_verify(FAKE, 1, ac, FAKE, lh.ctypes.data, 1, 2, 32, 0.0, FAKE, FAKE, 1 << 30, None) == K.KVA_EUNSUPPORTED
     assert L.kv_attn_decode_static(FAKE, 1, ac, FAKE, lh.ctypes.data, 1, 32, 0.0, FAKE, None) == K.KVA_EUNSUPPORTED
     pc = _cache(FAKE, hkv=32, d=160, dv=128, cap=64)
@@ -191,7 +198,7 @@ def test_decode_step_validation(K):
     assert step([3], norm=_norm(k=FAKE)) == K.KVA_EINVAL
     assert step([3], ws=None) == K.KVA_EWORKSPACE
     assert step([3], ws_bytes=16) == K.KVA_EWORKSPACE
-    assert step([3], cache=_cache(FAKE, dtype=0, cap=64)) == K.KVA_EUNSUPPORTED   # f32 cache: two calls
+    assert step([3], cache=_cache(FAKE, dtype=0, cap=64)) in (K.KVA_OK, K.KVA_ECUDA)   # f32 cache: CUDA-core form
     assert step([3], cache=_cache(FAKE, d=64, cap=64)) == K.KVA_EUNSUPPORTED
     assert step([3], Hq=64) == K.KVA_EUNSUPPORTED                            # group size 8
     assert step([3], rope=_rope(kind=2, secs=(16, 16, 16, 8), n_axes=4)) == K.KVA_EINVAL

@@ -254,10 +254,12 @@ def test_mla_append_prefill_decode_chain(K):
     assert not np.any(kh[:, n:]) and not np.any(host(vc)[0][:, n:])
 
 
-def test_mla_benchmark_shapes_full_window(K):
+@pytest.mark.parametrize("fused", [True, False], ids=["decode_step", "append_then_decode"])
+def test_mla_benchmark_shapes_full_window(K, fused):
     """The shapes the benchmark times for the MLA-expanded cache: a 512-token prompt filling the
     512-slot window (append + causal prefill), then a token written into the last slot and
-    decoded over the whole window; sampled prompt rows and the token against the oracle."""
+    decoded over the whole window (fused: one kv_attn_decode_step launch, as the benchmark runs
+    it); sampled prompt rows and the token against the oracle."""
     torch = T()
     rng = np.random.default_rng(78)
     H, W = 32, 512
@@ -290,13 +292,21 @@ def test_mla_benchmark_shapes_full_window(K):
     p = np.array([[[W - 1]]], np.int32)
     sl = np.array([[W - 1]], np.int32)
     qo = torch.empty((1, 1, H, DK), device="cuda", dtype=torch.bfloat16)
-    K.kv_cache_append_rope_qknorm(dev(qn, torch.bfloat16), dev(kn, torch.bfloat16), dev(vn, torch.bfloat16), dev(p),
-                                  dev(sl), sl, cache, qo, rope_k)
     lens = np.array([W], np.int32)
     ws = torch.zeros(K.decode_workspace_bytes(1, H, H, W, DV), dtype=torch.uint8, device="cuda")
     o = torch.empty((1, H, DV), device="cuda")
-    K.kv_attn_decode(qo[:, 0], cache, dev(lens), lens, o, ws)
+    if fused:
+        K.kv_attn_decode_step(dev(qn[0], torch.bfloat16), dev(kn[0], torch.bfloat16), dev(vn[0], torch.bfloat16),
+                              dev(p[0]), cache, dev(lens), lens, o, ws, rope_k, q_out=qo[:, 0])
+    else:
+        K.kv_cache_append_rope_qknorm(dev(qn, torch.bfloat16), dev(kn, torch.bfloat16), dev(vn, torch.bfloat16),
+                                      dev(p), dev(sl), sl, cache, qo, rope_k)
+        K.kv_attn_decode(qo[:, 0], cache, dev(lens), lens, o, ws)
     torch.cuda.synchronize()
     kex = O.qk_transform(kn[0], p[0], None, 1e-6, rope_o, False)            # [1, H, DK]
     assert_bf16_store(bf16_bits(kc)[0][:, W - 1:W], kex.transpose(1, 0, 2), "token K row")
-    assert_fp32_close(host(o)[0], O.decode(host(qo)[0, 0], host(kc)[0], host(vc)[0], W), "token decode")
+    qex = O.qk_transform(qn[0], p[0], None, 1e-6, rope_o, False)[0]         # [H, DK], exact
+    assert_bf16_store(bf16_bits(qo)[0, 0], qex, "token q_out")
+    # the fused step attends with its fp32 query, the two calls with the stored bf16 one
+    q_used = qex if fused else host(qo)[0, 0]
+    assert_fp32_close(host(o)[0], O.decode(q_used, host(kc)[0], host(vc)[0], W), "token decode")

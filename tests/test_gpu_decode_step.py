@@ -148,3 +148,88 @@ def test_decode_step_matches_append_then_decode(K):
     kd = (kc.float() - kc2.float()).abs().max().item()
     assert kd <= 2 * 2.0 ** -8 * kc2.float().abs().max().item()    # at most an ulp apart
     assert_bf16_close(host(out_f), host(out_s), "fused vs two calls")
+
+
+SIMT_STEP_CASES = [
+    # cache dtype, Dk, Dv, Hkv, G, rope kind, sections, rot_offset, rot_dim, norm, input dtype, q_out dtype
+    ("f32", 128, 128, 2, 2, "1d", (), 0, 0, "before", "f32", "f32"),        # the tiny fp32 layer's step
+    ("f32", 128, 128, 2, 4, "sections", (16, 16, 16, 16), 0, 0, "after", "bf16", None),
+    ("f32", 128, 128, 3, 1, "2d", (), 0, 0, None, "f32", "bf16"),
+    ("bf16", 128, 128, 2, 2, "interleaved", (), 64, 64, "before", "f32", "bf16"),   # rotary sub-range
+    ("bf16", 192, 128, 4, 1, "interleaved", (), 128, 64, None, "bf16", "bf16"),     # the MLA-expanded cache
+    ("f32", 192, 128, 2, 2, "1d", (), 128, 64, "after", "f32", "f32"),
+    ("bf16", 192, 128, 2, 4, "1d", (), 0, 0, "before", "f32", None),
+]
+
+
+@pytest.mark.parametrize("c_dt,Dk,Dv,Hkv,G,kind,secs,ro,rw,norm,in_dt,qo_dt", SIMT_STEP_CASES)
+def test_decode_step_cuda_core_form(K, c_dt, Dk, Dv, Hkv, G, kind, secs, ro, rw, norm, in_dt, qo_dt):
+    """The fused step on the CUDA-core kernel (fp32 caches, the K 192 / V 128 cache, RoPE over a
+    sub-range of the head) against the oracle's append followed by its decode, with NaN canaries
+    past the valid prefix and in the new token's slot."""
+    torch = _torch()
+    rng = np.random.default_rng(zlib.crc32(repr((c_dt, Dk, Hkv, G, kind, ro, norm, in_dt)).encode()))
+    Hq = Hkv * G
+    lengths = np.array([1, 2, 33, 64, 65, 300, 1000, 1500], np.int32)
+    B, W = lengths.size, 1536
+    n_axes = {"none": 1, "1d": 1, "sections": 4, "2d": 2, "interleaved": 1}[kind]
+    base = 1.11588e7 if kind == "sections" else 1e6
+    cdt = {"f32": torch.float32, "bf16": torch.bfloat16}[c_dt]
+    idt = {"f32": torch.float32, "bf16": torch.bfloat16}[in_dt]
+    q = O.store(rng.standard_normal((B, Hq, Dk)) * 3, in_dt)
+    k = O.store(rng.standard_normal((B, Hkv, Dk)) * 3, in_dt)
+    v = O.store(rng.standard_normal((B, Hkv, Dv)), in_dt)
+    pos = rng.integers(0, 40000, size=(B, n_axes)).astype(np.int32)
+    qw = (1 + 0.1 * rng.standard_normal((B, Dk))).astype(np.float32)
+    kw = (1 + 0.1 * rng.standard_normal((B, Dk))).astype(np.float32)
+    kc0 = O.store(rng.standard_normal((B, Hkv, W, Dk)), c_dt)
+    vc0 = O.store(rng.standard_normal((B, Hkv, W, Dv)), c_dt)
+    kd = dev(kc0, cdt); vd = dev(vc0, cdt)
+    for b, L in enumerate(lengths):
+        kd[b, :, L:] = float("nan"); vd[b, :, L:] = float("inf")
+        kd[b, :, L - 1] = float("nan"); vd[b, :, L - 1] = float("nan")
+    rope = K.Rope(kind, base, secs, rot_offset=ro, rot_dim=rw)
+    ws = torch.zeros(K.decode_workspace_bytes(B, Hkv, Hq, W, Dv), dtype=torch.uint8, device="cuda")
+    q_out = None if qo_dt is None else torch.empty((B, Hq, Dk), device="cuda",
+                                                     dtype={"f32": torch.float32, "bf16": torch.bfloat16}[qo_dt])
+    cache = K.KVCache(kd, vd)
+    outs = []
+    for rep in range(2):                     # the second call rewrites the same slot and reuses the workspace
+        out = torch.full((B, Hq, Dv), float("nan"), device="cuda")
+        K.kv_attn_decode_step(dev(q, idt), dev(k, idt), dev(v, idt), dev(pos), cache, dev(lengths), lengths, out, ws,
+                              rope, q_norm_w=dev(qw) if norm else None, k_norm_w=dev(kw) if norm else None, eps=1e-6,
+                              norm_after_rope=(norm == "after"), norm_inst_stride=Dk, q_out=q_out)
+        torch.cuda.synchronize()
+        outs.append(host(out))
+    np.testing.assert_array_equal(outs[0], outs[1])
+    got = outs[0]
+    assert np.all(np.isfinite(got))
+    orope = O.Rope(kind, base, secs if secs else None, rot_offset=ro, rot_dim=rw if rw else None)
+    kh, vh = host(kd), host(vd)
+    for b, L in enumerate(lengths):
+        L = int(L)
+        ck = kc0[b].copy(); cv = vc0[b].copy()
+        wq = qw[b] if norm else None
+        wk = kw[b] if norm else None
+        qr = O.cache_append(q[b][None], k[b][None], v[b][None], pos[b][None], np.array([L - 1]), wq, wk, 1e-6,
+                            orope, norm == "after", ck, cv, c_dt)[0]
+        kr = O.qk_transform(k[b][None], pos[b][None], wk, 1e-6, orope, norm == "after")[0]
+        if c_dt == "bf16":
+            assert_bf16_store(bf16_bits(kd[b])[:, L - 1], kr, f"k slot b={b}")
+        else:
+            assert_fp32_close(kh[b][:, L - 1], kr, f"k slot b={b}")
+        np.testing.assert_array_equal(vh[b][:, L - 1], cv[:, L - 1])          # v stored exactly
+        other = np.ones(W, bool); other[L - 1] = False
+        assert not np.any(np.isfinite(kh[b][:, L:])) and not np.any(np.isfinite(vh[b][:, L:]))   # canaries kept
+        # attention over the prefix with the row the kernel wrote; the query is the exact transform
+        ck[:, L - 1] = kh[b][:, L - 1]
+        ref = O.decode(qr, ck, cv, L)
+        if c_dt == "f32":
+            assert_fp32_close(got[b], ref, f"step b={b} L={L}")
+        else:
+            assert_bf16_close(got[b], ref, f"step b={b} L={L}")
+        if q_out is not None:
+            if qo_dt == "f32":
+                assert_fp32_close(host(q_out[b]), qr, "q_out")
+            else:
+                assert_bf16_store(bf16_bits(q_out[b]), qr, "q_out")

@@ -42,7 +42,10 @@ def _argmax_check(got_ids, z_cols, what):
 # ----------------------------------------------------------------------------
 # 1. tiny fp32 single layer: prefill 64, 16 decode steps
 # ----------------------------------------------------------------------------
-def test_tiny_fp32_prefill_decode(K):
+@pytest.mark.parametrize("fused", [True, False], ids=["decode_step", "append_then_decode"])
+def test_tiny_fp32_prefill_decode(K, fused):
+    """fused: each decode step is one kv_attn_decode_step launch (the CUDA-core form on the fp32
+    cache), as the benchmark times it; otherwise an append and a decode."""
     torch = T()
     w = WL.tiny_fp32(0)
     Hq, Hkv, D, W = 16, 8, 128, w["capacity"]
@@ -63,12 +66,17 @@ def test_tiny_fp32_prefill_decode(K):
     for t in range(P, W):
         qd = torch.empty((1, 1, Hq, D), device="cuda")
         s = np.array([[t]], np.int32)
-        K.kv_cache_append_rope_qknorm(dev(w["q"][None, t:t + 1]), dev(w["k"][None, t:t + 1]),
-                                      dev(w["v"][None, t:t + 1]), dev(w["pos"][None, t:t + 1]), dev(s), s,
-                                      cache, qd, rope, q_norm_w=qw, k_norm_w=kw, eps=w["eps"])
         o = torch.empty((1, Hq, D), device="cuda")
         L = np.array([t + 1], np.int32)
-        K.kv_attn_decode(qd[:, 0], cache, dev(L), L, o, ws)
+        if fused:
+            K.kv_attn_decode_step(dev(w["q"][t:t + 1]), dev(w["k"][t:t + 1]), dev(w["v"][t:t + 1]),
+                                  dev(w["pos"][t:t + 1]), cache, dev(L), L, o, ws, rope, q_norm_w=qw, k_norm_w=kw,
+                                  eps=w["eps"])
+        else:
+            K.kv_cache_append_rope_qknorm(dev(w["q"][None, t:t + 1]), dev(w["k"][None, t:t + 1]),
+                                          dev(w["v"][None, t:t + 1]), dev(w["pos"][None, t:t + 1]), dev(s), s,
+                                          cache, qd, rope, q_norm_w=qw, k_norm_w=kw, eps=w["eps"])
+            K.kv_attn_decode(qd[:, 0], cache, dev(L), L, o, ws)
         dec.append(o)
     torch.cuda.synchronize()
 
