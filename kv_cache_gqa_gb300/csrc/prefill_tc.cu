@@ -3,8 +3,9 @@
 //
 // Work unit: two 128-row query tiles ("slots") that read the same KV head: the two query
 // heads of a GQA group at the same rows when the group size is even (each K/V tile is loaded
-// once for both), otherwise two row tiles of one head paired so that causal work is balanced
-// (tiles t and n-1-t).  One CTA per SM walks units b, 2P-1-b, 2P+b, ... (a snake over the P
+// once for both), otherwise two row tiles of one head: tiles t and n-1-t so that causal work is
+// balanced, or neighbouring tiles 2t and 2t+1 under a window mask (their key ranges overlap,
+// where t and n-1-t would see disjoint windows one after the other).  One CTA per SM walks units b, 2P-1-b, 2P+b, ... (a snake over the P
 // CTAs, which evens out the causal cost), so a unit's epilogue overlaps the next unit's Q load
 // and first Q K^T.
 //
@@ -191,7 +192,11 @@ __device__ __forceinline__ Slots unit_slots(const PrefillArgs& a, const Units& g
   } else if ((a.Hq / a.Hkv) % 2 == 0) {   // the two heads of a pair, heaviest row tiles first
     sl.h[0] = 2 * x; sl.h[1] = 2 * x + 1;
     sl.qt[0] = sl.qt[1] = nq - 1 - z;
-  } else {                         // row tiles z and nq-1-z of one head
+  } else if (a.mask == KVA_MASK_SEGMENT) {   // row tiles 2z and 2z+1 of one head: their windows
+    sl.h[0] = sl.h[1] = x;                    // overlap, so the two slots share key tiles
+    sl.qt[0] = 2 * z;
+    sl.qt[1] = 2 * z + 1 < nq ? 2 * z + 1 : -1;
+  } else {                         // row tiles z and nq-1-z of one head (balanced causal work)
     sl.h[0] = sl.h[1] = x;
     sl.qt[0] = z;
     sl.qt[1] = nq - 1 - z;
