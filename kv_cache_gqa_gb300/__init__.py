@@ -15,4 +15,5 @@ from .kv_attn import (KVCache, KvaError, Rope, decode_workspace_bytes, kv_attn_d
                       kv_attn_decode_step, kv_attn_verify, kv_verify_commit, verify_workspace_bytes,
                       kv_attn_prefill, kv_cache_append_rope_qknorm, launch_count, lib,
                       lmhead_argmax, lmhead_topk, lmhead_topk_workspace_bytes, lmhead_workspace_bytes,
-                      version, wait_timeouts, workspace_bytes)
+                      version, wait_timeouts, workspace_bytes, PreparedCall, prepare_decode_step,
+                      prepare_lmhead_argmax)

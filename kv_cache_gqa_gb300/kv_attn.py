@@ -309,23 +309,52 @@ def _norm_struct(q_norm_w, k_norm_w, inst_stride, eps, after):
     return st
 
 
-def kv_attn_decode_step(q, k, v, pos, cache: KVCache, lengths, lengths_host, out, workspace, rope: Rope,
+class PreparedCall:
+    """One C-ABI call whose arguments were marshalled once.  Calling it calls the entry point
+    again: the library validates, plans and launches every time; only the Python-side conversion
+    of tensors into pointers and descriptors is skipped.  The tensors and host arrays it was made
+    from must stay alive and keep their storage (their contents may change between calls, which
+    is how a decode loop advances its lengths), and the stream is the one current (or given)
+    when it was made."""
+    __slots__ = ("_fn", "_args", "_keep")
+
+    def __init__(self, fn, args, keep):
+        self._fn, self._args, self._keep = fn, args, keep
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != KVA_OK:
+            raise KvaError(st, lib().kva_last_error().decode())
+
+
+def prepare_decode_step(q, k, v, pos, cache: KVCache, lengths, lengths_host, out, workspace, rope: Rope,
                         q_norm_w=None, k_norm_w=None, eps: float = 1e-6, norm_after_rope: bool = False,
                         norm_inst_stride: int = 0, pos_inst_stride: Optional[int] = None, q_out=None,
-                        scale: float = 0.0, stream=None):
-    """Fused append + decode of one new token per instance.  q [B,Hq,D], k/v [B,Hkv,D] raw
-    projections (CUDA f32|bf16); pos [B|1, n_axes] int32 CUDA; lengths [B] int32 CUDA (valid
-    slots incl. the new token, which is written to slot L-1) + host mirror; out [B,Hq,D] f32."""
+                        scale: float = 0.0, stream=None) -> PreparedCall:
+    """kv_attn_decode_step with its arguments marshalled once (see PreparedCall)."""
     B, Hq, _ = q.shape
     if pos_inst_stride is None:
         pos_inst_stride = 0 if (pos is None or pos.dim() < 2 or pos.shape[0] == 1) else pos.shape[-1]
     lh = _host_i32(lengths_host)
     norm = _norm_struct(q_norm_w, k_norm_w, norm_inst_stride, eps, 1 if norm_after_rope else 0)
-    _check(lib().kv_attn_decode_step(
-        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(pos), pos_inst_stride, norm, rope.struct, cache.struct,
-        _ptr(lengths), lh.ctypes.data, B, Hq, float(scale), _ptr(q_out),
-        _dtype_code(q_out) if q_out is not None else 0, _ptr(out), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+    args = (_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(pos), pos_inst_stride, norm, rope.struct,
+            cache.struct, _ptr(lengths), lh.ctypes.data, B, Hq, float(scale), _ptr(q_out),
+            _dtype_code(q_out) if q_out is not None else 0, _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    return PreparedCall(lib().kv_attn_decode_step, args, (lh, cache, rope))
+
+
+def kv_attn_decode_step(q, k, v, pos, cache: KVCache, lengths, lengths_host, out, workspace, rope: Rope,
+                        q_norm_w=None, k_norm_w=None, eps: float = 1e-6, norm_after_rope: bool = False,
+                        norm_inst_stride: int = 0, pos_inst_stride: Optional[int] = None, q_out=None,
+                        scale: float = 0.0, stream=None):
+    """Fused append + decode of one new token per instance.  q [B,Hq,Dk], k [B,Hkv,Dk], v [B,Hkv,Dv]
+    raw projections (CUDA f32|bf16); pos [B|1, n_axes] int32 CUDA; lengths [B] int32 CUDA (valid
+    slots incl. the new token, which is written to slot L-1) + host mirror; out [B,Hq,Dv] f32."""
+    prepare_decode_step(q, k, v, pos, cache, lengths, lengths_host, out, workspace, rope, q_norm_w=q_norm_w,
+                        k_norm_w=k_norm_w, eps=eps, norm_after_rope=norm_after_rope,
+                        norm_inst_stride=norm_inst_stride, pos_inst_stride=pos_inst_stride, q_out=q_out,
+                        scale=scale, stream=stream)()
 
 
 def verify_workspace_bytes(B: int, n_kv_heads: int, n_q_heads: int, k: int, max_len: int, head_dim: int) -> int:
@@ -366,15 +395,21 @@ def lmhead_topk(h, W, out_ids, workspace, norm_w=None, eps: float = 1e-6, V=None
                              _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def lmhead_argmax(h, W, out_ids, workspace, V: Optional[int] = None, out_max=None, logits=None,
-                  stream=None):
-    """h [B,H] float32 CUDA; W [V_rows,H] bf16|f32 CUDA; out_ids [B] int32 CUDA."""
+def prepare_lmhead_argmax(h, W, out_ids, workspace, V: Optional[int] = None, out_max=None, logits=None,
+                          stream=None) -> PreparedCall:
+    """lmhead_argmax with its arguments marshalled once (see PreparedCall)."""
     B, H = h.shape
     V_rows = W.shape[0]
     V = V_rows if V is None else V
-    _check(lib().lmhead_argmax(
-        _ptr(h), _ptr(W), _dtype_code(W), B, H, V, V_rows, _ptr(out_ids), _ptr(out_max),
-        _ptr(logits), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    args = (_ptr(h), _ptr(W), _dtype_code(W), B, H, V, V_rows, _ptr(out_ids), _ptr(out_max), _ptr(logits),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return PreparedCall(lib().lmhead_argmax, args, ())
+
+
+def lmhead_argmax(h, W, out_ids, workspace, V: Optional[int] = None, out_max=None, logits=None,
+                  stream=None):
+    """h [B,H] float32 CUDA; W [V_rows,H] bf16|f32 CUDA; out_ids [B] int32 CUDA."""
+    prepare_lmhead_argmax(h, W, out_ids, workspace, V=V, out_max=out_max, logits=logits, stream=stream)()
 
 
 def launch_count() -> int:

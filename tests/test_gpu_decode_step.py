@@ -233,3 +233,33 @@ def test_decode_step_cuda_core_form(K, c_dt, Dk, Dv, Hkv, G, kind, secs, ro, rw,
                 assert_fp32_close(host(q_out[b]), qr, "q_out")
             else:
                 assert_bf16_store(bf16_bits(q_out[b]), qr, "q_out")
+
+
+def test_prepared_call_matches_direct_call_and_follows_updated_lengths(K):
+    """A PreparedCall marshals the arguments once; calling it again after the lengths (device
+    array and host mirror) are updated in place runs the next step, as a direct call would."""
+    torch = _torch()
+    rng = np.random.default_rng(77)
+    B, Hkv, G, D, W = 3, 2, 2, 128, 600
+    Hq = Hkv * G
+    kc = torch.randn((B, Hkv, W, D), device="cuda").to(torch.bfloat16); vc = torch.randn_like(kc)
+    kc2, vc2 = kc.clone(), vc.clone()
+    q = dev(rng.standard_normal((B, Hq, D)).astype(np.float32))
+    k = dev(rng.standard_normal((B, Hkv, D)).astype(np.float32))
+    v = dev(rng.standard_normal((B, Hkv, D)).astype(np.float32))
+    pos = dev(np.array([[100], [200], [300]], np.int32))
+    rope = K.Rope("1d", 1e6)
+    ws = torch.zeros(K.decode_workspace_bytes(B, Hkv, Hq, W, D), dtype=torch.uint8, device="cuda")
+    ws2 = torch.zeros_like(ws)
+    lh = np.array([10, 300, 555], np.int32)
+    ld = dev(lh)
+    out_p = torch.empty((B, Hq, D), device="cuda")
+    call = K.prepare_decode_step(q, k, v, pos, K.KVCache(kc, vc), ld, lh, out_p, ws, rope)
+    for step in range(2):
+        call()
+        out_d = torch.empty((B, Hq, D), device="cuda")
+        K.kv_attn_decode_step(q, k, v, pos, K.KVCache(kc2, vc2), ld, lh, out_d, ws2, rope)
+        torch.cuda.synchronize()
+        assert torch.equal(out_p, out_d) and torch.equal(kc, kc2) and torch.equal(vc, vc2), step
+        lh += 1                                    # the next step: both mirrors advance in place
+        ld += 1
