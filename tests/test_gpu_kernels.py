@@ -427,3 +427,28 @@ def test_lmhead_ties_lowest_id_last_row_and_clamp(K):
                 K.lmhead_argmax(dev(hz), Wd, ids, ws, V=Vrows)
                 torch.cuda.synchronize()
                 assert np.all(ids.cpu().numpy() == lo_row), (Wd.dtype, B, lo_val, ids.cpu().numpy())
+
+
+@pytest.mark.parametrize("mask", ["causal", "full"])
+def test_prefill_bf16_long_prompt_sampled_rows(K, mask):
+    """A 4096-token prompt (32 row tiles, 32 key tiles per row tile under the full mask), two
+    instances, 16/8 heads: every head of sampled rows against the oracle."""
+    torch = T()
+    N, S, Hkv, G, D = 2, 4096, 8, 2, 128
+    Hq = Hkv * G
+    g = torch.Generator(device="cuda"); g.manual_seed(4096 + len(mask))
+    kc = torch.randn((N, Hkv, S, D), device="cuda", generator=g).to(torch.bfloat16)
+    vc = torch.randn_like(kc)
+    q = torch.randn((N, S, Hq, D), device="cuda", generator=g).to(torch.bfloat16)
+    out = torch.full((N, S, Hq, D), float("nan"), device="cuda")
+    K.kv_attn_prefill(q, K.KVCache(kc, vc), out, mask=mask)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    rows = np.array([0, 1, 127, 128, 1000, 2047, 2048, 3071, 4094, 4095])
+    for n in range(N):
+        kh, vh = host(kc[n]), host(vc[n])
+        allowed = np.zeros((rows.size, S), bool)
+        for i, r in enumerate(rows):
+            allowed[i, :(r + 1 if mask == "causal" else S)] = True
+        ref = O.attend(host(q[n])[rows], kh, vh, allowed)
+        assert_bf16_close(host(out[n])[rows], ref, f"long prompt n={n} {mask}")
