@@ -38,6 +38,9 @@ LAYERS, PROMPT, STEPS, WINDOW = 28, 512, 256, 1024
 HQ, HKV, D, HIDDEN, VOCAB = 16, 8, 128, 1024, 151936
 TOKENS_PER_JOB = STEPS + 1          # one greedy token after prefill + one per decode step
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The part's nominal figures (HBM3e bandwidth, dense bf16 tensor rate), quoted beside the
+# measured ones: every fraction is reported against both.
+NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
 
 # ----------------------------------------------------------------------------
@@ -672,6 +675,24 @@ def run_only(args, torch, K):
         torch.cuda.synchronize()
         ms = graph_avg_ms(torch, stream, lambda: K.lmhead_argmax(h, W, ids, lws), 8, reps=2)
         res = {"lm_head_b64_us": round(ms * 1e3, 2), "GB/s": round(VOCAB * HIDDEN * 2 / (ms / 1e3) / 1e9, 1)}
+    elif args.only == "configs":                     # tiny fp32, image span and vision workloads
+        peaks, _ = load_peaks()
+        res = configs_bench(torch, K, stream, float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+                            float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
+    elif args.only == "topk":                        # final RMSNorm + lm_head, top 1 and top 8, batch 1
+        g = torch.Generator(device="cuda"); g.manual_seed(3)
+        W = (torch.randn((VOCAB, HIDDEN), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        h = torch.randn((1, HIDDEN), device="cuda", generator=g)
+        fn_w = 1 + 0.1 * torch.randn(HIDDEN, device="cuda", generator=g)
+        ws = torch.zeros(K.lmhead_topk_workspace_bytes(1, HIDDEN, VOCAB, 8), dtype=torch.uint8, device="cuda")
+        ids1 = torch.empty((1, 1), dtype=torch.int32, device="cuda")
+        ids8 = torch.empty((1, 8), dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(stream):
+            K.lmhead_topk(h, W, ids8, ws, norm_w=fn_w)   # configures the kernels before capture
+        torch.cuda.synchronize()
+        ms1 = graph_avg_ms(torch, stream, lambda: K.lmhead_topk(h, W, ids1, ws, norm_w=fn_w), 8, reps=2)
+        ms8 = graph_avg_ms(torch, stream, lambda: K.lmhead_topk(h, W, ids8, ws, norm_w=fn_w), 8, reps=2)
+        res = {"top1_us": round(ms1 * 1e3, 2), "top8_us": round(ms8 * 1e3, 2)}
     else:                                            # serving16: the first 16 sequences of the draw
         g = torch.Generator(device="cuda"); g.manual_seed(3)
         W = (torch.randn((VOCAB, HIDDEN), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
@@ -957,6 +978,21 @@ def run_gpu(args, rank, world, local_rank):
                 "lm_head_final_norm_top8_us": round(lm_top8_ms * 1e3, 2),
                 "time_share": {k: round(v / sum(totals.values()), 4) for k, v in totals.items()},
                 "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": peak_src},
+                "frac_of_nominal": {
+                    "peaks": NOMINAL_PEAKS,
+                    "lm_head": round(lm_gbs / NOMINAL_PEAKS["hbm_gbs"], 4),
+                    "decode_step": round(dec_gbs / NOMINAL_PEAKS["hbm_gbs"], 4),
+                    "append_prefill_alone": round(append_bytes(LAYERS * PROMPT) / (app_iso_ms / 1e3) / 1e9
+                                                  / NOMINAL_PEAKS["hbm_gbs"], 4),
+                    "prefill_alone": round(prefill_flops() / (pre_iso_ms / 1e3) / 1e12
+                                           / NOMINAL_PEAKS["bf16_tflops"], 4),
+                    "prefill_in_job": round(pre_tf / NOMINAL_PEAKS["bf16_tflops"], 4),
+                    "serving_decode": round(sv["decode_GB/s"] / NOMINAL_PEAKS["hbm_gbs"], 4),
+                    "serving_lm_head": round(sv["lm_head_GB/s"] / NOMINAL_PEAKS["hbm_gbs"], 4),
+                    "verify_block": round(vb["GB/s"] / NOMINAL_PEAKS["hbm_gbs"], 4),
+                    "mla_decode_16x4096": round(mla["decode_16x4096_GB/s"] / NOMINAL_PEAKS["hbm_gbs"], 4),
+                    "vision_bf16_full": round(cfg["vision"]["bf16"]["full_TFLOP/s"] / NOMINAL_PEAKS["bf16_tflops"], 4),
+                    "image_span_prefill": round(cfg["image_span"]["prefill_TFLOP/s"] / NOMINAL_PEAKS["bf16_tflops"], 4)},
                 "timing": ("lm_head: graph of 32 back-to-back launches; prefill, append: " + kt_source +
                            "; decode step: graph of the job's 256 decode launches over 4 rotating cache copies; "
                            "verify block: graph of 8 back-to-back launches (outside the job)"),
@@ -1139,18 +1175,62 @@ def oracle_job_samples(target_s=None, n=None, warmup=0):
     return wall, jobs, sample
 
 
+def oracle_serving_step_sample(n_seq=2, lm_rows=8192):
+    """One step of the 64-sequence serving workload on the oracle, sampled: the append and
+    decode of n_seq of the 64 sequences (evenly spaced, each at its own context) and the
+    lm_head of one hidden row over lm_rows vocab rows.  The attention part is scaled by the
+    keys read (all 64 sequences' lengths over the sample's), the lm_head part by rows x vocab
+    (64 x 151936 over 1 x lm_rows).  Returns the extrapolated seconds of one step and the
+    sample's description."""
+    import oracle as O
+    import workloads as WL
+    ctx = WL.serving_contexts(0)
+    B = ctx.size
+    qw, kw = WL.serving_norm_weights(0)
+    inp = WL.serving_step_inputs(0, 0, batch=B)
+    rope = O.Rope("1d", 1e6)
+    picks = [i * (B // n_seq) for i in range(n_seq)]
+    t_att = 0.0
+    for b in picks:
+        c = int(ctx[b])
+        kb, vb = WL.serving_prefix(0, b, c)
+        ck = np.zeros((HKV, c + 128, D)); cv = np.zeros((HKV, c + 128, D))
+        ck[:, :c] = WL.bf16_bits_to_f32(kb); cv[:, :c] = WL.bf16_bits_to_f32(vb)
+        t0 = time.perf_counter()
+        qd = O.cache_append(inp["q"][b:b + 1], inp["k"][b:b + 1], inp["v"][b:b + 1], [[c]], [c], qw, kw, 1e-6,
+                            rope, False, ck, cv, "bf16")
+        O.decode(qd[0], ck, cv, c + 1)
+        t_att += time.perf_counter() - t0
+    keys_all = float(np.sum(ctx.astype(np.int64) + 1))
+    keys_pick = float(sum(int(ctx[b]) + 1 for b in picks))
+    rng = np.random.default_rng(5)
+    W = WL.f32_to_bf16_bits((0.02 * rng.standard_normal((lm_rows, HIDDEN))).astype(np.float32))
+    t0 = time.perf_counter()
+    O.lmhead_argmax(inp["h"][0], W, lm_rows)
+    t_lm = time.perf_counter() - t0
+    step_s = t_att * keys_all / keys_pick + t_lm * B * VOCAB / lm_rows
+    sample = (f"append + decode of sequences {picks} (contexts {[int(ctx[b]) for b in picks]}) scaled by keys "
+              f"read to all {B}; lm_head of 1 hidden row over {lm_rows} of {VOCAB} vocab rows scaled to {B} rows "
+              f"x {VOCAB}")
+    return step_s, sample
+
+
 def cpu_baseline(target_s=12.0):
     """Oracle (single thread, float64) on repeated bounded samples of the job for ~target_s
-    seconds, plus the small workloads timed in full."""
+    seconds, the small workloads timed in full, and one sampled step of the serving workload
+    (extrapolated)."""
     t_start = time.perf_counter()
     wall, jobs, sample = oracle_job_samples(target_s=target_s, warmup=1)
     job_s = statistics.median(jobs)
     full = oracle_full_configs()
+    serving_s, serving_sample = oracle_serving_step_sample()
     return {"value": round(TOKENS_PER_JOB / job_s, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "host": host_info(),
             "sample": f"{len(jobs)} samples of {statistics.median(wall):.2f} s each (after one warm-up sample); "
                       f"{sample}", "job_seconds_extrapolated": round(job_s, 2),
             "full_configs_seconds": full,
+            "serving_step": {"seconds_extrapolated": round(serving_s, 2),
+                             "tokens_per_s_extrapolated": round(64 / serving_s, 4), "sample": serving_sample},
             "cpu_seconds": round(time.perf_counter() - t_start, 1)}
 
 
@@ -1197,7 +1277,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--job-only", action="store_true",
                     help="time the job only and print a short line (for counter captures); not the benchmark line")
-    ap.add_argument("--only", choices=["verify", "mla", "serving16", "lm64"], default=None,
+    ap.add_argument("--only", choices=["verify", "mla", "serving16", "lm64", "configs", "topk"], default=None,
                     help="run one sub-benchmark alone and print its figures (for counter captures); "
                          "not the benchmark line")
     args = ap.parse_args(argv)
