@@ -318,6 +318,36 @@ def graph_seq_ms(torch, stream, fns, reps=4):
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
+def prefill_long_bench(torch, K, stream, bf16):
+    """The tcgen05 prefill on long prompts: 2 instances x 4096 tokens, 16/8 heads, D = 128, bf16
+    cache, causal and full masks (units of 32 key tiles, where the 512-token prompt's units hold
+    1 to 4).  Graphs of launches alternating over two buffer sets (2 x 134 MB, larger than L2).
+    Flops count visible pairs only: 4 D Hq per pair, S (S + 1) / 2 pairs per head when causal."""
+    N, S = 2, 4096
+    g = torch.Generator(device="cuda"); g.manual_seed(11)
+    sets = []
+    for _ in range(2):
+        kc = torch.randn((N, HKV, S, D), device="cuda", generator=g).to(torch.bfloat16)
+        vc = torch.randn_like(kc)
+        q = torch.randn((N, S, HQ, D), device="cuda", generator=g).to(torch.bfloat16)
+        sets.append((q, K.KVCache(kc, vc), torch.empty((N, S, HQ, D), device="cuda")))
+    res = {"config": f"{N} instances x {S} tokens, {HQ}/{HKV} heads, D={D}, bf16 cache, fp32 out",
+           "timing": "graphs of 8 launches alternating over 2 buffer sets (larger than L2)"}
+    for mask in ("causal", "full"):
+        fns = [(lambda st: (lambda: K.kv_attn_prefill(st[0], st[1], st[2], mask=mask)))(st) for st in sets]
+        with torch.cuda.stream(stream):
+            fns[0]()
+        torch.cuda.synchronize()
+        ms = graph_seq_ms(torch, stream, fns * 4, reps=4)
+        pairs = S * (S + 1) // 2 if mask == "causal" else S * S
+        flops = 4 * D * HQ * N * pairs
+        tf = flops / (ms / 1e3) / 1e12
+        res[mask] = {"us": round(ms * 1e3, 1), "flops": flops, "TFLOP/s": round(tf, 1),
+                     "frac_bf16": round(tf / bf16, 4)}
+    del sets
+    return res
+
+
 def decode_step_bench(torch, K, stream, job, copies=4):
     """kv_attn_decode_step alone as the job runs it (28 layer caches, 256 steps at L = 513..768,
     the job's inputs and per-layer norm weights), timed directly: one graph of the 256 launches,
@@ -679,6 +709,9 @@ def run_only(args, torch, K):
         peaks, _ = load_peaks()
         res = configs_bench(torch, K, stream, float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
                             float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
+    elif args.only == "prefill_long":
+        peaks, _ = load_peaks()
+        res = prefill_long_bench(torch, K, stream, float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
     elif args.only == "topk":                        # final RMSNorm + lm_head, top 1 and top 8, batch 1
         g = torch.Generator(device="cuda"); g.manual_seed(3)
         W = (torch.randn((VOCAB, HIDDEN), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
@@ -804,6 +837,7 @@ def run_gpu(args, rank, world, local_rank):
     mla = mla_bench(torch, K, stream)
     ds = decode_step_bench(torch, K, stream, job)
     peaks0, _ = load_peaks()
+    pl = prefill_long_bench(torch, K, stream, float(peaks0.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
     cfg = configs_bench(torch, K, stream, float(peaks0.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
                         float(peaks0.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
 
@@ -961,6 +995,7 @@ def run_gpu(args, rank, world, local_rank):
                                  "alone_frac_of_roofline": round(max(prefill_min_bytes() / (hbm * 1e9),
                                                                      prefill_flops() / (bf16 * 1e12))
                                                                  / (pre_iso_ms / 1e3), 4)},
+                "prefill_attn_long": pl,
                 "tiny_fp32": cfg["tiny_fp32"],
                 "image_span": cfg["image_span"],
                 "vision": cfg["vision"],
@@ -987,6 +1022,8 @@ def run_gpu(args, rank, world, local_rank):
                     "prefill_alone": round(prefill_flops() / (pre_iso_ms / 1e3) / 1e12
                                            / NOMINAL_PEAKS["bf16_tflops"], 4),
                     "prefill_in_job": round(pre_tf / NOMINAL_PEAKS["bf16_tflops"], 4),
+                    "prefill_long_causal": round(pl["causal"]["TFLOP/s"] / NOMINAL_PEAKS["bf16_tflops"], 4),
+                    "prefill_long_full": round(pl["full"]["TFLOP/s"] / NOMINAL_PEAKS["bf16_tflops"], 4),
                     "serving_decode": round(sv["decode_GB/s"] / NOMINAL_PEAKS["hbm_gbs"], 4),
                     "serving_lm_head": round(sv["lm_head_GB/s"] / NOMINAL_PEAKS["hbm_gbs"], 4),
                     "verify_block": round(vb["GB/s"] / NOMINAL_PEAKS["hbm_gbs"], 4),
@@ -1277,7 +1314,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--job-only", action="store_true",
                     help="time the job only and print a short line (for counter captures); not the benchmark line")
-    ap.add_argument("--only", choices=["verify", "mla", "serving16", "lm64", "configs", "topk"], default=None,
+    ap.add_argument("--only", choices=["verify", "mla", "serving16", "lm64", "configs", "topk", "prefill_long"],
+                    default=None,
                     help="run one sub-benchmark alone and print its figures (for counter captures); "
                          "not the benchmark line")
     args = ap.parse_args(argv)
