@@ -3,7 +3,7 @@
 // This is the path for fp32 caches (where the contract asks for 1e-5 relative error, which
 // bf16 tensor-core operands cannot give) and for head dims the tensor-core kernel does not
 // tile, including asymmetric caches (K rows Dk = 192 wide, V rows Dv = 128: an MLA layer
-// expanded per head, Youtu-VL-4B ncnn port, section 6).  One CTA per (64-query tile, query
+// expanded per head, Youtu-VL-4B ncnn port, section 6).  One CTA per (64- or 48-query tile, query
 // head, instance): Q, K and V tiles are widened
 // to fp32 in shared memory; each warp owns 8 query rows, computes their 8x64 score block
 // as a register tile, applies the mask, runs the online softmax (max -> subtract -> exp
@@ -21,11 +21,10 @@ namespace kva {
 
 namespace {
 
-constexpr int THREADS = 256;
-constexpr int WARPS = THREADS / 32;
-constexpr int BQ = 64;                 // query slots per CTA
+// A CTA of W warps owns BQ = 8 W query slots (8 rows per warp); W is 8 (64 rows) or 6 (48 rows,
+// chosen on the host when it spreads a one-wave grid more evenly over the SMs).
 constexpr int BK = 64;                 // keys per tile
-constexpr int RPW = BQ / WARPS;        // query rows per warp (8)
+constexpr int RPW = 8;                 // query rows per warp
 
 template <typename T>
 __device__ __forceinline__ void load_row_f32(const T* src, float* dst, int D, int tid0, int nthr) {
@@ -48,11 +47,12 @@ __device__ int seg_upper(const int32_t* seg, int S, int key) {
   return lo;
 }
 
-template <int D, int DV, typename T>
+template <int D, int DV, typename T, int WARPS>
 // Resident CTAs per SM: one for wide heads (shared memory); three for heads up to 80 wide (the
-// 1288-patch vision pass then fits its 336 tiles in one wave: 437 instead of 538 us), two between.
-__global__ void __launch_bounds__(THREADS, (D + DV > 256) ? 1 : (D + DV > 160 ? 2 : 3))
+// 1288-patch vision pass then fits its tiles in one wave: 437 instead of 538 us), two between.
+__global__ void __launch_bounds__(WARPS * 32, (D + DV > 256) ? 1 : (D + DV > 160 ? 2 : 3))
 prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
+  constexpr int BQ = WARPS * RPW;                    // query slots per CTA
   constexpr int DP = D + 4;                          // padded K row (conflict-free float4)
   constexpr int DPL = (DV + 31) / 32;                // output columns per lane
   extern __shared__ __align__(16) float sm[];
@@ -216,22 +216,40 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
   }
 }
 
-template <int D, int DV>
-size_t simt_smem() { return sizeof(float) * ((size_t)BQ * D + BK * (D + 4) + BK * DV + WARPS * BK * RPW); }
+template <int D, int DV, int WARPS>
+size_t simt_smem() {
+  return sizeof(float) * ((size_t)WARPS * RPW * D + BK * (D + 4) + BK * DV + WARPS * BK * RPW);
+}
 
-template <int D, int DV, typename T>
-cudaError_t launch_dt(const PrefillArgs& a, cudaStream_t s) {
-  const size_t smem = simt_smem<D, DV>();
+template <int D, int DV, typename T, int WARPS>
+cudaError_t launch_w(const PrefillArgs& a, cudaStream_t s) {
+  constexpr int BQ = WARPS * RPW;
+  const size_t smem = simt_smem<D, DV, WARPS>();
   static DeviceOnce configured;
   if (!configured.done()) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<D, DV, T>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<D, DV, T, WARPS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured.mark();
   }
   dim3 grid((a.S + BQ - 1) / BQ, a.Hq, a.N);
-  prefill_simt_kernel<D, DV, T><<<grid, THREADS, smem, s>>>(a);
+  prefill_simt_kernel<D, DV, T, WARPS><<<grid, WARPS * 32, smem, s>>>(a);
   return cudaGetLastError();
+}
+
+// 48-row CTAs when they lower the rows the busiest SM carries by at least 5% (the 1288-patch
+// vision pass: 336 CTAs of 64 rows put 192 rows on some SMs, 432 of 48 rows at most 144; full
+// pass 437 -> 389 us), else 64-row CTAs (more warps per CTA, one K/V tile load per 64 rows).
+int simt_warps(const PrefillArgs& a) {
+  const long long heads = (long long)a.Hq * a.N, sms = decode_num_sms();   // the device's SM count
+  const long long rows64 = ((heads * ((a.S + 63) / 64) + sms - 1) / sms) * 64;
+  const long long rows48 = ((heads * ((a.S + 47) / 48) + sms - 1) / sms) * 48;
+  return rows48 * 100 < rows64 * 95 ? 6 : 8;
+}
+
+template <int D, int DV, typename T>
+cudaError_t launch_dt(const PrefillArgs& a, cudaStream_t s) {
+  return simt_warps(a) == 6 ? launch_w<D, DV, T, 6>(a, s) : launch_w<D, DV, T, 8>(a, s);
 }
 
 template <int D, int DV>

@@ -230,6 +230,14 @@ def test_prefill_f32_ragged(K, S, mask):
     _prefill_case(K, 128, S, mask, "f32", 2, seed=S * 7 + len(mask))
 
 
+@pytest.mark.parametrize("mask", ["causal", "segment"])
+def test_prefill_f32_wide_grid(K, mask):
+    """Enough (instance, head, row tile) work that the fp32 kernel keeps 64-row CTAs (the small
+    cases above run 48-row CTAs, which spread a one-wave grid more evenly): 16 instances x 16
+    heads x 256 tokens."""
+    _prefill_case(K, 128, 256, mask, "f32", 2, seed=256 + len(mask), N=16, Hkv=8)
+
+
 @pytest.mark.parametrize("S", [1, 5, 64, 127, 128, 129, 255, 300])
 @pytest.mark.parametrize("mask", ["causal", "full", "segment"])
 def test_prefill_bf16_ragged(K, S, mask):
