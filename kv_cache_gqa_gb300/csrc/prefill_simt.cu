@@ -54,7 +54,12 @@ __global__ void __launch_bounds__(WARPS * 32, (D + DV > 256) ? 1 : (D + DV > 160
 prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
   constexpr int BQ = WARPS * RPW;                    // query slots per CTA
   constexpr int DP = D + 4;                          // padded K row (conflict-free float4)
-  constexpr int DPL = (DV + 31) / 32;                // output columns per lane
+  constexpr int DPL = (DV + 31) / 32;                // output column groups per lane
+  // Value widths of 32 k + 8 (72): each lane owns k full column groups for all 8 rows of its
+  // warp and two outputs of the 8-column tail (rows tr0 and tr0 + 1, column 32 k + lane % 8),
+  // instead of a (k+1)-th group that only 8 lanes use.
+  constexpr bool TAIL8 = (DV % 32 == 8);
+  constexpr int NC = TAIL8 ? DV / 32 : DPL;          // column groups per lane
   extern __shared__ __align__(16) float sm[];
   float* sQ = sm;                                    // [BQ][D]
   float* sK = sQ + BQ * D;                           // [BK][DP]
@@ -101,12 +106,14 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
   __syncthreads();
   const int k_lo = s_range[0], k_hi = s_range[1];
 
-  float m_run[RPW], l_run[RPW], acc[RPW][DPL];
+  float m_run[RPW], l_run[RPW], acc[RPW][NC];
+  float acc_t[2] = {0.f, 0.f};              // the tail outputs (TAIL8 only)
+  const int tr0 = 2 * (lane >> 3);          // the tail rows of this lane: tr0, tr0 + 1
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
     m_run[r] = -INFINITY; l_run[r] = 0.f;
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) acc[r][c] = 0.f;
+    for (int c = 0; c < NC; ++c) acc[r][c] = 0.f;
   }
   const int rbase = warp * RPW;            // this warp's first query row in the tile
   float* myP = sP + warp * BK * RPW;
@@ -176,7 +183,8 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
       l_run[r] = l_run[r] * alpha + sum;
       m_run[r] = m_new;
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) acc[r][c] *= alpha;
+      for (int c = 0; c < NC; ++c) acc[r][c] *= alpha;
+      if (TAIL8 && (r >> 1) == (lane >> 3)) acc_t[r & 1] *= alpha;
     }
     __syncwarp();
 
@@ -189,11 +197,17 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
         p[r] = pv.x; p[r + 1] = pv.y; p[r + 2] = pv.z; p[r + 3] = pv.w;
       }
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) {
+      for (int c = 0; c < NC; ++c) {
         const int d = lane + 32 * c;
-        const float v = (d < DV) ? sV[j * DV + d] : 0.f;
+        const float v = (TAIL8 || d < DV) ? sV[j * DV + d] : 0.f;
 #pragma unroll
         for (int r = 0; r < RPW; ++r) acc[r][c] = fmaf(p[r], v, acc[r][c]);
+      }
+      if (TAIL8) {
+        const float2 pt = *reinterpret_cast<const float2*>(myP + j * RPW + tr0);
+        const float vt = sV[j * DV + 32 * NC + (lane & 7)];
+        acc_t[0] = fmaf(pt.x, vt, acc_t[0]);
+        acc_t[1] = fmaf(pt.y, vt, acc_t[1]);
       }
     }
     __syncwarp();
@@ -209,10 +223,11 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
     float* o = a.out + (((int64_t)n * a.S + row) * a.Hq + h) * DV;
     const float inv = 1.0f / l_run[r];
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) {
+    for (int c = 0; c < NC; ++c) {
       const int d = lane + 32 * c;
-      if (d < DV) o[d] = acc[r][c] * inv;
+      if (TAIL8 || d < DV) o[d] = acc[r][c] * inv;
     }
+    if (TAIL8 && (r >> 1) == (lane >> 3)) o[32 * NC + (lane & 7)] = acc_t[r & 1] * inv;
   }
 }
 
