@@ -10,7 +10,8 @@
 //  - Any head width that is a multiple of 8 up to 256.
 //
 // One CTA per (token t, instance n, row group), one warp per row; short appends (a decode
-// token) split a token's rows over several CTAs so that its row loads run in parallel.  Each
+// token) split a token's rows over several CTAs so that its row loads run in parallel, and a
+// warp loads four of its rows before transforming them (long appends).  Each
 // CTA evaluates the token's rot_dim/2 angles once into shared memory.  A lane holds 8 consecutive elements of its row in
 // registers (a 16- or 32-byte access); the row is mirrored into a per-warp shared buffer so
 // that each element can read its rotation partner wherever it sits (rotate-half partner,
@@ -33,6 +34,7 @@ namespace {
 constexpr int GEN_THREADS = 256;
 constexpr int GEN_WARPS = GEN_THREADS / 32;
 constexpr int GEN_MAX_D = 256;   // 32 lanes x 8 elements
+constexpr int RB = 4;            // rows a warp loads before transforming them
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -41,7 +43,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 template <typename InT, typename QOutT, typename CacheT>
-__global__ void __launch_bounds__(GEN_THREADS)
+__global__ void __launch_bounds__(GEN_THREADS, 4)
 append_general_kernel(const __grid_constant__ AppendArgs a) {
   __shared__ float s_cos[MAX_ROPE_FREQ];
   __shared__ float s_sin[MAX_ROPE_FREQ];
@@ -69,20 +71,36 @@ append_general_kernel(const __grid_constant__ AppendArgs a) {
 
   float* rowbuf = s_row[warp];
   const int e0 = lane * 8;
-  for (int r = blockIdx.z * GEN_WARPS + warp; r < n_rows; r += GEN_WARPS * gridDim.z) {
-    const int kind = r < a.Hq ? 0 : (r < a.Hq + a.Hkv ? 1 : 2);     // q, k, v (warp-uniform)
+  // A warp takes RB rows per pass and issues all their loads before transforming any of them:
+  // with one row at a time a warp had a single 16-byte load per lane in flight, too few bytes
+  // per SM for HBM when a token's rows all sit in one CTA (long appends).
+  const int stride = GEN_WARPS * gridDim.z;
+  for (int r0 = blockIdx.z * GEN_WARPS + warp; r0 < n_rows; r0 += RB * stride) {
+    float xs[RB][8];
+#pragma unroll
+    for (int k = 0; k < RB; ++k) {
+      const int r = r0 + k * stride;
+      const int kind = r < a.Hq ? 0 : (r < a.Hq + a.Hkv ? 1 : 2);     // q, k, v (warp-uniform)
+      const int head = kind == 0 ? r : (kind == 1 ? r - a.Hq : r - a.Hq - a.Hkv);
+      const int width = kind == 2 ? Dv : Dk;
+      if (r < n_rows && e0 < width) {
+        if (kind == 0) load8(reinterpret_cast<const InT*>(a.q) + (tok * a.Hq + head) * Dk + e0, xs[k]);
+        else if (kind == 1) load8(reinterpret_cast<const InT*>(a.k) + (tok * a.Hkv + head) * Dk + e0, xs[k]);
+        else load8(reinterpret_cast<const InT*>(a.v) + (tok * a.Hkv + head) * Dv + e0, xs[k]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xs[k][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < RB; ++k) {
+    const int r = r0 + k * stride;
+    if (r >= n_rows) break;                     // warp-uniform
+    const int kind = r < a.Hq ? 0 : (r < a.Hq + a.Hkv ? 1 : 2);
     const int head = kind == 0 ? r : (kind == 1 ? r - a.Hq : r - a.Hq - a.Hkv);
     const int width = kind == 2 ? Dv : Dk;
     const bool on = e0 < width;
-    float x[8];
-    if (on) {
-      if (kind == 0) load8(reinterpret_cast<const InT*>(a.q) + (tok * a.Hq + head) * Dk + e0, x);
-      else if (kind == 1) load8(reinterpret_cast<const InT*>(a.k) + (tok * a.Hkv + head) * Dk + e0, x);
-      else load8(reinterpret_cast<const InT*>(a.v) + (tok * a.Hkv + head) * Dv + e0, x);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = 0.f;
-    }
+    float (&x)[8] = xs[k];
 
     if (kind <= 1) {
       const float* w = kind == 0 ? qw : kw;
@@ -148,6 +166,7 @@ append_general_kernel(const __grid_constant__ AppendArgs a) {
         store8(reinterpret_cast<CacheT*>(a.kc) + (int64_t)n * a.inst_stride + ((int64_t)head * a.capacity + slot) * Dk + e0, x);
       else
         store8(reinterpret_cast<CacheT*>(a.vc) + (int64_t)n * a.inst_stride_v + ((int64_t)head * a.capacity + slot) * Dv + e0, x);
+    }
     }
   }
   // the next kernel may start its set-up only as this CTA finishes: a long (many-wave) append
