@@ -6,6 +6,13 @@
  *   kv_attn_prefill              parallel prefill attention over the cache
  *   kv_attn_decode               single-token split-KV decode attention
  *   lmhead_argmax                tied lm_head GEMV + greedy argmax
+ * and the ones that extend them:
+ *   kv_attn_decode_step          the new token's append and its decode in one launch
+ *   kv_attn_decode_static        kv_attn_decode without a caller workspace (allocates nothing)
+ *   kv_attn_verify, kv_verify_commit   speculative-decoding verify block and its commit
+ *   lmhead_topk                  final RMSNorm + lm_head + the k best ids
+ * plus workspace sizers (kva_workspace_size and the per-call ones), error strings, the
+ * version, and the counter of in-kernel waits that gave up (kva_wait_timeouts).
  *
  * Conventions shared by every call
  *  - Ownership: every buffer belongs to the caller.  The library never allocates or
