@@ -198,12 +198,17 @@ void set_last_error(const char* msg) { std::snprintf(g_msg, sizeof(g_msg), "%s",
 // simple cost model and the cheapest wins:
 //   one wave:   fixed cost + max(all bytes / HBM bandwidth, one chunk / one CTA's share)
 //   more waves: waves x fixed cost + all bytes / HBM bandwidth + one chunk / share (the tail)
-// (fixed cost = a CTA's first DRAM round trip and its merge; a CTA's share of the bandwidth is
+//   plus, when instances are split, the merge (partials written, the counter, the last CTA's
+//   reads): a 65..80-key fp32 decode step is one chunk per head instead of 64 + 1..16 keys
+//   (6.0 instead of 7.7 us); a larger merge cost would also keep the 512-slot MLA step whole,
+//   which measured 35% slower
+// (fixed cost = a CTA's first DRAM round trip and its warps' merge; a CTA's share of the bandwidth is
 // at most what its ~100 KB of copies in flight sustain, so a small batch still spreads its keys)
 // Short contexts thus get one wave of whole-instance CTAs (no partials to merge); long, ragged
 // contexts get a few waves of equal chunks so that no CTA runs long past the others.
 int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len, double row_bytes, int ctas_per_sm) {
   constexpr double T_FIX_US = 3.0;           // per-wave fixed cost
+  constexpr double T_MERGE_US = 1.5;         // a split instance's partial write, counter and merge
   constexpr double BW = 6.5e6;               // bytes per microsecond (HBM)
   constexpr double CTA_BW = 1.0e5;           // bytes per microsecond one CTA sustains
   const double ROW = row_bytes;              // bytes per key and KV head (512: bf16 K + V, D = 128)
@@ -226,8 +231,9 @@ int decode_plan_chunk(const int32_t* lengths, int B, int Hkv, int max_len, doubl
     const double waves = std::ceil((double)ctas / slots);
     const double share = std::min(CTA_BW, BW / std::min((double)ctas, slots));
     const double chunk_t = (double)chunk * ROW / share;  // one CTA's chunk at its bandwidth share
-    const double t = waves <= 1.0 ? T_FIX_US + std::max(total_bytes / BW, chunk_t)
-                                  : waves * T_FIX_US + total_bytes / BW + chunk_t;   // + tail of the last wave
+    double t = waves <= 1.0 ? T_FIX_US + std::max(total_bytes / BW, chunk_t)
+                            : waves * T_FIX_US + total_bytes / BW + chunk_t;   // + tail of the last wave
+    if (chunk < max_len) t += T_MERGE_US;      // partials written, counted and merged
     if (t < best_t - 1e-9) { best_t = t; best_chunk = chunk; }
   }
   const int floor_chunk = (max_len + DECODE_MAX_CHUNKS - 1) / DECODE_MAX_CHUNKS;
