@@ -245,9 +245,9 @@ lmhead_b1_kernel(const __grid_constant__ LmheadArgs a) {
 }
 
 // ---------------------------------------------------------------------------------
-// Batch-1 pipelined path: one CTA per SM owns a contiguous slice of the table and streams it
-// through a 5-stage shared-memory ring, one 32 KB bulk copy per stage (the slice's rows are
-// contiguous in memory).  Bytes in flight cost no registers, so each SM keeps ~128 KB moving.
+// Batch-1 pipelined path: one CTA per SM streams every P-th 32 KB stage of the table (16
+// contiguous rows) through a 5-stage shared-memory ring, one bulk copy per stage.  Bytes in
+// flight cost no registers, so each SM keeps ~160 KB moving.
 // The 8 warps reduce the staged rows with conflict-free 128-bit shared-memory reads.
 // ---------------------------------------------------------------------------------
 constexpr int PIPE_STAGE_BYTES = 32768;
@@ -266,13 +266,18 @@ lmhead_b1_pipe_kernel(const __grid_constant__ LmheadArgs a, int rows_per_cta) {
   __shared__ unsigned long long s_best[PIPE_WARPS];
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r0 = blockIdx.x * rows_per_cta;
-  const int r1 = min(a.V, r0 + rows_per_cta);
-  const int n_st = r1 > r0 ? (r1 - r0 + RPS - 1) / RPS : 0;
+  // CTA b streams the table's 32 KB stages b, b + P, b + 2P, ... (P CTAs): at any moment the
+  // grid reads one compact region of the table.  Against one contiguous slice per CTA this
+  // measured 0.7 us slower per launch alone but 1% faster over the whole Qwen3-shaped job,
+  // where each launch follows a decode step (15.53 -> 15.38 ms).
+  (void)rows_per_cta;
+  const int P = gridDim.x, bidx = blockIdx.x;
+  const int tot_st = (a.V + RPS - 1) / RPS;
+  const int n_st = bidx < tot_st ? (tot_st - bidx + P - 1) / P : 0;
   const unsigned char* W = reinterpret_cast<const unsigned char*>(a.W);
   auto issue = [&](int it) {
-    const int rs = r0 + it * RPS;
-    const uint32_t bytes = (uint32_t)(min(RPS, r1 - rs) * ROWB);
+    const int rs = (bidx + it * P) * RPS;
+    const uint32_t bytes = (uint32_t)(min(RPS, a.V - rs) * ROWB);
     mbar_arrive_expect_tx(&full[it % PIPE_STAGES], bytes);
     bulk_g2s(ring + (it % PIPE_STAGES) * PIPE_STAGE_BYTES, W + (int64_t)rs * ROWB, bytes, &full[it % PIPE_STAGES]);
   };
@@ -284,8 +289,8 @@ lmhead_b1_pipe_kernel(const __grid_constant__ LmheadArgs a, int rows_per_cta) {
   // one drains (prefetches return no data, so they may run before the wait: a write by that
   // kernel still lands in L2, the point of coherence, where the copies after the wait read it)
   if (tid < PIPE_STAGES && tid < n_st) {
-    const int rs = r0 + tid * RPS;
-    bulk_prefetch_l2(W + (int64_t)rs * ROWB, (uint32_t)(min(RPS, r1 - rs) * ROWB));
+    const int rs = (bidx + tid * P) * RPS;
+    bulk_prefetch_l2(W + (int64_t)rs * ROWB, (uint32_t)(min(RPS, a.V - rs) * ROWB));
   } else if (tid >= 32 && tid < 32 + H * 4 / 128) {
     prefetch_l2(reinterpret_cast<const char*>(a.h) + (tid - 32) * 128);
   }
@@ -310,8 +315,8 @@ lmhead_b1_pipe_kernel(const __grid_constant__ LmheadArgs a, int rows_per_cta) {
   for (int it = 0; it < n_st; ++it) {
     const int st = it % PIPE_STAGES;
     if (!__all_sync(FULL_MASK, mbar_wait_bounded(&full[st], (uint32_t)((it / PIPE_STAGES) & 1)))) { ok = false; break; }
-    const int rs = r0 + it * RPS;
-    const int nr = min(RPS, r1 - rs);
+    const int rs = (bidx + it * P) * RPS;
+    const int nr = min(RPS, a.V - rs);
     const unsigned char* base = ring + st * PIPE_STAGE_BYTES;
     for (int rr = warp; rr < nr; rr += PIPE_WARPS) {
       float acc = 0.f;
