@@ -170,8 +170,14 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
     else if (tid < qlines + 2 * kvlines)
       prefetch_l2(reinterpret_cast<const char*>(st.v) + kvoff + (tid - qlines - kvlines) * 128);
   }
+  // Prefetch depth: each warp's first 2 x NS tiles.  Over the whole Qwen3-shaped job (28 layers,
+  // L = 513..768, each step after an lm_head launch) 0 / 1 / 3 / 6 / 8 / 12 / 16 tiles gave
+  // 15.72 / 15.55 / 15.39 / 15.29 / 15.29 / 15.65 / 16.02 ms: deeper, and the prefetches
+  // compete with the lm_head launch still draining.  Around the optimum, 5 / 6 / 7 tiles gave
+  // the step alone (back to back over rotating caches) 13.65 / 13.73 / 13.90 us and the job
+  // 15.31 / 15.26 / 15.25 ms.
   if (c == 0 && lane == 0)
-    for (int u = 0; u < NS; ++u) {
+    for (int u = 0; u < 2 * NS; ++u) {
       const int ks = (warp + u * WARPS) * KT;
       if (ks >= a.capacity) break;
       tc::tma_prefetch_l2_4d(&tmK, 0, ks, g, b); tc::tma_prefetch_l2_4d(&tmK, 64, ks, g, b);
