@@ -31,10 +31,21 @@ namespace {
 
 constexpr int TM = 128;                 // vocabulary rows per tile
 constexpr int KC = 64;                  // K elements per chunk (one 128-byte swizzle row)
-template <int BP> struct Stages { static constexpr int value = BP >= 128 ? 3 : 4; };   // fits 227 KB
 constexpr int THREADS = 192;
 constexpr int A_BYTES = TM * 128;       // 16 KB
 constexpr int MAX_N = 256;              // 2 * Bp
+constexpr int BAR_BYTES = 256;          // barriers (2 per stage + 4) and the TMEM address
+// Shared memory beside the ring: the padded logits tile, 64 bytes of gap, the barriers and the
+// slack that aligns the base to 1024.
+template <int BP> struct Fixed { static constexpr int value = TM * (BP + 1) * 4 + 64 + BAR_BYTES + 1024; };
+// Ring stages: as many [128 x 64] W chunks (with their h chunks) as fit in 227 KB, at most 8.
+// The table bytes in flight per SM set the kernel's rate (HBM-bound): at B = 64, 6 stages
+// instead of 4 took a launch from 56.4 to 54.5 us.
+template <int BP> struct Stages {
+  static constexpr int fit = (232448 - Fixed<BP>::value) / (A_BYTES + 2 * BP * 128);
+  static constexpr int value = fit < 8 ? fit : 8;
+  static_assert(fit >= 2, "ring stages");
+};
 
 // One CTA per padded batch row b: the row's final RMSNorm (when norm_w is given), then its
 // bf16 high half into row b and the residual's bf16 into row Bp + b (rows >= B are zeros).
@@ -278,7 +289,9 @@ int num_sms_tc() {
 template <int BP>
 cudaError_t launch_bp(const LmheadArgs& a, uint16_t* hb, cudaStream_t s) {
   constexpr int N = 2 * BP;
-  const int smem = Stages<BP>::value * (A_BYTES + N * 128) + TM * (BP + 1) * 4 + 64 + 128 + 1024;
+  constexpr int smem = Stages<BP>::value * (A_BYTES + N * 128) + Fixed<BP>::value;
+  static_assert(smem <= 232448, "shared memory per CTA");
+  static_assert((2 * Stages<BP>::value + 4) * 8 + 4 <= BAR_BYTES, "barrier area");
   static DeviceOnce configured;
   if (!configured.done()) {
     cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<BP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
