@@ -437,6 +437,30 @@ def test_lmhead_ties_lowest_id_last_row_and_clamp(K):
                 assert np.all(ids.cpu().numpy() == lo_row), (Wd.dtype, B, lo_val, ids.cpu().numpy())
 
 
+def test_lmhead_b1_pipeline_ties_across_stages_and_ctas(K):
+    """The batch-1 pipelined kernel (hidden 1024, bf16 table of the full vocabulary) hands its
+    16-row stages to the CTAs in turn (CTA c takes stages c, c + P, ...): exact ties between
+    rows that different CTAs reduce, or that one CTA reduces in different stages, go to the
+    lowest id, as do ties with the last row."""
+    torch = T()
+    H, V = 1024, 151936
+    P = torch.cuda.get_device_properties(0).multi_processor_count
+    W = torch.full((V, H), -0.01, device="cuda", dtype=torch.bfloat16)
+    h = torch.ones((1, H), device="cuda")
+    ws = torch.zeros(K.lmhead_workspace_bytes(1, H), dtype=torch.uint8, device="cuda")
+    ids = torch.empty((1,), dtype=torch.int32, device="cuda")
+    cases = [(20, 5000),                          # stages 1 and 312: different CTAs
+             (20, 20 + 16 * P),                   # one CTA, stages 1 and 1 + P
+             (20 + 16 * P * 3, 7),                # the higher id reduced first by its CTA
+             (V - 1, V - 2), (3, V - 1)]          # the last rows
+    for rows in cases:
+        W[list(rows)] = 0.01
+        K.lmhead_argmax(h, W, ids, ws)
+        torch.cuda.synchronize()
+        assert int(ids.cpu()[0]) == min(rows), (rows, int(ids.cpu()[0]))
+        W[list(rows)] = -0.01
+
+
 @pytest.mark.parametrize("mask", ["causal", "full"])
 def test_prefill_bf16_long_prompt_sampled_rows(K, mask):
     """A 4096-token prompt (32 row tiles, 32 key tiles per row tile under the full mask), two
