@@ -9,7 +9,7 @@
 //
 // Persistent CTAs walk vocabulary tiles of 128 rows (ascending within a CTA).  Warp roles:
 //   warp 0  TMA producer: W tile chunks [128 rows x 64] and B chunks [2*Bp rows x 64], 128-byte
-//           swizzled, into a 4-stage ring (W rows past the vocabulary read as zeros)
+//           swizzled, into a ring of as many stages as fit (W rows past the vocabulary read as zeros)
 //   warp 1  MMA issuer: 4 MMAs per 64-wide K chunk into one of two TMEM accumulators
 //   warps 2-5 epilogue: row r = TMEM lane r; logits go through a padded shared tile so that
 //           thread b scans the 128 rows of column b in order, keeping (max, lowest row)
