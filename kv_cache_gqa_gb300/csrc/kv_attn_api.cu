@@ -410,6 +410,17 @@ kva_status kv_attn_prefill(
   a.N = N; a.S = S; a.Hq = n_q_heads; a.Hkv = Hkv; a.D = D; a.capacity = cache.capacity;
   a.mask = (int)mask; a.inst_stride = cache.inst_stride;
   a.Dv = cache.head_dim_v; a.inst_stride_v = cache.inst_stride_v;
+  a.seg_table = 0;
+  if (a.segment && segment_host[0] >= 0 && segment_host[S - 1] < PREFILL_SEG_TABLE) {
+    // ids are non-decreasing (checked above): each id's slots are one contiguous run
+    for (int g = 0; g <= segment_host[S - 1]; ++g) a.seg_lo[g] = a.seg_hi[g] = 0;
+    for (int i = 0; i < S; ++i) {
+      const int g = segment_host[i];
+      if (i == 0 || segment_host[i - 1] != g) a.seg_lo[g] = i;
+      a.seg_hi[g] = i + 1;
+    }
+    a.seg_table = segment_host[S - 1] + 1;
+  }
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   a.scale_log2 = sc * 1.4426950408889634f;
   cudaError_t e;

@@ -193,6 +193,7 @@ cudaError_t launch_topk_rows(const float* logits, int B, int V, int k, void* wor
                              float* out_vals, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------
+constexpr int PREFILL_SEG_TABLE = 64;   // segment ids with bounds passed in the arguments
 struct PrefillArgs {
   const void* q;              // [N, S, Hq, D]
   const void* kc;
@@ -206,6 +207,11 @@ struct PrefillArgs {
   int64_t inst_stride_v;
   float scale_log2;
   int single_slot;            // tcgen05 form: one query tile per work unit (set by its launcher)
+  // Segment masks: slots [seg_lo[g], seg_hi[g]) hold segment id g, for ids g < seg_table
+  // (filled on the host from the segment ids' host mirror; 0 = no table).  A row whose id is
+  // in the table reads its window bounds here instead of bisecting the ids.
+  int seg_table;
+  int seg_lo[PREFILL_SEG_TABLE], seg_hi[PREFILL_SEG_TABLE];
 };
 int lmhead_max_hidden();
 cudaError_t launch_prefill(const PrefillArgs& a, kva_dtype dtype, cudaStream_t s);

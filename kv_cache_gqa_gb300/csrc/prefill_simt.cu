@@ -84,10 +84,12 @@ prefill_simt_kernel(const __grid_constant__ PrefillArgs a) {
     int lo = 0, hi = a.S;
     if (a.mask == KVA_MASK_CAUSAL) hi = i1;
     else if (a.mask == KVA_MASK_SEGMENT) {
-      lo = seg_lower(a.segment, a.S, a.segment[i0]);
-      hi = seg_upper(a.segment, a.S, a.segment[i1 - 1]);
+      const int g0 = a.segment[i0], g1 = a.segment[i1 - 1];   // bounds from the launch's table if there
+      lo = (unsigned)g0 < (unsigned)a.seg_table ? a.seg_lo[g0] : seg_lower(a.segment, a.S, g0);
+      hi = (unsigned)g1 < (unsigned)a.seg_table ? a.seg_hi[g1] : seg_upper(a.segment, a.S, g1);
     } else if (a.mask == KVA_MASK_CAUSAL_SEGMENT) {
-      hi = seg_upper(a.segment, a.S, a.segment[i1 - 1]);   // the last row's segment end
+      const int g1 = a.segment[i1 - 1];                        // the last row's segment end
+      hi = (unsigned)g1 < (unsigned)a.seg_table ? a.seg_hi[g1] : seg_upper(a.segment, a.S, g1);
     }
     s_range[0] = lo; s_range[1] = hi;
   }

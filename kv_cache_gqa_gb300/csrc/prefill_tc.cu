@@ -93,6 +93,14 @@ __device__ int seg_upper_tc(const int32_t* seg, int S, int key) {
   while (lo < hi) { const int mid = (lo + hi) >> 1; if (seg[mid] <= key) lo = mid + 1; else hi = mid; }
   return lo;
 }
+// First slot and one past the last slot of segment id g: from the launch's table when g is in
+// it, else by bisecting the ids (11 dependent loads for 1288 slots, on every unit's start).
+__device__ __forceinline__ int seg_first(const PrefillArgs& a, int g) {
+  return (unsigned)g < (unsigned)a.seg_table ? a.seg_lo[g] : seg_lower_tc(a.segment, a.S, g);
+}
+__device__ __forceinline__ int seg_end(const PrefillArgs& a, int g) {
+  return (unsigned)g < (unsigned)a.seg_table ? a.seg_hi[g] : seg_upper_tc(a.segment, a.S, g);
+}
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -211,10 +219,10 @@ __device__ __forceinline__ void tile_keys(const PrefillArgs& a, int i0, int i_la
   if (a.mask == KVA_MASK_CAUSAL) {
     hi = i_last + 1;
   } else if (a.mask == KVA_MASK_SEGMENT) {
-    lo = seg_lower_tc(a.segment, a.S, a.segment[i0]);
-    hi = seg_upper_tc(a.segment, a.S, a.segment[i_last]);
+    lo = seg_first(a, a.segment[i0]);
+    hi = seg_end(a, a.segment[i_last]);
   } else if (a.mask == KVA_MASK_CAUSAL_SEGMENT) {
-    hi = seg_upper_tc(a.segment, a.S, a.segment[i_last]);    // the last row's segment end
+    hi = seg_end(a, a.segment[i_last]);    // the last row's segment end
   }
 }
 
@@ -503,8 +511,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       if (row_ok) {
         if (a.mask == KVA_MASK_CAUSAL) { rlo = 0; rhi = i + 1; }
         else if (a.mask == KVA_MASK_FULL) { rlo = 0; rhi = a.S; }
-        else if (a.mask == KVA_MASK_CAUSAL_SEGMENT) { rlo = 0; rhi = seg_upper_tc(a.segment, a.S, a.segment[i]); }
-        else { const int sg = a.segment[i]; rlo = seg_lower_tc(a.segment, a.S, sg); rhi = seg_upper_tc(a.segment, a.S, sg); }
+        else if (a.mask == KVA_MASK_CAUSAL_SEGMENT) { rlo = 0; rhi = seg_end(a, a.segment[i]); }
+        else { const int sg = a.segment[i]; rlo = seg_first(a, sg); rhi = seg_end(a, sg); }
       }
       const int nk = tr.ntiles(s);
       float m = -INFINITY, l = 0.f;
