@@ -558,7 +558,7 @@ append_stream_kernel(const __grid_constant__ AppendArgs a, int tb, int stage_byt
       }
     }
     // the item's rows have landed and its angles are in the table, for every consumer warp (the
-    // verdict of the bounded wait is reduced over all of them, so they leave the loop together)
+    // outcome of the bounded wait is reduced over all of them, so they leave the loop together)
     const bool landed = mbar_wait_bounded(&full[st], (uint32_t)((k / STREAM_STAGES) & 1));
     if (!consumers_all(landed)) break;
     const unsigned char* stage = ring + (size_t)st * stage_bytes;
