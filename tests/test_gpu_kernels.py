@@ -253,6 +253,23 @@ def test_prefill_bf16_many_instances(K, mask, G):
     _prefill_case(K, 128, 300, mask, "bf16", G, seed=500 + G + len(mask), N=48, Hkv=2)
 
 
+@pytest.mark.parametrize("G", [1, 2])
+def test_prefill_bf16_split_last_round(K, G):
+    """Full-mask paired work units in two rounds over the SMs whose second round fills less
+    than half of them: that round runs as single query tiles (two per paired unit; with an odd
+    number of row tiles one of the halves is empty).  N is chosen from the GPU's SM count so
+    that the last round holds about a quarter of the CTAs."""
+    mask = "full"
+    torch = T()
+    P = torch.cuda.get_device_properties(0).multi_processor_count
+    nq, pairs = 3, 2                               # S = 300: 3 row tiles; 2 heads or 2 head pairs
+    per_inst = pairs * (nq if G == 2 else (nq + 1) // 2)
+    N = (P + P // 4) // per_inst + 1
+    units = per_inst * N
+    assert units > P and 2 * (units - P) <= P
+    _prefill_case(K, 128, 300, mask, "bf16", G, seed=700 + G + len(mask), N=N, Hkv=2)
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("mask", ["full", "segment"])
 def test_prefill_d72_mha_permuted(K, dt, mask):
