@@ -207,7 +207,6 @@ struct PrefillArgs {
   int64_t inst_stride_v;
   float scale_log2;
   int single_slot;            // tcgen05 form: one query tile per work unit (set by its launcher)
-  int split_last;             // tcgen05 form: the last round of units runs as single query tiles
   // Segment masks: slots [seg_lo[g], seg_hi[g]) hold segment id g, for ids g < seg_table
   // (filled on the host from the segment ids' host mirror; 0 = no table).  A row whose id is
   // in the table reads its window bounds here instead of bisecting the ids.

@@ -178,6 +178,11 @@ __host__ __device__ __forceinline__ Units unit_geometry_of(int N, int S, int Hq,
 __device__ __forceinline__ Units unit_geometry(const PrefillArgs& a) {
   return unit_geometry_of(a.N, a.S, a.Hq, a.Hkv, a.single_slot != 0);
 }
+// The r-th unit of CTA b out of P (snake order), or -1 past the end.
+__device__ __forceinline__ int unit_of(int r, int b, int P, int total) {
+  const int u = r * P + ((r & 1) ? (P - 1 - b) : b);
+  return u < total ? u : -1;
+}
 
 // The two slots of a unit: (query head, row tile) each, or an empty slot (qt < 0).
 struct Slots {
@@ -206,30 +211,6 @@ __device__ __forceinline__ Slots unit_slots(const PrefillArgs& a, const Units& g
     if (sl.qt[1] == sl.qt[0]) sl.qt[1] = -1;
   }
   return sl;
-}
-
-// The r-th unit of CTA b out of P (snake order) into sl; false past the end.  When the last
-// round of units fills at most half of the CTAs, each of its units runs as two single-tile
-// units on two CTAs (slot 1 moved into a unit of its own), so that round takes about as long
-// as one slot's work instead of a pair's while the other CTAs would idle.
-__device__ __forceinline__ bool unit_at(const PrefillArgs& a, const Units& g, int r, int b, int P, Slots& sl) {
-  const int pos = (r & 1) ? (P - 1 - b) : b;
-  const int last = (g.total - 1) / P;
-  if (a.split_last && r == last) {
-    const int half = pos & 1;
-    const int u = r * P + (pos >> 1);
-    if (u >= g.total) return false;
-    sl = unit_slots(a, g, u);
-    if (sl.qt[half] < 0) return false;
-    sl.h[0] = sl.h[half];
-    sl.qt[0] = sl.qt[half];
-    sl.qt[1] = -1;
-    return true;
-  }
-  const int u = r * P + pos;
-  if (u >= g.total) return false;
-  sl = unit_slots(a, g, u);
-  return true;
 }
 
 // Key range [lo, hi) that rows [i0, i_last] of a tile may see.
@@ -350,8 +331,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       int it = 0;                               // ring entries issued so far (all units)
       int nu = 0;                               // units begun so far
       for (int r = 0; ok; ++r, ++nu) {
-        Slots sl;
-        if (!unit_at(a, ug, r, b, P, sl)) break;
+        const int u = unit_of(r, b, P, ug.total);
+        if (u < 0) break;
+        const Slots sl = unit_slots(a, ug, u);
         const TileRanges tr = tile_ranges(a, sl);
         const int g = sl.h[0] / (a.Hq / a.Hkv);
         if (!gather) {
@@ -403,8 +385,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       int ks[2] = {0, 0};                       // key tiles of each slot so far
       int nus[2] = {0, 0};                      // units in which each slot was active so far
       for (int r = 0; ok; ++r) {
-        Slots sl;
-        if (!unit_at(a, ug, r, b, P, sl)) break;
+        const int u = unit_of(r, b, P, ug.total);
+        if (u < 0) break;
+        const Slots sl = unit_slots(a, ug, u);
         const TileRanges tr = tile_ranges(a, sl);
         const int s_total = tr.ntiles(0) + tr.ntiles(1);
         int s_issued = 0;
@@ -494,8 +477,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     int ks = 0, nus = 0, nu = 0;                // tiles and active units of this slot, units begun
     int r = 0;
     for (; ok; ++r, ++nu) {
-      Slots sl;
-      if (!unit_at(a, ug, r, b, P, sl)) break;
+      const int u = unit_of(r, b, P, ug.total);
+      if (u < 0) break;
+      const Slots sl = unit_slots(a, ug, u);
       const TileRanges tr = tile_ranges(a, sl);
       if (s == 1 && !tr.act1) continue;         // the slot is empty in this unit
       const int h = sl.h[s], n = sl.n;
@@ -704,8 +688,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       *s_abort = 1;
       // a wait gave up: this CTA's unfinished rows of this slot become NaN (plain stores)
       for (;; ++r) {
-        Slots sl;
-        if (!unit_at(a, ug, r, b, P, sl)) break;
+        const int u = unit_of(r, b, P, ug.total);
+        if (u < 0) break;
+        const Slots sl = unit_slots(a, ug, u);
         if (sl.qt[s] < 0) continue;
         const int i = sl.qt[s] * BM + t;
         if (i >= a.S) continue;
@@ -835,13 +820,6 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   const long long units = b.single_slot ? singles : paired;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)std::min<long long>(units, prefill_num_sms());
-  // several rounds of equal units (a full mask) whose last round leaves at least half of the
-  // CTAs idle: that round runs as single query tiles instead (two per paired unit).  Two
-  // 4096-token full-mask instances: 281 -> 268 us.  Causal units are not split: heaviest
-  // first in a snake order already leaves the lightest for the last round, and splitting them
-  // measured slower (139 -> 141 us).
-  const long long last = units - (units - 1) / grid * grid;
-  b.split_last = (a.mask == KVA_MASK_FULL && !b.single_slot && units > grid && 2 * last <= grid) ? 1 : 0;
   return launch_pdl(prefill_tc_kernel<D, DV, NST>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, b, mk, mv, mq, mo);
 }
 

@@ -254,11 +254,10 @@ def test_prefill_bf16_many_instances(K, mask, G):
 
 
 @pytest.mark.parametrize("G", [1, 2])
-def test_prefill_bf16_split_last_round(K, G):
-    """Full-mask paired work units in two rounds over the SMs whose second round fills less
-    than half of them: that round runs as single query tiles (two per paired unit; with an odd
-    number of row tiles one of the halves is empty).  N is chosen from the GPU's SM count so
-    that the last round holds about a quarter of the CTAs."""
+def test_prefill_bf16_two_rounds_last_quarter_full(K, G):
+    """Full-mask paired work units in two rounds over the SMs, the second filling about a
+    quarter of them (N chosen from the GPU's SM count); 3 row tiles, so for G = 1 (row tiles
+    t and n-1-t of one head) one unit per head holds a single tile."""
     mask = "full"
     torch = T()
     P = torch.cuda.get_device_properties(0).multi_processor_count
