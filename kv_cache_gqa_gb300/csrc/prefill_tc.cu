@@ -259,7 +259,25 @@ __device__ __forceinline__ TileRanges tile_ranges(const PrefillArgs& a, const Sl
   return tr;
 }
 
-template <int D, int DV, int NST>
+// A wait gave up: the CTA's unfinished rows of slot s (from its r-th unit on) become NaN, by
+// plain stores.  Out of line: it never runs in a healthy launch.
+template <int DV, bool GATHER>
+__device__ __noinline__ void nan_rows(const PrefillArgs& a, const Units& ug, int r, int b, int P, int s, int t) {
+  for (;; ++r) {
+    const int u = unit_of(r, b, P, ug.total);
+    if (u < 0) break;
+    const Slots sl = unit_slots(a, ug, u);
+    if (sl.qt[s] < 0) continue;
+    const int i = sl.qt[s] * BM + t;
+    if (i >= a.S) continue;
+    const int row = GATHER ? a.row_of_slot[i] : i;
+    if (row < 0 || row >= a.S) continue;
+    float* o = a.out + (((int64_t)sl.n * a.S + row) * a.Hq + sl.h[s]) * DV;
+    for (int d = 0; d < DV; ++d) o[d] = NAN;
+  }
+}
+
+template <int D, int DV, int NST, bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ,
@@ -291,7 +309,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   uint64_t* q_free = bars + 20;    // the unit's last Q K^T done: both Q tiles may be replaced
   uint32_t* s_taddr = reinterpret_cast<uint32_t*>(bars + 21);
   volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 22);
-  const bool gather = a.row_of_slot != nullptr;   // permuted rows: threads stage Q and store O
+  constexpr bool gather = GATHER;               // permuted rows: threads stage Q and store O
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Units ug = unit_geometry(a);
@@ -686,19 +704,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     }
     if (!ok) {
       *s_abort = 1;
-      // a wait gave up: this CTA's unfinished rows of this slot become NaN (plain stores)
-      for (;; ++r) {
-        const int u = unit_of(r, b, P, ug.total);
-        if (u < 0) break;
-        const Slots sl = unit_slots(a, ug, u);
-        if (sl.qt[s] < 0) continue;
-        const int i = sl.qt[s] * BM + t;
-        if (i >= a.S) continue;
-        const int row = gather ? a.row_of_slot[i] : i;
-        if (row < 0 || row >= a.S) continue;
-        float* o = a.out + (((int64_t)sl.n * a.S + row) * a.Hq + sl.h[s]) * DV;
-        for (int d = 0; d < DV; ++d) o[d] = NAN;
-      }
+      nan_rows<DV, GATHER>(a, ug, r, b, P, s, t);
     }
   }
 
@@ -785,18 +791,18 @@ int prefill_num_sms() {
   return n[dev];
 }
 
-template <int D, int DV, int NST>
-cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
+template <int D, int DV, int NST, bool GATHER>
+cudaError_t launch_g(const PrefillArgs& a, cudaStream_t s) {
   constexpr int SMEM = Layout<D, DV, NST>::SMEM;
   static_assert(SMEM <= 232448, "shared memory per CTA");
   static DeviceOnce configured;
   if (!configured.done()) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, DV, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, DV, NST, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     // the register split assumes the launch holds exactly REGS_LAUNCH per thread: with fewer,
     // the softmax warpgroups' setmaxnreg.inc could never be satisfied
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D, DV, NST>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D, DV, NST, GATHER>)) != cudaSuccess) return e;
     if (fa.numRegs != REGS_LAUNCH) return cudaErrorInvalidDeviceFunction;
     configured.mark();
   }
@@ -820,7 +826,7 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   const long long units = b.single_slot ? singles : paired;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)std::min<long long>(units, prefill_num_sms());
-  return launch_pdl(prefill_tc_kernel<D, DV, NST>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, b, mk, mv, mq, mo);
+  return launch_pdl(prefill_tc_kernel<D, DV, NST, GATHER>, dim3(grid), dim3(THREADS), (size_t)SMEM, s, b, mk, mv, mq, mo);
 }
 
 }  // namespace
@@ -828,6 +834,13 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
 bool prefill_tc_supports(int D, int Dv, kva_dtype dt) {
   const bool shapes = (Dv == D && (D == 64 || D == 72 || D == 128)) || (D == 192 && Dv == 128);
   return dt == KVA_BF16 && shapes && encode_fn() != nullptr;
+}
+
+// Permuted rows (row_of_slot) and token-order rows are separate instantiations, so that neither
+// kernel carries the other's Q staging and output path.
+template <int D, int DV, int NST>
+cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
+  return a.row_of_slot != nullptr ? launch_g<D, DV, NST, true>(a, s) : launch_g<D, DV, NST, false>(a, s);
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
